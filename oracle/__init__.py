@@ -1,0 +1,135 @@
+"""fp64 CPU oracle for causal sliding-window softmax attention (test infrastructure).
+
+Only the test suite, the package's ``smoke()`` check and the CPU-baseline leg of
+``bench.py`` may import this module.  The CUDA library and its Python binding
+never do; the two implementations share no code.
+
+The arithmetic lives in ``nc_oracle.c`` (plain loops, double precision, OpenMP
+over independent (batch, head) slices).  This module only compiles it on
+demand, converts inputs to contiguous float64 arrays and calls it through
+ctypes.  See ``nc_oracle.c`` for the definition, the pages it follows and the
+readings taken where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nc_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+WINDOW_FULL = -1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class OracleLib:
+    """ctypes view of one compiled oracle library (the default one, or a test's mutant)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        L = ctypes.c_long
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_fwd.restype = None
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_bwd.restype = None
+        lib.oracle_decode.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_int), dp, dp,
+                                      L, L, L, L, L, ctypes.c_double]
+        lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        self.lib = lib
+
+    def fwd(self, q, k, v, window: int, scale: float):
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, T, H, D = q.shape
+        assert k.shape == q.shape and v.shape == q.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, H, T), dtype=np.float64)
+        self.lib.oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, H, D,
+                            int(window), float(scale))
+        return o, lse
+
+    def bwd(self, q, k, v, dO, window: int, scale: float):
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        B, T, H, D = q.shape
+        dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+        self.lib.oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                            B, T, H, D, int(window), float(scale))
+        return dq, dk, dv
+
+    def decode(self, q, kcache, vcache, cache_lens, window: int, scale: float):
+        q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+        if hasattr(cache_lens, "detach"):
+            cache_lens = cache_lens.detach().to("cpu").numpy()
+        lens = np.ascontiguousarray(cache_lens, dtype=np.int32)
+        N, H, D = q.shape
+        Tmax = kc.shape[1]
+        assert kc.shape == (N, Tmax, H, D) and vc.shape == kc.shape and lens.shape == (N,)
+        o = np.empty_like(q)
+        lse = np.empty((N, H), dtype=np.float64)
+        rc = self.lib.oracle_decode(_ptr(q), _ptr(kc), _ptr(vc),
+                                    lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                    _ptr(o), _ptr(lse), N, Tmax, H, D, int(window), float(scale))
+        return o, lse, rc == 0
+
+
+def _load() -> OracleLib:
+    global _lib
+    if _lib is None:
+        _lib = OracleLib(build())
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Widen a torch tensor (any float dtype, any device) or array to contiguous float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    return int(_load().lib.oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().lib.oracle_set_num_threads(int(n))
+
+
+def fwd(q, k, v, window: int, scale: float):
+    """Exact attention forward.  q, k, v: [B, T, H, D].  Returns (o [B,T,H,D], lse [B,H,T])."""
+    return _load().fwd(q, k, v, window, scale)
+
+
+def bwd(q, k, v, dO, window: int, scale: float):
+    """Exact gradients of sum(O * dO) w.r.t. q, k, v.  Returns (dq, dk, dv), each [B, T, H, D]."""
+    return _load().bwd(q, k, v, dO, window, scale)
+
+
+def decode(q, kcache, vcache, cache_lens, window: int, scale: float):
+    """One-token decode.  q [N,H,D]; caches [N,Tmax,H,D]; cache_lens [N] (int).
+
+    Returns (o [N,H,D], lse [N,H], ok).  ok is False when some length is outside
+    [1, Tmax]; that sequence's rows are NaN.
+    """
+    return _load().decode(q, kcache, vcache, cache_lens, window, scale)

@@ -1,0 +1,231 @@
+/*
+ * fp64 CPU oracle for exact causal sliding-window softmax attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is compiled into liboracle.so and is
+ * called by the test suite, by the package's smoke check and by the CPU
+ * baseline leg of the benchmark.  The CUDA library never links, includes or
+ * calls it, and it shares no code, header or table with the CUDA sources.
+ *
+ * What it computes, and where that comes from:
+ *   - "nanochat GPT-2 speedrun" post (page 2; repeated on page 5), paragraph
+ *     on the biggest improvements: attention runs through FlashAttention-3
+ *     with its `window_size` argument, which gives alternating local/global
+ *     (sliding-window / full causal) attention per layer.  The pages give no
+ *     formula, so the oracle is the textbook definition of exact softmax
+ *     attention restricted to the causal window.
+ *   - "nanochat" walkthrough (page 4, inference paragraph closing the
+ *     pretraining section; page 1 launch post): inference uses an Engine with
+ *     a KV cache and a prefill/decode split, so decode is one query token
+ *     attending over the cached keys/values.
+ *
+ * Readings where the pages are silent (each one is restated in the design
+ * notes of the repository):
+ *   - visibility: key j is visible to query i iff j <= i and i - j < W, i.e.
+ *     the window counts W keys including the query's own position;
+ *   - W <= -1 (the value -1) or W >= T mean full causal attention;
+ *   - layout: q, k, v, o, dO, dq, dk, dv are contiguous [B, T, H, D];
+ *     lse is [B, H, T] and holds the natural log of the softmax normaliser
+ *     of the *scaled* scores;
+ *   - decode: the query of sequence n is position L_n - 1 whose key/value
+ *     already sit in the cache; cache rows max(0, L_n - W) .. L_n - 1 are
+ *     visible.
+ *
+ * Everything is computed from the definition in double precision with plain
+ * loops: no tiling, no online softmax, no reordering beyond the sums as
+ * written.  OpenMP only splits independent (b, h) slices across threads.
+ *
+ * Definition (per batch b, head h, query i, with V(i) the visible set):
+ *   s_ij  = scale * sum_d q_id k_jd                      j in V(i)
+ *   M_i   = max_j s_ij
+ *   lse_i = M_i + ln sum_j exp(s_ij - M_i)
+ *   p_ij  = exp(s_ij - lse_i)
+ *   o_i   = sum_j p_ij v_j
+ * Gradients of a loss L given dO = dL/dO:
+ *   dv_j  = sum_{i : j in V(i)} p_ij dO_i
+ *   dp_ij = dO_i . v_j
+ *   Delta_i = sum_j p_ij dp_ij
+ *   ds_ij = p_ij (dp_ij - Delta_i)
+ *   dq_i  = scale * sum_j ds_ij k_j
+ *   dk_j  = scale * sum_i ds_ij q_i
+ *
+ * Parity pins: every function here is pinned by the CPU tests against
+ * closed forms, invariants, brute-force enumeration, a library routine for
+ * the same definition and finite differences; none is "parity unpinned".
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Number of keys visible in a row of length T with window W (W <= 0 -> full). */
+static long eff_window(long W, long T) {
+    if (W <= 0 || W >= T) return T;
+    return W;
+}
+
+/* Element (b, t, h, d) of a contiguous [B, T, H, D] array. */
+static size_t idx_bthd(long b, long t, long h, long d, long T, long H, long D) {
+    return (((size_t)b * T + t) * H + h) * D + d;
+}
+
+/* Softmax weights of one query row over its visible keys.
+ * p[j - lo] = exp(s_ij - lse_i) for j in [lo, i]; returns lse_i. */
+static double row_probs(const double* q, const double* k, long b, long i, long h,
+                        long lo, long T, long H, long D, double scale, double* p) {
+    long n = i - lo + 1;
+    double M = -INFINITY;
+    for (long j = lo; j <= i; ++j) {
+        double s = 0.0;
+        for (long d = 0; d < D; ++d)
+            s += q[idx_bthd(b, i, h, d, T, H, D)] * k[idx_bthd(b, j, h, d, T, H, D)];
+        s *= scale;
+        p[j - lo] = s;
+        if (s > M) M = s;
+    }
+    double sum = 0.0;
+    for (long t = 0; t < n; ++t) sum += exp(p[t] - M);
+    double lse = M + log(sum);
+    for (long t = 0; t < n; ++t) p[t] = exp(p[t] - lse);
+    return lse;
+}
+
+/* Forward: o [B,T,H,D], lse [B,H,T]. */
+void oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
+                long B, long T, long H, long D, long window, double scale) {
+    long W = eff_window(window, T);
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)W);
+#pragma omp for schedule(dynamic, 1) collapse(2)
+        for (long b = 0; b < B; ++b)
+            for (long h = 0; h < H; ++h) {
+                for (long i = 0; i < T; ++i) {
+                    long lo = i - W + 1 < 0 ? 0 : i - W + 1;
+                    double l = row_probs(q, k, b, i, h, lo, T, H, D, scale, p);
+                    lse[((size_t)b * H + h) * T + i] = l;
+                    for (long d = 0; d < D; ++d) {
+                        double acc = 0.0;
+                        for (long j = lo; j <= i; ++j)
+                            acc += p[j - lo] * v[idx_bthd(b, j, h, d, T, H, D)];
+                        o[idx_bthd(b, i, h, d, T, H, D)] = acc;
+                    }
+                }
+            }
+        free(p);
+    }
+}
+
+/* Backward from the definition: dq, dk, dv [B,T,H,D] for upstream dO.
+ * The softmax weights are recomputed in fp64; nothing from a forward run is
+ * reused, so the gradients are those of the exact function. */
+void oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
+                double* dq, double* dk, double* dv,
+                long B, long T, long H, long D, long window, double scale) {
+    long W = eff_window(window, T);
+    size_t n_all = (size_t)B * T * H * D;
+    memset(dq, 0, sizeof(double) * n_all);
+    memset(dk, 0, sizeof(double) * n_all);
+    memset(dv, 0, sizeof(double) * n_all);
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)W);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)W);
+#pragma omp for schedule(dynamic, 1) collapse(2)
+        for (long b = 0; b < B; ++b)
+            for (long h = 0; h < H; ++h) {
+                for (long i = 0; i < T; ++i) {
+                    long lo = i - W + 1 < 0 ? 0 : i - W + 1;
+                    long n = i - lo + 1;
+                    (void)row_probs(q, k, b, i, h, lo, T, H, D, scale, p);
+                    /* dp_ij = dO_i . v_j and Delta_i = sum_j p_ij dp_ij */
+                    double delta = 0.0;
+                    for (long j = lo; j <= i; ++j) {
+                        double s = 0.0;
+                        for (long d = 0; d < D; ++d)
+                            s += dO[idx_bthd(b, i, h, d, T, H, D)] * v[idx_bthd(b, j, h, d, T, H, D)];
+                        dp[j - lo] = s;
+                        delta += p[j - lo] * s;
+                    }
+                    for (long t = 0; t < n; ++t) {
+                        long j = lo + t;
+                        double ds = p[t] * (dp[t] - delta);
+                        for (long d = 0; d < D; ++d) {
+                            dq[idx_bthd(b, i, h, d, T, H, D)] += scale * ds * k[idx_bthd(b, j, h, d, T, H, D)];
+                            dk[idx_bthd(b, j, h, d, T, H, D)] += scale * ds * q[idx_bthd(b, i, h, d, T, H, D)];
+                            dv[idx_bthd(b, j, h, d, T, H, D)] += p[t] * dO[idx_bthd(b, i, h, d, T, H, D)];
+                        }
+                    }
+                }
+            }
+        free(p);
+        free(dp);
+    }
+}
+
+/* Decode over a padded KV cache.
+ * q [N,H,D]; kc, vc [N,Tmax,H,D]; lens [N] with 1 <= lens[n] <= Tmax;
+ * o [N,H,D]; lse [N,H].  Returns 0, or -1 when a length is out of range
+ * (the rows of that sequence are then left as NaN). */
+int oracle_decode(const double* q, const double* kc, const double* vc, const int* lens,
+                  double* o, double* lse, long N, long Tmax, long H, long D, long window,
+                  double scale) {
+    int bad = 0;
+    for (long n = 0; n < N; ++n) {
+        long L = lens[n];
+        if (L < 1 || L > Tmax) {
+            bad = 1;
+            for (long h = 0; h < H; ++h) {
+                lse[n * H + h] = NAN;
+                for (long d = 0; d < D; ++d) o[(n * H + h) * D + d] = NAN;
+            }
+            continue;
+        }
+        long W = eff_window(window, L);
+        long lo = L - W;
+        for (long h = 0; h < H; ++h) {
+            double* p = (double*)malloc(sizeof(double) * (size_t)W);
+            double M = -INFINITY;
+            for (long j = lo; j < L; ++j) {
+                double s = 0.0;
+                for (long d = 0; d < D; ++d)
+                    s += q[(n * H + h) * D + d] * kc[idx_bthd(n, j, h, d, Tmax, H, D)];
+                s *= scale;
+                p[j - lo] = s;
+                if (s > M) M = s;
+            }
+            double sum = 0.0;
+            for (long t = 0; t < W; ++t) sum += exp(p[t] - M);
+            double l = M + log(sum);
+            lse[n * H + h] = l;
+            for (long t = 0; t < W; ++t) p[t] = exp(p[t] - l);
+            for (long d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (long j = lo; j < L; ++j) acc += p[j - lo] * vc[idx_bthd(n, j, h, d, Tmax, H, D)];
+                o[(n * H + h) * D + d] = acc;
+            }
+            free(p);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -1,0 +1,299 @@
+"""Pins for the fp64 CPU oracle, checked against things other than itself.
+
+Each test ties the oracle to something the definition of windowed causal
+softmax attention fixes on its own: a hand-worked example, closed forms,
+invariants, brute-force dense enumeration, a library routine for the same
+definition (torch SDPA in fp64 with an explicit band mask) and finite
+differences of the forward.  A mistake in the oracle (a dropped term, a wrong
+sign, an off-by-one window, a transposed operand) fails at least one of them;
+``test_oracle_mutants.py`` plants such mistakes to show it.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from causal_sliding_window_fwd_b300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _val(x):
+    if isinstance(x, str):
+        return eval(x, {"ln3": math.log(3.0), "ln4": math.log(4.0), "ln5": math.log(5.0)})
+    return float(x)
+
+
+def _arr(rows):
+    return np.array([[_val(c) for c in r] for r in rows], dtype=np.float64)
+
+
+def _bthd(rows):
+    a = _arr(rows)
+    return a.reshape(1, a.shape[0], 1, a.shape[1])
+
+
+# ---------------------------------------------------------------- golden
+
+
+def test_hand_worked_example(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "hand_window2.json")))
+    q, k, v, dO = (_bthd(g[n]) for n in ("q", "k", "v", "dO"))
+    o, lse = oracle_mod.fwd(q, k, v, g["window"], g["scale"])
+    np.testing.assert_allclose(o[0, :, 0, :], _arr(g["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], [_val(x) for x in g["lse"]], rtol=0, atol=1e-12)
+    dq, dk, dv = oracle_mod.bwd(q, k, v, dO, g["window"], g["scale"])
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got[0, :, 0, :], _arr(g[name]), rtol=0, atol=1e-12, err_msg=name)
+    # decode over a cache of the same three rows, length 3, query q2
+    od, lsed, ok = oracle_mod.decode(q[:, 2], k, v, np.array([3]), g["window"], g["scale"])
+    assert ok
+    np.testing.assert_allclose(od[0, 0], _arr(g["o"])[2], rtol=0, atol=1e-12)
+    assert abs(lsed[0, 0] - math.log(5.0)) < 1e-12
+
+
+# ---------------------------------------------------------------- closed forms
+
+
+def test_window_one_is_identity(oracle_mod):
+    B, T, H, D = 2, 9, 3, 5
+    q, k, v, dO = (_rand((B, T, H, D), s) for s in range(4))
+    o, lse = oracle_mod.fwd(q, k, v, 1, 0.7)
+    np.testing.assert_array_equal(o, v)
+    np.testing.assert_allclose(lse, 0.7 * np.einsum("bthd,bthd->bht", q, k), rtol=1e-14, atol=1e-14)
+    dq, dk, dv = oracle_mod.bwd(q, k, v, dO, 1, 0.7)
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_array_equal(dv, dO)
+
+
+@pytest.mark.parametrize("window", [2, 7, 40, -1])
+def test_first_query_sees_only_itself(oracle_mod, window):
+    B, T, H, D = 1, 12, 2, 6
+    q, k, v = (_rand((B, T, H, D), 10 + s) for s in range(3))
+    o, lse = oracle_mod.fwd(q, k, v, window, 0.3)
+    np.testing.assert_array_equal(o[:, 0], v[:, 0])
+    np.testing.assert_allclose(lse[:, :, 0], 0.3 * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0]), atol=1e-14)
+
+
+@pytest.mark.parametrize("window", [1, 3, 8, 100])
+def test_identical_keys_give_uniform_weights(oracle_mod, window):
+    B, T, H, D = 1, 11, 2, 4
+    q, v = _rand((B, T, H, D), 20), _rand((B, T, H, D), 21)
+    c = _rand((H, D), 22)
+    k = np.broadcast_to(c, (B, T, H, D)).copy()
+    o, lse = oracle_mod.fwd(q, k, v, window, 0.5)
+    for i in range(T):
+        lo = max(0, i - window + 1)
+        n = i - lo + 1
+        np.testing.assert_allclose(o[:, i], v[:, lo:i + 1].mean(axis=1), atol=1e-13)
+        expect = 0.5 * np.einsum("bhd,hd->bh", q[:, i], c) + math.log(n)
+        np.testing.assert_allclose(lse[:, :, i], expect, atol=1e-13)
+
+
+# ---------------------------------------------------------------- invariants
+
+
+@pytest.mark.parametrize("window", [1, 4, 13, -1])
+def test_rows_sum_to_one(oracle_mod, window):
+    B, T, H, D = 2, 13, 2, 3
+    q, k = _rand((B, T, H, D), 30), _rand((B, T, H, D), 31)
+    o, _ = oracle_mod.fwd(q, k, np.ones((B, T, H, D)), window, 1.3)
+    np.testing.assert_allclose(o, 1.0, atol=1e-14)
+
+
+def test_window_at_least_T_is_full_causal(oracle_mod):
+    B, T, H, D = 1, 10, 2, 4
+    q, k, v, dO = (_rand((B, T, H, D), 40 + s) for s in range(4))
+    ref_o, ref_l = oracle_mod.fwd(q, k, v, -1, 0.5)
+    ref_g = oracle_mod.bwd(q, k, v, dO, -1, 0.5)
+    for w in (T, T + 5, 10 ** 6):
+        o, l = oracle_mod.fwd(q, k, v, w, 0.5)
+        np.testing.assert_array_equal(o, ref_o)
+        np.testing.assert_array_equal(l, ref_l)
+        for a, b in zip(oracle_mod.bwd(q, k, v, dO, w, 0.5), ref_g):
+            np.testing.assert_array_equal(a, b)
+    # and a window of T-1 differs (the last row loses key 0)
+    o, _ = oracle_mod.fwd(q, k, v, T - 1, 0.5)
+    assert not np.allclose(o[:, T - 1], ref_o[:, T - 1])
+    np.testing.assert_array_equal(o[:, :T - 1], ref_o[:, :T - 1])
+
+
+def test_key_shift_invariance(oracle_mod):
+    B, T, H, D = 1, 9, 2, 5
+    q, k, v = (_rand((B, T, H, D), 50 + s) for s in range(3))
+    c = _rand((H, D), 53)
+    o1, l1 = oracle_mod.fwd(q, k, v, 4, 0.8)
+    o2, l2 = oracle_mod.fwd(q, k + c, v, 4, 0.8)
+    np.testing.assert_allclose(o2, o1, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, 0.8 * np.einsum("bthd,hd->bht", q, c), atol=1e-12)
+
+
+def test_window_edge_is_exact(oracle_mod):
+    """Key i-W+1 is seen by query i and key i-W is not."""
+    B, T, H, D, W = 1, 12, 1, 3, 4
+    q, k, v = (_rand((B, T, H, D), 60 + s) for s in range(3))
+    i = 9
+    o0, _ = oracle_mod.fwd(q, k, v, W, 1.0)
+    v_out = v.copy(); v_out[:, i - W] += 100.0
+    o1, _ = oracle_mod.fwd(q, k, v_out, W, 1.0)
+    np.testing.assert_array_equal(o1[:, i], o0[:, i])
+    v_in = v.copy(); v_in[:, i - W + 1] += 100.0
+    o2, _ = oracle_mod.fwd(q, k, v_in, W, 1.0)
+    assert np.abs(o2[:, i] - o0[:, i]).max() > 1e-3
+    v_fut = v.copy(); v_fut[:, i + 1] += 100.0
+    o3, _ = oracle_mod.fwd(q, k, v_fut, W, 1.0)
+    np.testing.assert_array_equal(o3[:, i], o0[:, i])
+
+
+@pytest.mark.parametrize("window", [1, 3, 6, -1])
+def test_gradient_sums(oracle_mod, window):
+    B, T, H, D = 2, 10, 2, 4
+    q, k, v, dO = (_rand((B, T, H, D), 70 + s) for s in range(4))
+    dq, dk, dv = oracle_mod.bwd(q, k, v, dO, window, 0.6)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=1), dO.sum(axis=1), atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [1, 5, 64, -1])
+def test_decode_equals_last_forward_row(oracle_mod, window):
+    N, Tmax, H, D = 3, 20, 2, 8
+    kc, vc = _rand((N, Tmax, H, D), 80), _rand((N, Tmax, H, D), 81)
+    qs = _rand((N, Tmax, H, D), 82)
+    lens = np.array([1, 7, 20], dtype=np.int32)
+    q_dec = np.stack([qs[n, lens[n] - 1] for n in range(N)])
+    o, lse, ok = oracle_mod.decode(q_dec, kc, vc, lens, window, 0.35)
+    assert ok
+    for n in range(N):
+        L = lens[n]
+        of, lf = oracle_mod.fwd(qs[n:n + 1, :L], kc[n:n + 1, :L], vc[n:n + 1, :L], window, 0.35)
+        np.testing.assert_allclose(o[n], of[0, L - 1], atol=1e-13)
+        np.testing.assert_allclose(lse[n], lf[0, :, L - 1], atol=1e-13)
+
+
+def test_decode_ignores_slots_outside_window_and_length(oracle_mod):
+    N, Tmax, H, D, W = 2, 16, 1, 4, 5
+    q = _rand((N, H, D), 90)
+    kc, vc = _rand((N, Tmax, H, D), 91), _rand((N, Tmax, H, D), 92)
+    lens = np.array([9, 16], dtype=np.int32)
+    o0, l0, _ = oracle_mod.decode(q, kc, vc, lens, W, 0.5)
+    kp, vp = kc.copy(), vc.copy()
+    for n, L in enumerate(lens):
+        kp[n, L:] = np.nan; vp[n, L:] = np.nan
+        kp[n, :L - W] = np.nan; vp[n, :L - W] = np.nan
+    o1, l1, _ = oracle_mod.decode(q, kp, vp, lens, W, 0.5)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+
+
+def test_decode_bad_length_is_reported(oracle_mod):
+    q = _rand((2, 1, 4), 95)
+    kc, vc = _rand((2, 8, 1, 4), 96), _rand((2, 8, 1, 4), 97)
+    o, lse, ok = oracle_mod.decode(q, kc, vc, np.array([0, 8], dtype=np.int32), -1, 0.5)
+    assert not ok
+    assert np.isnan(o[0]).all() and np.isnan(lse[0]).all()
+    assert np.isfinite(o[1]).all()
+
+
+# ---------------------------------------------------------------- brute force
+
+
+def _dense_masked_reference(q, k, v, window, scale):
+    """Dense T x T enumeration with an explicit 0/1 visibility matrix (pure Python loops)."""
+    B, T, H, D = q.shape
+    W = T if window <= 0 else min(window, T)
+    mask = [[1 if (j <= i and i - j < W) else 0 for j in range(T)] for i in range(T)]
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            for i in range(T):
+                logits = [scale * sum(q[b, i, h, d] * k[b, j, h, d] for d in range(D)) if mask[i][j] else -math.inf
+                          for j in range(T)]
+                m = max(logits)
+                z = sum(math.exp(x - m) for x in logits)
+                lse[b, h, i] = m + math.log(z)
+                for d in range(D):
+                    o[b, i, h, d] = sum(math.exp(logits[j] - m) / z * v[b, j, h, d] for j in range(T))
+    return o, lse
+
+
+@pytest.mark.parametrize("T,D,window", [(1, 1, 1), (5, 3, 2), (8, 4, 3), (8, 2, 8), (7, 4, -1)])
+def test_brute_force_tiny(oracle_mod, T, D, window):
+    B, H = 2, 2
+    q, k, v = (_rand((B, T, H, D), 100 + s) for s in range(3))
+    o, lse = oracle_mod.fwd(q, k, v, window, 0.9)
+    ob, lb = _dense_masked_reference(q, k, v, window, 0.9)
+    np.testing.assert_allclose(o, ob, atol=1e-13)
+    np.testing.assert_allclose(lse, lb, atol=1e-13)
+
+
+# ---------------------------------------------------------------- library routine
+
+
+def _band_mask(T, window):
+    W = T if window <= 0 else min(window, T)
+    i = torch.arange(T).view(T, 1)
+    j = torch.arange(T).view(1, T)
+    return (j <= i) & (i - j < W)
+
+
+@pytest.mark.parametrize("T,D,window", [(16, 8, 1), (33, 16, 5), (40, 8, 40), (64, 16, 17), (29, 8, -1)])
+def test_matches_torch_sdpa_fp64(oracle_mod, T, D, window):
+    B, H = 2, 3
+    scale = 1.0 / math.sqrt(D)
+    q, k, v, dO = (torch.from_numpy(_rand((B, T, H, D), 110 + s)) for s in range(4))
+    qt, kt, vt = (x.transpose(1, 2).clone().requires_grad_(True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=_band_mask(T, window), scale=scale)
+    out.backward(dO.transpose(1, 2))
+    logits = scale * qt.detach() @ kt.detach().transpose(-1, -2)
+    lse_ref = torch.logsumexp(logits.masked_fill(~_band_mask(T, window), -math.inf), dim=-1)
+
+    o, lse = oracle_mod.fwd(q, k, v, window, scale)
+    np.testing.assert_allclose(o, out.detach().transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref.numpy(), atol=1e-12)
+    dq, dk, dv = oracle_mod.bwd(q, k, v, dO, window, scale)
+    np.testing.assert_allclose(dq, qt.grad.transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.transpose(1, 2).numpy(), atol=1e-12)
+
+
+def test_matches_torch_sdpa_on_bf16_workload(oracle_mod):
+    """The tiny workload's own bf16 tensors, widened exactly to fp64."""
+    call = workloads.TINY.calls[0]
+    q, k, v, dO = workloads.make_qkvdo(call, "cpu")
+    q64, k64, v64 = (x.double().transpose(1, 2) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q64, k64, v64, attn_mask=_band_mask(call.T, call.window), scale=call.scale)
+    o, _ = oracle_mod.fwd(q, k, v, call.window, call.scale)
+    np.testing.assert_allclose(o, ref.transpose(1, 2).numpy(), atol=1e-12)
+
+
+# ---------------------------------------------------------------- finite differences
+
+
+@pytest.mark.parametrize("window", [1, 3, 8])
+def test_backward_matches_finite_differences(oracle_mod, window):
+    """Central differences of L = sum(O * G) from the oracle's own forward."""
+    B, T, H, D = 1, 8, 1, 4
+    scale = 0.5
+    base = [_rand((B, T, H, D), 120 + s) for s in range(3)]
+    G = _rand((B, T, H, D), 123)
+    grads = oracle_mod.bwd(*base, G, window, scale)
+    eps = 1e-6
+    rng = np.random.default_rng(7)
+    for which in range(3):
+        for _ in range(12):
+            idx = (0, int(rng.integers(T)), 0, int(rng.integers(D)))
+            plus = [x.copy() for x in base]; plus[which][idx] += eps
+            minus = [x.copy() for x in base]; minus[which][idx] -= eps
+            lp = (oracle_mod.fwd(*plus, window, scale)[0] * G).sum()
+            lm = (oracle_mod.fwd(*minus, window, scale)[0] * G).sum()
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grads[which][idx]) < 1e-7, (which, idx, fd, grads[which][idx])
