@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark: sliding-window causal attention forward+backward on one B300.
+
+One step = forward + backward of the depth-20-like training layer pair
+(B=16, T=2048, H=10, D=128; one call with window 1024 and one full-causal
+call), inputs resident in HBM.  The metric is useful TFLOP/s: 14 * D flops
+per in-window (query, key) pair (4*D forward, 10*D backward), divided by the
+device time of the step.  Single-token KV-cache decode (64 sequences, lengths
+U[256, 8192], windows 1024 and full) is timed after the step loop and
+reported in its own object.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line on rank 0.  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas, weak scaling); the step time is
+the maximum over ranks.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from causal_sliding_window_fwd_b300 import workloads  # noqa: E402
+
+METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def useful_flops(call) -> float:
+    return 14.0 * call.D * call.B * call.H * workloads.pairs_in_window(call.T, call.window)
+
+
+def fwd_flops(call) -> float:
+    return 4.0 * call.D * call.B * call.H * workloads.pairs_in_window(call.T, call.window)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+
+def oracle_sample_time(max_slices: int | None = None, rows: int = 2048):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the layer pair.
+
+    The sample is the first `s` heads of batch row 0 of each call, restricted
+    to the first `rows` positions of the sequence (a causal prefix is itself a
+    valid problem of length `rows`), forward + backward, both windows.
+    Returns (useful TFLOP/s, seconds, cores, description).
+    """
+    import oracle
+    oracle.build()
+    s = max_slices or min(oracle.num_threads(), 10)
+    cores = min(oracle.num_threads(), s)  # OpenMP splits the (b, h) slices
+    flops, secs = 0.0, 0.0
+    for call in workloads.D20_PAIR.calls:
+        T = min(rows, call.T)
+        sub = workloads.AttnCall(1, T, s, call.D, call.window, call.seed)
+        q, k, v, dO = (x[:1, :T, :s].contiguous() for x in workloads.make_qkvdo(
+            workloads.AttnCall(1, call.T, call.H, call.D, call.window, call.seed), "cpu"))
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, call.window, call.scale)
+        oracle.bwd(q, k, v, dO, call.window, call.scale)
+        secs += time.perf_counter() - t0
+        flops += useful_flops(sub)
+    desc = (f"fp64 oracle fwd+bwd on {s} (b,h) slices x first {min(rows, 2048)} rows of each call of the "
+            f"layer pair (D=128, W=1024 and full), {cores} OpenMP threads")
+    return flops / secs / 1e12, secs, cores, desc
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, dist: Dist):
+    from causal_sliding_window_fwd_b300 import nc_attn
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    peaks, peak_kind = load_peaks()
+    wl = workloads.D20_PAIR
+    calls = wl.calls
+    stream = torch.cuda.Stream(dev)
+
+    bufs = []
+    for call in calls:
+        q, k, v, dO = workloads.make_qkvdo(call, dev)
+        B, T, H, D = call.shape
+        bufs.append(dict(q=q, k=k, v=v, dO=dO, o=torch.empty_like(q),
+                         lse=torch.empty((B, H, T), dtype=torch.float32, device=dev),
+                         dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
+                         ws=torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8,
+                                        device=dev)))
+    torch.cuda.synchronize()
+
+    def step(ev_list=None):
+        for call, b in zip(calls, bufs):
+            if ev_list is not None:
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+            nc_attn.nc_attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], call.window, call.scale, stream)
+            if ev_list is not None:
+                e1.record(stream)
+            nc_attn.nc_attn_bwd(b["q"], b["k"], b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"],
+                                call.window, call.scale, b["ws"], stream)
+            if ev_list is not None:
+                e2.record(stream)
+                ev_list.append((call, e0, e1, e2))
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    assert nc_attn.nc_get_device_error(stream) == 0
+
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dist.local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = nc_attn.nc_launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = []
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            step(evs)
+        end.record(stream)
+    torch.cuda.synchronize()
+    launches = nc_attn.nc_launch_count() - launches0
+    dist.barrier()
+    clk = clocks.stop()
+    err = nc_attn.nc_get_device_error(stream)
+    if err != 0:
+        raise RuntimeError(f"device error {err} during the timed region")
+    ms_total = start.elapsed_time(end)
+    ms_total = dist.max(ms_total)
+    ms_per_step = ms_total / args.steps
+    flops_step = sum(useful_flops(c) for c in calls)
+    value = dist.world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+
+    fwd_ms = sum(e0.elapsed_time(e1) for _, e0, e1, _ in evs)
+    bwd_ms = sum(e1.elapsed_time(e2) for _, _, e1, e2 in evs)
+    fwd_fl = sum(fwd_flops(c) for c, *_ in evs)
+    bwd_fl = sum(useful_flops(c) - fwd_flops(c) for c, *_ in evs)
+    bwd_tf = bwd_fl / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = fwd_fl / (fwd_ms * 1e-3) / 1e12
+    peak_tf = peaks["bf16_tflops"]
+    per_call = []
+    for call in calls:
+        f = [e0.elapsed_time(e1) for c, e0, e1, _ in evs if c == call]
+        b = [e1.elapsed_time(e2) for c, _, e1, e2 in evs if c == call]
+        per_call.append({"window": call.window, "fwd_ms": statistics.median(f), "bwd_ms": statistics.median(b),
+                         "fwd_tflops": fwd_flops(call) / (statistics.median(f) * 1e-3) / 1e12,
+                         "bwd_tflops": (useful_flops(call) - fwd_flops(call)) / (statistics.median(b) * 1e-3) / 1e12})
+
+    dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    roofline = {"bound": "tensor", "kernel": "nc_attn_bwd (all kernels of the call)" if dominant == "bwd"
+                else "nc_attn_fwd", "achieved": round(dom_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(dom_tf / peak_tf, 4), "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                "traffic": None,
+                "fwd": {"achieved": round(fwd_tf, 2), "frac": round(fwd_tf / peak_tf, 4)},
+                "bwd": {"achieved": round(bwd_tf, 2), "frac": round(bwd_tf / peak_tf, 4)},
+                "step_frac": round(value / dist.world / peak_tf, 4)}
+
+    out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic N(0,1) bf16, seeded",
+           "config": {"workload": wl.name, "model": "depth-20-like attention layer pair (fwd+bwd)",
+                      "global_batch": 16 * dist.world, "seq_len": 2048, "heads": 10, "head_dim": 128,
+                      "windows": [c.window for c in calls], "parallelism": f"replicas x{dist.world}",
+                      "l2": "inputs larger than L2 (q,k,v,dO = 335 MB per call, 671 MB per step)",
+                      "per_call": per_call},
+           "gpu_launches": int(launches), "clocks": clk, "roofline": roofline}
+
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(calls, bufs, stream, dist, nc_attn, args)
+    if not args.no_decode:
+        out["decode"] = run_decode(dev, stream, nc_attn, peaks, peak_kind)
+    return out
+
+
+def run_e2e(calls, bufs, stream, dist, nc_attn, args):
+    """Same metric through the C-ABI calls with host buffers: H2D of the step's inputs
+    from pinned memory, fwd + bwd, D2H of o, lse, dq, dk, dv, every step."""
+    host_in, host_out = [], []
+    for b in bufs:
+        host_in.append({k: b[k].cpu().pin_memory() for k in ("q", "k", "v", "dO")})
+        host_out.append({k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory()
+                         for k in ("o", "lse", "dq", "dk", "dv")})
+    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
+    d2h = sum(t.numel() * t.element_size() for d in host_out for t in d.values())
+
+    def step():
+        for call, b, hi, ho in zip(calls, bufs, host_in, host_out):
+            for k in ("q", "k", "v", "dO"):
+                b[k].copy_(hi[k], non_blocking=True)
+            nc_attn.nc_attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], call.window, call.scale, stream)
+            nc_attn.nc_attn_bwd(b["q"], b["k"], b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"],
+                                call.window, call.scale, b["ws"], stream)
+            for k in ("o", "lse", "dq", "dk", "dv"):
+                ho[k].copy_(b[k], non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(s.elapsed_time(e)) / steps
+    flops = sum(useful_flops(c) for c in calls)
+    return {"value": round(dist.world * flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def decode_bytes(lens, wl, window):
+    W = wl.Tmax if window <= 0 else window
+    rows = sum(min(int(L), W) for L in lens.tolist())
+    return rows * wl.H * wl.D * 2 * 2 + wl.N * wl.H * wl.D * 2 * 2 + wl.N * wl.H * 4 + wl.N * 4
+
+
+def run_decode(dev, stream, nc_attn, peaks, peak_kind):
+    wl = workloads.DECODE
+    q, kc, vc, lens = workloads.make_decode(wl, dev)
+    ws = torch.empty(nc_attn.nc_attn_decode_workspace_bytes(wl.N, wl.Tmax, wl.H, wl.D), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty((wl.N, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.N, wl.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {"workload": wl.name, "l2": "flushed (256 MB write) before every timed call"}
+    launches_per = None
+    for window in wl.windows:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                nc_attn.nc_attn_decode(q, kc, vc, lens, o, lse, window, wl.scale, ws, stream)
+            times = []
+            for _ in range(20):
+                flush.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0 = nc_attn.nc_launch_count()
+                s.record(stream)
+                nc_attn.nc_attn_decode(q, kc, vc, lens, o, lse, window, wl.scale, ws, stream)
+                e.record(stream)
+                launches_per = nc_attn.nc_launch_count() - c0
+                e.synchronize()
+                times.append(s.elapsed_time(e))
+        ms = statistics.median(times)
+        nbytes = decode_bytes(lens.cpu(), wl, window)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        key = "w1024" if window > 0 else "full"
+        res[key] = {"window": window, "us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+                    "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                 "frac_vs_8TBs_nominal": round(gbs / 8000.0, 4),
+                                 "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None}}
+    res["gpu_launches_per_call"] = launches_per
+    assert nc_attn.nc_get_device_error(stream) == 0
+    return res
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+
+def run_reference(args, dist: Dist):
+    cfg = {"workload": workloads.D20_PAIR.name, "model": "depth-20-like attention layer pair (fwd+bwd)",
+           "global_batch": 16, "seq_len": 2048, "heads": 10, "head_dim": 128,
+           "windows": [c.window for c in workloads.D20_PAIR.calls], "parallelism": "host cores"}
+    # keep the whole run to a few minutes: about 7 s per full-length step on 8 cores
+    rows = 2048 if args.steps <= 20 else max(256, int(2048 * math.sqrt(20.0 / args.steps)) // 128 * 128)
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample_time(rows=rows)
+    vals, secs_all = [], []
+    cores, desc = None, None
+    for _ in range(args.steps):
+        v, secs, cores, desc = oracle_sample_time(rows=rows)
+        vals.append(v)
+        secs_all.append(secs)
+    value = statistics.median(vals)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(statistics.median(secs_all) * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic N(0,1) bf16 widened to fp64, seeded", "config": cfg, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, dist)), flush=True)
+        return 0
+    dist.init("nccl")
+    out = run_ours(args, dist)
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        v, secs, cores, desc = oracle_sample_time()
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+                               "seconds": round(secs, 2)}
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

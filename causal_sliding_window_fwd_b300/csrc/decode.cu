@@ -1,0 +1,228 @@
+// Single-token decode over a padded KV cache: split-K partial softmax over
+// chunks of visible cache rows, then a per-(sequence, head) combine.
+//
+// Operation: the "nanochat" walkthrough (page 4, close of the pretraining
+// section; page 1 launch post) runs inference through an Engine with a KV
+// cache and a prefill/decode split; decode is one query token attending over
+// the cached keys/values, restricted to the layer's sliding window
+// ("nanochat GPT-2 speedrun" post, page 2, FlashAttention-3 window_size).
+//
+// This path is bound by HBM bandwidth (about one flop per byte), so it runs
+// on CUDA cores: a cache row of one token holds all H heads contiguously
+// (H * D bf16), each warp streams one head's 256-byte (D = 128) slice of
+// consecutive rows with 16-byte vector loads, and a CTA covers every head of
+// a chunk of rows, so the CTA reads whole contiguous rows.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "nc_attn.h"
+#include "nc_decode.h"
+#include "nc_kernels.h"
+#include "nc_ptx.cuh"
+
+namespace nc {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Visible cache rows of a sequence of length L: [L - W', L) with W' = min(W, L).
+__device__ __forceinline__ int visible_lo(int L, int window) {
+    return (window <= 0 || window >= L) ? 0 : L - window;
+}
+
+// One CTA = (split s, sequence n).  Warp w handles heads w, w + nwarps, ...
+// Lanes are grouped G = D / 8 per token; a warp handles 32 / G tokens per step.
+template <int D>
+__global__ void __launch_bounds__(512)
+decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
+                    float* __restrict__ part_ml, float* __restrict__ part_o, int N, int Tmax, int H,
+                    int window, float scale_log2, int n_splits, int chunk) {
+    constexpr int G = D / 8;          // lanes per token row of one head
+    constexpr int TPS = 32 / G;       // tokens per warp step
+    constexpr int U = 4;              // steps in flight per iteration
+    const int s = blockIdx.x, n = blockIdx.y;
+    const int L = lens[n];
+    if (L < 1 || L > Tmax) return;  // reported by the combine kernel
+    const int lo = visible_lo(L, window);
+    const int t_begin = lo + s * chunk;
+    const int t_end = min(L, t_begin + chunk);
+    if (t_begin >= t_end) return;  // this split lies past the sequence's visible rows
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int g = lane / G;           // token slot within a step
+    const int c = lane % G;           // 8-element column group
+    const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
+
+    for (int h = warp; h < H; h += nwarps) {
+        float qf[8];
+        bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
+        float m = -INFINITY, l = 0.f, acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+        const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+        for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
+            uint4 kr[U], vr[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + u * TPS + g;
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+                if (t < t_end) {
+                    kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
+                    vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + u * TPS + g;
+                float kf[8];
+                bf16x8_to_f32(kr[u], kf);
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+#pragma unroll
+                for (int off = G / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                if (t < t_end) {
+                    const float sc = dot * scale_log2;
+                    const float m_new = fmaxf(m, sc);
+                    const float alpha = exp2f(m - m_new);
+                    const float p = exp2f(sc - m_new);
+                    float vf[8];
+                    bf16x8_to_f32(vr[u], vf);
+                    l = l * alpha + p;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i] * alpha);
+                    m = m_new;
+                }
+            }
+        }
+        // merge the TPS token slots of this warp (lanes with equal c)
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) {
+            const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
+            const float l_o = __shfl_xor_sync(0xffffffffu, l, off);
+            const float m_new = fmaxf(m, m_o);
+            const float a_s = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+            const float a_o = (m_o == -INFINITY) ? 0.f : exp2f(m_o - m_new);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float o_o = __shfl_xor_sync(0xffffffffu, acc[i], off);
+                acc[i] = acc[i] * a_s + o_o * a_o;
+            }
+            l = l * a_s + l_o * a_o;
+            m = m_new;
+        }
+        const size_t pidx = ((size_t)n * n_splits + s) * H + h;
+        if (lane < G) {
+            float4* po = reinterpret_cast<float4*>(part_o + pidx * D + c * 8);
+            po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) {
+            part_ml[pidx * 2 + 0] = m;
+            part_ml[pidx * 2 + 1] = l;
+        }
+    }
+}
+
+// One warp per (sequence, head): merge the partials of the splits that saw rows.
+template <int D>
+__global__ void __launch_bounds__(256)
+decode_combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
+                      const int* __restrict__ lens, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                      int N, int Tmax, int H, int window, int n_splits, int chunk, int* err) {
+    constexpr int E = D / 32;  // elements per lane
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= N * H) return;
+    const int n = gw / H, h = gw % H;
+    const int L = lens[n];
+    __nv_bfloat16* orow = o + (size_t)gw * D;
+    if (L < 1 || L > Tmax) {
+        if (lane == 0) set_device_error(err, NC_ERR_BAD_CACHE_LEN);
+#pragma unroll
+        for (int i = 0; i < E; ++i) orow[lane * E + i] = __float2bfloat16(NAN);
+        if (lse != nullptr && lane == 0) lse[gw] = NAN;
+        return;
+    }
+    const int lo = visible_lo(L, window);
+    const int used = (L - lo + chunk - 1) / chunk;
+    float M = -INFINITY;
+    for (int s = 0; s < used; ++s) M = fmaxf(M, part_ml[(((size_t)n * n_splits + s) * H + h) * 2]);
+    float lsum = 0.f, acc[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] = 0.f;
+    for (int s = 0; s < used; ++s) {
+        const size_t pidx = ((size_t)n * n_splits + s) * H + h;
+        const float w = exp2f(part_ml[pidx * 2] - M);
+        lsum = fmaf(part_ml[pidx * 2 + 1], w, lsum);
+        const float* po = part_o + pidx * D + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) acc[i] = fmaf(po[i], w, acc[i]);
+    }
+    const float inv = 1.f / lsum;
+#pragma unroll
+    for (int i = 0; i < E; ++i) orow[lane * E + i] = __float2bfloat16_rn(acc[i] * inv);
+    if (lse != nullptr && lane == 0) lse[gw] = (M + log2f(lsum)) * kLn2;
+}
+
+}  // namespace
+
+int decode_chunk_rows(int D) { return D == 64 ? 128 : 64; }
+
+int decode_max_splits(int Tmax, int D) {
+    const int chunk = decode_chunk_rows(D);
+    return (Tmax + chunk - 1) / chunk;
+}
+
+cudaError_t launch_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
+                          float* lse, int N, int Tmax, int H, int D, int window, float scale, float* part_ml,
+                          float* part_o, int* err, cudaStream_t stream) {
+    const int chunk = decode_chunk_rows(D);
+    const int max_splits = decode_max_splits(Tmax, D);
+    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
+    const int n_splits = (w_eff + chunk - 1) / chunk;  // splits any sequence can need
+    const float scale_log2 = scale * kLog2e;
+    (void)max_splits;
+    dim3 grid(n_splits, N);
+    const int threads = 32 * (H < 16 ? H : 16);
+    const int cblocks = (N * H * 32 + 255) / 256;
+    if (D == 128) {
+        decode_split_kernel<128><<<grid, threads, 0, stream>>>(
+            (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
+            part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
+        decode_combine_kernel<128><<<cblocks, 256, 0, stream>>>(part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
+                                                                Tmax, H, window, n_splits, chunk, err);
+    } else {
+        decode_split_kernel<64><<<grid, threads, 0, stream>>>(
+            (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
+            part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
+        decode_combine_kernel<64><<<cblocks, 256, 0, stream>>>(part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
+                                                               Tmax, H, window, n_splits, chunk, err);
+    }
+    count_launches(2);
+    return cudaGetLastError();
+}
+
+}  // namespace nc

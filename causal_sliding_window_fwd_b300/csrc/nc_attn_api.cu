@@ -1,0 +1,191 @@
+// C ABI of the attention library: argument validation, workspace sizing,
+// dispatch to the kernels and the sticky device error word.  The operation
+// and its sources are documented in include/nc_attn.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nc_attn.h"
+#include "nc_decode.h"
+#include "nc_kernels.h"
+
+namespace {
+
+__device__ int g_nc_error_word;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the error word on the current device (looked up once per device).
+int* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (g_err_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_nc_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool window_ok(int window) { return window >= 1 || window == NC_WINDOW_FULL; }
+
+bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks shared by the forward and backward calls.
+nc_status check_shape(int B, int T, int H, int D, int window, float scale) {
+    if (B <= 0 || T <= 0 || H <= 0 || D <= 0) return NC_ERR_INVALID;
+    if (!window_ok(window) || !scale_ok(scale)) return NC_ERR_INVALID;
+    if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
+    if ((int64_t)B * T * H >= (int64_t(1) << 31)) return NC_ERR_UNSUPPORTED;
+    return NC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nc_status_string(nc_status s) {
+    switch (s) {
+        case NC_OK: return "NC_OK";
+        case NC_ERR_INVALID: return "NC_ERR_INVALID";
+        case NC_ERR_UNSUPPORTED: return "NC_ERR_UNSUPPORTED";
+        case NC_ERR_WORKSPACE: return "NC_ERR_WORKSPACE";
+        case NC_ERR_CUDA: return "NC_ERR_CUDA";
+        case NC_ERR_DEVICE_TIMEOUT: return "NC_ERR_DEVICE_TIMEOUT";
+        case NC_ERR_BAD_CACHE_LEN: return "NC_ERR_BAD_CACHE_LEN";
+    }
+    return "NC_ERR_UNKNOWN";
+}
+
+nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
+                      int window, float scale, cudaStream_t stream) {
+    nc_status st = check_shape(B, T, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (!q || !k || !v || !o || !lse) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NC_ERR_INVALID;
+    const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4;
+    const void* ins[3] = {q, k, v};
+    for (const void* in : ins)
+        if (overlap(in, nb, o, nb) || overlap(in, nb, lse, nl)) return NC_ERR_INVALID;
+    if (overlap(o, nb, lse, nl)) return NC_ERR_INVALID;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const cudaError_t e = nc::launch_fwd(q, k, v, o, lse, B, T, H, D, window, scale, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D) {
+    if (B <= 0 || T <= 0 || H <= 0 || D <= 0) return 0;
+    return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256);
+}
+
+nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    nc_status st = check_shape(B, T, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return NC_ERR_INVALID;
+    const void* all[9] = {q, k, v, o, dO, lse, dq, dk, dv};
+    for (const void* p : all)
+        if (!aligned16(p)) return NC_ERR_INVALID;
+    const size_t need = nc_attn_bwd_workspace_bytes(B, T, H, D);
+    if (workspace == nullptr || workspace_bytes < need) return NC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return NC_ERR_INVALID;
+    const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4;
+    const void* ins[6] = {q, k, v, o, dO, lse};
+    const size_t in_n[6] = {nb, nb, nb, nb, nb, nl};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_n[4] = {nb, nb, nb, need};
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 6; ++i)
+            if (overlap(ins[i], in_n[i], outs[a], out_n[a])) return NC_ERR_INVALID;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], out_n[a], outs[b], out_n[b])) return NC_ERR_INVALID;
+    }
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    float* dq_acc = static_cast<float*>(workspace);
+    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)B * T * H * D * 4, 256));
+    const cudaError_t e = nc::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc, delta,
+                                         err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D) {
+    if (N <= 0 || Tmax <= 0 || H <= 0 || (D != 64 && D != 128)) return 0;
+    const size_t parts = (size_t)N * nc::decode_max_splits(Tmax, D) * H;
+    return round_up(parts * 2 * 4, 256) + round_up(parts * D * 4, 256);
+}
+
+nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, const int* cache_lens, void* o,
+                         float* lse, int N, int Tmax, int H, int D, int window, float scale, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    if (N <= 0 || Tmax <= 0 || H <= 0 || D <= 0) return NC_ERR_INVALID;
+    if (!window_ok(window) || !scale_ok(scale)) return NC_ERR_INVALID;
+    if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
+    if ((int64_t)N * H >= (int64_t(1) << 31) || (int64_t)Tmax * H * D >= (int64_t(1) << 40)) return NC_ERR_UNSUPPORTED;
+    if (!q || !kcache || !vcache || !cache_lens || !o) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return NC_ERR_INVALID;
+    const size_t need = nc_attn_decode_workspace_bytes(N, Tmax, H, D);
+    if (workspace == nullptr || workspace_bytes < need) return NC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return NC_ERR_INVALID;
+    const size_t nq = (size_t)N * H * D * 2, nc_ = (size_t)N * Tmax * H * D * 2, nl = (size_t)N * H * 4;
+    const void* ins[4] = {q, kcache, vcache, cache_lens};
+    const size_t in_n[4] = {nq, nc_, nc_, (size_t)N * 4};
+    void* outs[3] = {o, lse, workspace};
+    const size_t out_n[3] = {nq, lse ? nl : 0, need};
+    for (int a = 0; a < 3; ++a) {
+        if (outs[a] == nullptr) continue;
+        for (int i = 0; i < 4; ++i)
+            if (overlap(ins[i], in_n[i], outs[a], out_n[a])) return NC_ERR_INVALID;
+        for (int b = a + 1; b < 3; ++b)
+            if (outs[b] != nullptr && overlap(outs[a], out_n[a], outs[b], out_n[b])) return NC_ERR_INVALID;
+    }
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const size_t parts = (size_t)N * nc::decode_max_splits(Tmax, D) * H;
+    float* part_ml = static_cast<float*>(workspace);
+    float* part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(parts * 2 * 4, 256));
+    const cudaError_t e = nc::launch_decode(q, kcache, vcache, cache_lens, o, lse, N, Tmax, H, D, window, scale,
+                                            part_ml, part_o, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+unsigned long long nc_launch_count(void) { return nc::launch_count(); }
+
+nc_status nc_get_device_error(int* code, cudaStream_t stream) {
+    if (code == nullptr) return NC_ERR_INVALID;
+    *code = NC_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NC_ERR_CUDA;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpy(&value, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NC_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return NC_ERR_CUDA;
+    *code = value;
+    return NC_OK;
+}
+
+}  // extern "C"
+
+namespace nc {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace nc

@@ -1,0 +1,20 @@
+// Internal launch interface of the forward / backward attention kernels.
+#pragma once
+#include <cuda_runtime_api.h>
+
+namespace nc {
+
+// Host-side count of kernels enqueued by the library (see nc_launch_count).
+void count_launches(unsigned n);
+unsigned long long launch_count();
+
+// Forward: o [B,T,H,D] bf16, lse [B,H,T] fp32.  `err` is the device error word.
+cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
+                       int window, float scale, int* err, cudaStream_t st);
+
+// Backward: dq_acc fp32 [B,T,H,D] and delta fp32 [B,H,T] are workspace.
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
+                       float* dq_acc, float* delta, int* err, cudaStream_t st);
+
+}  // namespace nc

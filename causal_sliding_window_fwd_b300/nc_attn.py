@@ -1,0 +1,200 @@
+"""Python binding of the nc_attn C ABI (``include/nc_attn.h``).
+
+Argument marshalling only: torch tensors are checked for dtype, device,
+shape and contiguity, and their device pointers and the current CUDA stream
+are handed to ``libnc_attn.so``.  Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation behind these calls,
+and importing this module fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnc_attn.so")
+
+NC_OK = 0
+NC_ERR_INVALID = 1
+NC_ERR_UNSUPPORTED = 2
+NC_ERR_WORKSPACE = 3
+NC_ERR_CUDA = 4
+NC_ERR_DEVICE_TIMEOUT = 5
+NC_ERR_BAD_CACHE_LEN = 6
+NC_WINDOW_FULL = -1
+
+# Entry points declared in include/nc_attn.h.
+EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
+            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_get_device_error", "nc_launch_count")
+
+
+class NcError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libnc_attn.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                          "or python causal_sliding_window_fwd_b300/build_lib.py")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.nc_status_string.argtypes = [i]
+    lib.nc_status_string.restype = ctypes.c_char_p
+    lib.nc_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.nc_attn_fwd.restype = i
+    lib.nc_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.nc_attn_bwd_workspace_bytes.restype = sz
+    lib.nc_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_bwd.restype = i
+    lib.nc_attn_decode_workspace_bytes.argtypes = [i, i, i, i]
+    lib.nc_attn_decode_workspace_bytes.restype = sz
+    lib.nc_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_decode.restype = i
+    lib.nc_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+    lib.nc_get_device_error.restype = i
+    lib.nc_launch_count.argtypes = []
+    lib.nc_launch_count.restype = ctypes.c_ulonglong
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.nc_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != NC_OK:
+        raise NcError(code, where)
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)
+
+
+# ---------------------------------------------------------------- raw C-ABI mirrors
+
+
+def nc_attn_bwd_workspace_bytes(B: int, T: int, H: int, D: int) -> int:
+    return int(lib.nc_attn_bwd_workspace_bytes(B, T, H, D))
+
+
+def nc_attn_decode_workspace_bytes(N: int, Tmax: int, H: int, D: int) -> int:
+    return int(lib.nc_attn_decode_workspace_bytes(N, Tmax, H, D))
+
+
+def nc_attn_fwd(q, k, v, o, lse, window: int, scale: float, stream=None) -> None:
+    """Forward into caller-owned o [B,T,H,D] bf16 and lse [B,H,T] fp32."""
+    B, T, H, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(t, n, torch.bfloat16, (B, T, H, D))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    _check(lib.nc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, H, D, int(window), float(scale),
+                           _stream(q.device, stream)), "nc_attn_fwd")
+
+
+def nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace, stream=None) -> None:
+    """Backward into caller-owned dq, dk, dv; ``workspace`` is a uint8 device tensor."""
+    B, T, H, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, n, torch.bfloat16, (B, T, H, D))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib.nc_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                           B, T, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
+                           _stream(q.device, stream)), "nc_attn_bwd")
+
+
+def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, workspace, stream=None) -> None:
+    """Decode into caller-owned o [N,H,D] bf16 and lse [N,H] fp32 (or None)."""
+    N, Tmax, H, D = kcache.shape
+    _need(q, "q", torch.bfloat16, (N, H, D))
+    _need(kcache, "kcache", torch.bfloat16)
+    _need(vcache, "vcache", torch.bfloat16, (N, Tmax, H, D))
+    _need(cache_lens, "cache_lens", torch.int32, (N,))
+    _need(o, "o", torch.bfloat16, (N, H, D))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (N, H))
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib.nc_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
+                              N, Tmax, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
+                              _stream(q.device, stream)), "nc_attn_decode")
+
+
+def nc_get_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device error code."""
+    code = ctypes.c_int(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib.nc_get_device_error(ctypes.byref(code), _stream(dev, stream)), "nc_get_device_error")
+    return code.value
+
+
+def nc_launch_count() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(lib.nc_launch_count())
+
+
+# ---------------------------------------------------------------- allocating conveniences
+
+
+def attn_fwd(q, k, v, window: int, scale: float | None = None, stream=None):
+    """Returns (o, lse) for bf16 q, k, v [B, T, H, D]."""
+    B, T, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    nc_attn_fwd(q, k, v, o, lse, window, scale, stream)
+    return o, lse
+
+
+def attn_bwd(q, k, v, o, dO, lse, window: int, scale: float | None = None, workspace=None, stream=None):
+    """Returns (dq, dk, dv)."""
+    B, T, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+    return dq, dk, dv
+
+
+def attn_decode(q, kcache, vcache, cache_lens, window: int, scale: float | None = None, workspace=None,
+                with_lse: bool = True, stream=None):
+    """Returns (o [N,H,D], lse [N,H] or None)."""
+    N, Tmax, H, D = kcache.shape
+    scale = default_scale(D) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nc_attn_decode_workspace_bytes(N, Tmax, H, D), dtype=torch.uint8, device=q.device)
+    o = torch.empty((N, H, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((N, H), dtype=torch.float32, device=q.device) if with_lse else None
+    nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window, scale, workspace, stream)
+    return o, lse

@@ -1,0 +1,145 @@
+/*
+ * nc_attn — exact causal sliding-window softmax attention for NVIDIA B300 (sm_103a).
+ *
+ * C ABI.  Every entry point takes plain device pointers, sizes and a CUDA
+ * stream; none allocates, none synchronises (except nc_get_device_error), and
+ * all work is enqueued on `stream`.  The caller owns every buffer, including
+ * the workspaces.
+ *
+ * The operation (what the calls compute):
+ *   "nanochat GPT-2 speedrun" post (page 2, repeated on page 5), paragraph on
+ *   the biggest improvements: attention runs through FlashAttention-3 kernels
+ *   whose `window_size` argument gives per-layer alternating local/global
+ *   (sliding-window / full causal) attention.  "nanochat" walkthrough (page 4,
+ *   close of the pretraining section; page 1 launch post): inference runs an
+ *   Engine with a KV cache and a prefill/decode split.  The pages give no
+ *   formula, so the calls compute the textbook definition:
+ *
+ *     visible(i, j)  <=>  j <= i  and  i - j < W        (W keys including i)
+ *     s_ij  = scale * <q_i, k_j>
+ *     lse_i = ln sum_{j visible} exp(s_ij)
+ *     o_i   = sum_{j visible} exp(s_ij - lse_i) v_j
+ *
+ *   per batch b and head h independently.  `window` <= 0 is rejected except
+ *   NC_WINDOW_FULL (-1); a window >= T is full causal attention.
+ *
+ * Layout (all contiguous, row-major):
+ *   q, k, v, o, dO, dq, dk, dv : bf16 [B, T, H, D]
+ *   lse                        : fp32 [B, H, T]   (natural log, of the scaled scores)
+ *   decode q, o                : bf16 [N, H, D]
+ *   decode kcache, vcache      : bf16 [N, Tmax, H, D]  (padded per sequence)
+ *   decode cache_lens          : int32 [N] in device memory
+ *   decode lse                 : fp32 [N, H] or NULL
+ *
+ * Supported sizes: D in {64, 128}; B, T, H, N >= 1; B*H and T small enough
+ * that every tensor has fewer than 2^31 rows of D elements.  All pointers
+ * must be 16-byte aligned (the kernels move data with TMA and 16-byte
+ * vectors).  Outputs must not alias inputs or each other.
+ *
+ * Errors: host-side argument checks return a status synchronously and launch
+ * nothing.  Conditions only the device can see (a decode cache length
+ * outside [1, Tmax], a pipeline wait that exceeded its time limit) set a
+ * sticky device error word, write NaN into the affected output rows and let
+ * the kernel finish; nc_get_device_error() reads and clears that word.
+ */
+#ifndef NC_ATTN_H_
+#define NC_ATTN_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NC_OK = 0,
+    NC_ERR_INVALID = 1,        /* null pointer, non-positive size, bad window/scale, misalignment, aliasing */
+    NC_ERR_UNSUPPORTED = 2,    /* head dimension other than 64 or 128, sizes beyond the index range */
+    NC_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than the *_workspace_bytes() figure */
+    NC_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
+    NC_ERR_DEVICE_TIMEOUT = 5, /* device: a pipeline wait ran out of time; outputs are not valid */
+    NC_ERR_BAD_CACHE_LEN = 6   /* device: a decode cache length was outside [1, Tmax]; its rows are NaN */
+} nc_status;
+
+#define NC_WINDOW_FULL (-1)
+
+/* Human-readable name of a status code (static string). */
+const char* nc_status_string(nc_status s);
+
+/*
+ * Forward.  o = attention(q, k, v) and lse = per-row log-sum-exp of the
+ * scaled scores over the visible keys.
+ *   q, k, v : const bf16 [B, T, H, D] device
+ *   o       : bf16 [B, T, H, D] device, written
+ *   lse     : fp32 [B, H, T] device, written (needed by nc_attn_bwd)
+ *   window  : keys visible per query including itself (>= 1), or NC_WINDOW_FULL
+ *   scale   : score multiplier, finite and > 0 (usually 1/sqrt(D))
+ * Returns NC_OK once the work is enqueued on `stream`.
+ */
+nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int T, int H, int D, int window, float scale, cudaStream_t stream);
+
+/* Bytes of device workspace nc_attn_bwd needs: an fp32 dQ accumulator
+ * [B, T, H, D] plus the fp32 row term Delta = rowsum(dO * O) [B, H, T]. */
+size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D);
+
+/*
+ * Backward.  Gradients of sum(o * dO) with respect to q, k and v, for the
+ * o and lse that nc_attn_fwd produced with the same arguments.
+ *   q, k, v, o, dO : const bf16 [B, T, H, D] device
+ *   lse            : const fp32 [B, H, T] device
+ *   dq, dk, dv     : bf16 [B, T, H, D] device, written
+ *   workspace      : device, >= nc_attn_bwd_workspace_bytes(B, T, H, D),
+ *                    16-byte aligned; its contents on entry do not matter
+ * The dQ accumulation uses fp32 atomics, so dq may differ in the last bits
+ * from run to run.
+ */
+nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv,
+                      int B, int T, int H, int D, int window, float scale,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace nc_attn_decode needs for its split-K partial
+ * results (fp32 running max, sum and output per split). */
+size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D);
+
+/*
+ * Single-token decode over a KV cache (one query per sequence).  The query
+ * of sequence n sits at position L = cache_lens[n] - 1, whose key and value
+ * are already in the cache; it sees cache rows max(0, L + 1 - window) .. L.
+ *   q          : const bf16 [N, H, D] device
+ *   kcache     : const bf16 [N, Tmax, H, D] device
+ *   vcache     : const bf16 [N, Tmax, H, D] device
+ *   cache_lens : const int32 [N] device, each in [1, Tmax]; a value outside
+ *                that range sets NC_ERR_BAD_CACHE_LEN on the device and
+ *                makes that sequence's o (and lse) rows NaN
+ *   o          : bf16 [N, H, D] device, written
+ *   lse        : fp32 [N, H] device, written, or NULL
+ *   workspace  : device, >= nc_attn_decode_workspace_bytes(N, Tmax, H, D)
+ * Cache rows at or beyond a sequence's length, and rows before its window,
+ * are never read.
+ */
+nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
+                         void* o, float* lse, int N, int Tmax, int H, int D, int window, float scale,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * the kernels set (NC_OK if nothing went wrong since the last call).
+ * Returns NC_ERR_CUDA if the synchronisation itself failed.
+ */
+nc_status nc_get_device_error(int* code, cudaStream_t stream);
+
+/*
+ * Number of CUDA kernels this library has enqueued (all devices, all
+ * streams) since it was loaded.  Host-side counter, for launch accounting in
+ * benchmarks; it does not synchronise and never fails.
+ */
+unsigned long long nc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_ATTN_H_ */

@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+entry point, sizes its workspaces, and rejects bad arguments before touching
+the GPU (these calls pass fake pointers, which validation refuses first)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_sliding_window_fwd_b300 import build_lib
+    build_lib.build()
+    from causal_sliding_window_fwd_b300 import nc_attn
+    return nc_attn
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "nc_attn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const char\*|nc_status|size_t|unsigned long long)\s+(nc_\w+)\s*\(",
+                                 txt, re.M)))
+
+
+def test_header_declares_the_abi():
+    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_bwd_workspace_bytes",
+            "nc_attn_decode_workspace_bytes", "nc_get_device_error", "nc_status_string",
+            "nc_launch_count"} <= set(_declared())
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared():
+        assert hasattr(raw, name), name
+    assert set(lib.EXPORTED) <= set(_declared())
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "NC_OK"
+    assert lib.status_string(6) == "NC_ERR_BAD_CACHE_LEN"
+
+
+def test_workspace_sizes(lib):
+    B, T, H, D = 16, 2048, 10, 128
+    need = lib.nc_attn_bwd_workspace_bytes(B, T, H, D)
+    assert need >= B * T * H * D * 4 + B * H * T * 4
+    assert need < B * T * H * D * 4 + B * H * T * 4 + 1024
+    assert lib.nc_attn_bwd_workspace_bytes(0, T, H, D) == 0
+    dec = lib.nc_attn_decode_workspace_bytes(64, 8192, 10, 128)
+    assert 0 < dec < 64 * 1024 * 1024
+    assert lib.nc_attn_decode_workspace_bytes(64, 8192, 10, 96) == 0
+
+
+# Fake, 16-byte aligned and non-overlapping "device" addresses: validation must
+# reject each call below before any CUDA call is made.
+A = [0x10000000 + i * 0x10000000 for i in range(12)]
+GOOD = dict(B=2, T=64, H=2, D=64, window=16, scale=0.125)
+
+
+def _fwd(lib, ptrs=None, **kw):
+    a = dict(GOOD, **kw)
+    p = list(A[:5]) if ptrs is None else ptrs
+    return lib.lib.nc_attn_fwd(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"], a["window"],
+                               ctypes.c_float(a["scale"]), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1),
+    (dict(D=96), 2), (dict(D=256), 2),
+    (dict(window=0), 1), (dict(window=-2), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=math.nan), 1), (dict(scale=math.inf), 1),
+])
+def test_fwd_rejects_bad_sizes(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def test_fwd_rejects_null_misaligned_and_aliased(lib):
+    for i in range(5):
+        p = list(A[:5]); p[i] = 0
+        assert _fwd(lib, p) == lib.NC_ERR_INVALID
+        p = list(A[:5]); p[i] += 8
+        assert _fwd(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[3] = p[0]            # o aliases q
+    assert _fwd(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[4] = p[3] + 64       # lse inside o
+    assert _fwd(lib, p) == lib.NC_ERR_INVALID
+
+
+def _bwd(lib, ptrs=None, ws=None, ws_bytes=None, **kw):
+    a = dict(GOOD, **kw)
+    p = list(A[:9]) if ptrs is None else ptrs
+    need = lib.nc_attn_bwd_workspace_bytes(a["B"], a["T"], a["H"], a["D"])
+    ws = A[9] if ws is None else ws
+    ws_bytes = need if ws_bytes is None else ws_bytes
+    return lib.lib.nc_attn_bwd(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"], a["window"],
+                               ctypes.c_float(a["scale"]), ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert _bwd(lib, D=80) == lib.NC_ERR_UNSUPPORTED
+    assert _bwd(lib, window=0) == lib.NC_ERR_INVALID
+    need = lib.nc_attn_bwd_workspace_bytes(2, 64, 2, 64)
+    assert _bwd(lib, ws_bytes=need - 1) == lib.NC_ERR_WORKSPACE
+    assert _bwd(lib, ws=0) == lib.NC_ERR_WORKSPACE
+    assert _bwd(lib, ws=A[9] + 4) == lib.NC_ERR_INVALID
+    for i in range(9):
+        p = list(A[:9]); p[i] = 0
+        assert _bwd(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:9]); p[6] = p[0]            # dq aliases q
+    assert _bwd(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:9]); p[7] = p[6]            # dk aliases dq
+    assert _bwd(lib, p) == lib.NC_ERR_INVALID
+    assert _bwd(lib, ws=A[1]) == lib.NC_ERR_INVALID  # workspace over k
+
+
+def _dec(lib, ptrs=None, ws_bytes=None, **kw):
+    a = dict(N=4, Tmax=256, H=2, D=128, window=64, scale=0.1)
+    a.update(kw)
+    p = list(A[:6]) if ptrs is None else ptrs
+    need = lib.nc_attn_decode_workspace_bytes(a["N"], a["Tmax"], a["H"], a["D"])
+    ws_bytes = need if ws_bytes is None else ws_bytes
+    return lib.lib.nc_attn_decode(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                                  a["N"], a["Tmax"], a["H"], a["D"], a["window"], ctypes.c_float(a["scale"]),
+                                  ctypes.c_void_p(A[10]), ws_bytes, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert _dec(lib, N=0) == lib.NC_ERR_INVALID
+    assert _dec(lib, D=32) == lib.NC_ERR_UNSUPPORTED
+    assert _dec(lib, window=0) == lib.NC_ERR_INVALID
+    assert _dec(lib, scale=-0.5) == lib.NC_ERR_INVALID
+    need = lib.nc_attn_decode_workspace_bytes(4, 256, 2, 128)
+    assert _dec(lib, ws_bytes=need - 4) == lib.NC_ERR_WORKSPACE
+    for i in range(5):
+        p = list(A[:6]); p[i] = 0
+        assert _dec(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[4] = p[1]            # o aliases the key cache
+    assert _dec(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[3] = p[3] + 2        # lens misaligned
+    assert _dec(lib, p) == lib.NC_ERR_INVALID

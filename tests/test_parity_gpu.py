@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances, max over all compared elements:
+  output          |O - O_ref|   <= 2e-2 * max|O_ref|
+  log-sum-exp     |L - L_ref|   <= 1e-3 (absolute)
+  gradients       |dX - dX_ref| <= 3e-2 * max|dX_ref|   for X in q, k, v
+The inputs are bf16 and the kernels accumulate in fp32; the oracle sees the
+same bf16 tensors widened exactly to fp64.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from causal_sliding_window_fwd_b300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL, G_TOL = 2e-2, 1e-3, 3e-2
+
+
+@pytest.fixture(scope="module")
+def nc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_sliding_window_fwd_b300 import nc_attn
+    return nc_attn
+
+
+def rel_err(got, ref):
+    got = got.detach().float().cpu().numpy() if torch.is_tensor(got) else got
+    ref = np.asarray(ref)
+    assert np.isfinite(got).all(), "non-finite values in GPU output"
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def abs_err(got, ref):
+    got = got.detach().float().cpu().numpy() if torch.is_tensor(got) else got
+    assert np.isfinite(got).all(), "non-finite values in GPU output"
+    return float(np.abs(got - np.asarray(ref)).max())
+
+
+def run_fwd_bwd(nc, q, k, v, dO, window, scale):
+    B, T, H, D = q.shape
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, T), float("nan"), dtype=torch.float32, device=q.device)
+    nc.nc_attn_fwd(q, k, v, o, lse, window, scale)
+    ws = torch.full((nc.nc_attn_bwd_workspace_bytes(B, T, H, D),), 0xFF, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    nc.nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window, scale, ws)
+    assert nc.nc_get_device_error() == 0
+    return o, lse, dq, dk, dv
+
+
+def check_against_oracle(oracle_mod, q, k, v, dO, window, scale, o, lse, dq, dk, dv, grads=True):
+    o_ref, lse_ref = oracle_mod.fwd(q, k, v, window, scale)
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+    if grads:
+        dq_r, dk_r, dv_r = oracle_mod.bwd(q, k, v, dO, window, scale)
+        assert rel_err(dq, dq_r) <= G_TOL, "dq"
+        assert rel_err(dk, dk_r) <= G_TOL, "dk"
+        assert rel_err(dv, dv_r) <= G_TOL, "dv"
+
+
+# ---------------------------------------------------------------- small shapes, whole tensors
+
+
+def test_tiny_workload(nc, oracle_mod):
+    call = workloads.TINY.calls[0]
+    q, k, v, dO = workloads.make_qkvdo(call, "cuda")
+    outs = run_fwd_bwd(nc, q, k, v, dO, call.window, call.scale)
+    check_against_oracle(oracle_mod, q, k, v, dO, call.window, call.scale, *outs)
+
+
+SWEEP = [
+    # (B, T, H, D, window)
+    (1, 1, 1, 64, 1), (1, 1, 1, 128, -1), (1, 7, 1, 128, 3), (2, 128, 1, 64, 1), (1, 128, 2, 128, 2),
+    (1, 200, 2, 128, 127), (1, 200, 1, 128, 128), (1, 257, 1, 128, 129), (1, 333, 2, 64, 332),
+    (1, 333, 1, 128, 333), (1, 333, 1, 128, 338), (2, 384, 3, 128, -1), (1, 513, 2, 64, 100),
+    (1, 640, 1, 128, 256), (1, 700, 1, 128, 512),
+]
+
+
+@pytest.mark.parametrize("B,T,H,D,window", SWEEP)
+def test_shape_sweep(nc, oracle_mod, B, T, H, D, window):
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=1000 + T + window, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    outs = run_fwd_bwd(nc, q, k, v, dO, window, scale)
+    check_against_oracle(oracle_mod, q, k, v, dO, window, scale, *outs)
+
+
+def test_window_one_is_exact_identity(nc):
+    q, k, v, dO = workloads.make_qkvdo_shape(2, 300, 3, 128, seed=77, device="cuda")
+    o, lse, dq, dk, dv = run_fwd_bwd(nc, q, k, v, dO, 1, 0.088)
+    assert torch.equal(o, v)
+    torch.testing.assert_close(dv, dO, rtol=0, atol=0)
+
+
+def test_scale_other_than_default(nc, oracle_mod):
+    q, k, v, dO = workloads.make_qkvdo_shape(1, 256, 2, 64, seed=5, device="cuda")
+    outs = run_fwd_bwd(nc, q, k, v, dO, 100, 0.3)
+    check_against_oracle(oracle_mod, q, k, v, dO, 100, 0.3, *outs)
+
+
+def test_repeat_calls_agree(nc):
+    q, k, v, dO = workloads.make_qkvdo_shape(2, 512, 2, 128, seed=9, device="cuda")
+    a = run_fwd_bwd(nc, q, k, v, dO, 200, 0.088)
+    b = run_fwd_bwd(nc, q, k, v, dO, 200, 0.088)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for x, y in zip(a[2:], b[2:]):
+        assert rel_err(x, y.float().cpu().numpy()) <= 1e-2
+
+
+def test_guard_bytes_untouched(nc):
+    """Outputs live inside larger buffers; the bytes around them must not change."""
+    B, T, H, D, W = 1, 300, 2, 128, 64
+    n = B * T * H * D
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=11, device="cuda")
+    pad = 4096
+    big = [torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    o, dq, dk, dv = (b[pad:pad + n].view(B, T, H, D) for b in big)
+    lbig = torch.full((B * H * T + 2 * pad,), 5.0, dtype=torch.float32, device="cuda")
+    lse = lbig[pad:pad + B * H * T].view(B, H, T)
+    nc.nc_attn_fwd(q, k, v, o, lse, W, 0.088)
+    wsz = nc.nc_attn_bwd_workspace_bytes(B, T, H, D)
+    wbig = torch.full((wsz + 2 * pad,), 0xAB, dtype=torch.uint8, device="cuda")
+    nc.nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, W, 0.088, wbig[pad:pad + wsz])
+    torch.cuda.synchronize()
+    for b in big:
+        assert (b[:pad] == 7.0).all() and (b[pad + n:] == 7.0).all()
+    assert (lbig[:pad] == 5.0).all() and (lbig[pad + B * H * T:] == 5.0).all()
+    assert (wbig[:pad] == 0xAB).all() and (wbig[pad + wsz:] == 0xAB).all()
+
+
+# ---------------------------------------------------------------- full workload sizes, sampled slices
+
+
+def _slice(x, b, h):
+    return x[b:b + 1, :, h:h + 1, :]
+
+
+@pytest.mark.parametrize("wl_name,call_idx", [("D20_PAIR", 0), ("D20_PAIR", 1), ("D30_ALT", 0), ("D30_ALT", 1),
+                                              ("LONG_SW", 0)])
+def test_full_size_sampled(nc, oracle_mod, wl_name, call_idx):
+    call = getattr(workloads, wl_name).calls[call_idx]
+    q, k, v, dO = workloads.make_qkvdo(call, "cuda")
+    o, lse, dq, dk, dv = run_fwd_bwd(nc, q, k, v, dO, call.window, call.scale)
+    for t in (o, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    # properties that hold for every (b, h): sum_j dV_j = sum_i dO_i and sum_j dK_j = 0
+    sv = dv.float().sum(1)
+    so = dO.float().sum(1)
+    assert (sv - so).abs().max().item() <= 3e-2 * so.abs().max().item() + 0.5
+    # sampled (b, h) slices against the oracle
+    rng = np.random.default_rng(call.seed)
+    picks = {(call.B - 1, call.H - 1)} | {(int(rng.integers(call.B)), int(rng.integers(call.H))) for _ in range(1)}
+    for b, h in sorted(picks):
+        sl = [_slice(x, b, h).contiguous().cpu() for x in (q, k, v, dO)]
+        check_against_oracle(oracle_mod, *sl, call.window, call.scale,
+                             _slice(o, b, h), lse[b:b + 1, h:h + 1], _slice(dq, b, h), _slice(dk, b, h),
+                             _slice(dv, b, h))
+
+
+# ---------------------------------------------------------------- decode
+
+
+def _decode_oracle_for(oracle_mod, q, kc, vc, lens, n_list, window, scale):
+    Lmax = int(max(int(lens[n]) for n in n_list))
+    qs = q[n_list].cpu()
+    ks = kc[n_list, :Lmax].cpu()
+    vs = vc[n_list, :Lmax].cpu()
+    return oracle_mod.decode(qs, ks, vs, lens[n_list].cpu(), window, scale)
+
+
+@pytest.mark.parametrize("window", [1024, -1])
+def test_decode_full_size_poisoned(nc, oracle_mod, window):
+    wl = workloads.DECODE
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda", poison_tail=True)
+    if window > 0:  # rows before the window are never read either
+        pos = torch.arange(wl.Tmax, device="cuda").view(1, -1)
+        dead = (pos < (lens.view(-1, 1) - window)).view(wl.N, wl.Tmax, 1, 1)
+        kc.masked_fill_(dead, float("nan"))
+        vc.masked_fill_(dead, float("nan"))
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    picks = [0, 1, int(torch.argmax(lens)), int(torch.argmin(lens)), 33, 63]
+    o_ref, lse_ref, ok = _decode_oracle_for(oracle_mod, q, kc, vc, lens, picks, window, wl.scale)
+    assert ok
+    assert rel_err(o[picks], o_ref) <= O_TOL
+    assert abs_err(lse[picks], lse_ref) <= LSE_TOL
+
+
+@pytest.mark.parametrize("D,window", [(64, 1), (64, 100), (128, 5), (128, -1), (64, -1)])
+def test_decode_small(nc, oracle_mod, D, window):
+    wl = workloads.DecodeWorkload("small", 7, 700, 3, D, 1, 700, (window,), 4242 + D)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda", poison_tail=True)
+    lens[0] = 1
+    lens[1] = 700
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
+                                           window, wl.scale)
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
+def test_decode_equals_last_forward_row(nc):
+    B, T, H, D, W = 2, 600, 2, 128, 256
+    q, k, v, _ = workloads.make_qkvdo_shape(B, T, H, D, seed=31, device="cuda")
+    o, lse = nc.attn_fwd(q, k, v, W)
+    lens = torch.tensor([T, 451], dtype=torch.int32, device="cuda")
+    qd = torch.stack([q[0, T - 1], q[1, 450]]).contiguous()
+    od, lsed = nc.attn_decode(qd, k, v, lens, W)
+    # sequence 1 is a 451-row prefix: compare with a forward over that prefix alone
+    o1, lse1 = nc.attn_fwd(q[1:2, :451].contiguous(), k[1:2, :451].contiguous(), v[1:2, :451].contiguous(), W)
+    torch.testing.assert_close(od[0].float(), o[0, T - 1].float(), atol=2e-2, rtol=0)
+    torch.testing.assert_close(od[1].float(), o1[0, 450].float(), atol=2e-2, rtol=0)
+    assert (lsed[0] - lse[0, :, T - 1]).abs().max().item() < 1e-3
+    assert (lsed[1] - lse1[0, :, 450]).abs().max().item() < 1e-3
+
+
+def test_decode_bad_length_reports_and_nans(nc):
+    wl = workloads.DecodeWorkload("bad", 4, 256, 2, 128, 1, 256, (-1,), 99)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda")
+    lens[1] = 0
+    lens[2] = 257
+    o, lse = nc.attn_decode(q, kc, vc, lens, -1, wl.scale)
+    assert nc.nc_get_device_error() == nc.NC_ERR_BAD_CACHE_LEN
+    assert torch.isnan(o[1].float()).all() and torch.isnan(o[2].float()).all()
+    assert torch.isfinite(o[0].float()).all() and torch.isfinite(o[3].float()).all()
+    assert nc.nc_get_device_error() == 0  # cleared by the read
