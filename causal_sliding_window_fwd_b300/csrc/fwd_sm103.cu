@@ -1,0 +1,418 @@
+// Forward attention on 5th-generation tensor cores (tcgen05, TMEM, TMA) for sm_103a.
+//
+// Operation (see include/nc_attn.h): exact causal softmax attention restricted
+// to a sliding window of W keys, with the per-row log-sum-exp, as the
+// "nanochat GPT-2 speedrun" post (page 2, biggest-improvements paragraph)
+// uses through FlashAttention-3's window_size argument.  The computation is
+// the textbook definition evaluated block by block with an online softmax.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and walks the
+// 128-key blocks that the causal window makes visible to either tile; blocks
+// wholly outside the window are never loaded (tile skipping).  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K and V blocks through a
+//               4-slot shared-memory ring (128-byte swizzle)
+//   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
+//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
+//   warps 8-11  softmax + epilogue of query tile 1
+// TMEM: S0 cols [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P (bf16, two per column) overwrites the first 64 columns of its S tile and
+// feeds the P*V product straight from TMEM.  The MMA issue order
+//   S0(j+1) after PV0(j), S1(j+1) after PV1(j)
+// lets one tile's softmax overlap the other tile's products.  The running
+// maximum is only raised (and O rescaled in TMEM) when it grows by more
+// than 2^8, which keeps every exponent bounded and the sum exact.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "nc_attn.h"
+#include "nc_kernels.h"
+#include "nc_ptx.cuh"
+#include "nc_tma.h"
+
+namespace nc {
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per block
+constexpr int kStages = 4;        // K/V ring slots
+constexpr int kThreads = 384;     // 12 warps
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdSmem {
+    static constexpr int kTileBytes = kBM * D * 2;     // one Q tile or one K/V block
+    static constexpr int kQOff = 0;                    // Q0, Q1
+    static constexpr int kKVOff = 2 * kTileBytes;      // ring
+    static constexpr int kBytes = kKVOff + kStages * kTileBytes;
+};
+
+struct FwdBarriers {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_final;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct FwdParams {
+    __nv_bfloat16* o;
+    float* lse;
+    int B, T, H, W;       // W: effective window, 1 <= W <= T
+    float scale_log2;
+    int n_pairs;          // query-tile pairs per (b, h)
+    int* err;
+};
+
+// Key blocks [lo, hi] that intersect the window of some row of the tile starting at r0.
+__device__ __forceinline__ void tile_blocks(int r0, int T, int W, int& lo, int& hi) {
+    const int first_key = r0 - W + 1;
+    lo = first_key <= 0 ? 0 : first_key / kBN;
+    const int last_row = min(r0 + kBM - 1, T - 1);
+    hi = last_row / kBN;
+}
+
+__device__ __forceinline__ bool aborted(const FwdBarriers& bars) {
+    return *reinterpret_cast<const volatile int*>(&bars.abort) != 0;
+}
+
+__device__ __forceinline__ void record_timeout(FwdBarriers& bars, int* err) {
+    set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
+    atomicExch(&bars.abort, 1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using L = FwdSmem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ FwdBarriers bars;
+
+    const int warp = warp_id(), lane = lane_id();
+    // heaviest query tiles first: they have the most key blocks under full causal masking
+    const int pair = p.n_pairs - 1 - blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int r0[2] = {pair * 2 * kBM, pair * 2 * kBM + kBM};
+    const bool active1 = r0[1] < p.T;
+    int lo[2], hi[2];
+    tile_blocks(r0[0], p.T, p.W, lo[0], hi[0]);
+    tile_blocks(r0[1], p.T, p.W, lo[1], hi[1]);
+    if (!active1) { lo[1] = hi[0] + 1; hi[1] = hi[0]; }
+    const int kb_lo = lo[0];
+    const int kb_hi = active1 ? hi[1] : hi[0];
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars.kv_full[i], 1);
+            mbar_init(&bars.kv_empty[i], 1);
+        }
+        mbar_init(&bars.q_full, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars.s_full[t], 1);
+            mbar_init(&bars.p_full[t], kBM);
+        }
+        mbar_init(&bars.o_final, 1);
+        mbar_init(&bars.drain, 1);
+        bars.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    // 384 threads x 168 registers at launch = 128 x 56 (producer/MMA warpgroup) + 256 x 224 (softmax);
+    // each role sets its budget at the top of its own branch
+    const uint32_t col_s[2] = {0u, 128u};
+    const uint32_t col_o[2] = {256u, 256u + D};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        regs_decrease<56>();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&bars.q_full, 2 * L::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64, h,
+                                r0[t], b);
+            const int n_loads = 2 * (kb_hi - kb_lo + 1);
+            int issued = 0;
+            for (int seq = 0; seq < n_loads; ++seq) {
+                const int slot = seq % kStages;
+                if (!mbar_wait(&bars.kv_empty[slot], ((seq / kStages) & 1) ^ 1) || aborted(bars)) {
+                    record_timeout(bars, p.err);
+                    break;
+                }
+                const int kb = kb_lo + seq / 2;
+                const CUtensorMap* tm = (seq & 1) ? &tm_v : &tm_k;
+                uint8_t* dst = smem + L::kKVOff + slot * L::kTileBytes;
+                mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, h, kb * kBN, b);
+                issued = seq + 1;
+            }
+            // never leave while a copy into this CTA's shared memory may still land
+            for (int seq = issued - kStages < 0 ? 0 : issued - kStages; seq < issued; ++seq)
+                mbar_wait(&bars.kv_full[seq % kStages], (seq / kStages) & 1);
+            mbar_wait(&bars.q_full, 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        regs_decrease<56>();
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
+            const uint32_t q_base = smem_u32(smem + L::kQOff);
+            const uint32_t kv_base = smem_u32(smem + L::kKVOff);
+            auto act = [&](int t, int kb) { return kb >= lo[t] && kb <= hi[t]; };
+            auto issue_s = [&](int t, int slot) {
+                const uint32_t qa = q_base + t * L::kTileBytes;
+                const uint32_t ka = kv_base + slot * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
+                    mma_ss(tmem + col_s[t], sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idesc_qk, kk > 0);
+                }
+                mma_commit(&bars.s_full[t]);
+            };
+            auto issue_pv = [&](int t, int slot, bool accumulate) {
+                const uint32_t va = kv_base + slot * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8, sdesc(va + kk * 2048, kBN * 128, 1024),
+                           idesc_pv, accumulate || kk > 0);
+            };
+            bool ok = mbar_wait(&bars.q_full, 0);
+            int seq = 0;
+            int n_pv[2] = {0, 0};
+            if (ok) {
+                const int slot_k = seq % kStages;
+                ok = mbar_wait(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t)
+                        if (act(t, kb_lo)) issue_s(t, slot_k);
+                    mma_commit(&bars.kv_empty[slot_k]);
+                    ++seq;
+                }
+            }
+            for (int kb = kb_lo; ok && kb <= kb_hi; ++kb) {
+                const int slot_v = seq % kStages;
+                ok = mbar_wait(&bars.kv_full[slot_v], (seq / kStages) & 1);
+                if (!ok) break;
+                ++seq;
+                const bool next = kb + 1 <= kb_hi;
+                const int slot_k = seq % kStages;
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (act(t, kb)) {
+                        ok = mbar_wait(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, slot_v, n_pv[t] > 0);
+                        ++n_pv[t];
+                    }
+                    if (next && act(t, kb + 1)) {
+                        if (!k_ready) {
+                            ok = mbar_wait(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_s(t, slot_k);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bars.kv_empty[slot_v]);
+                if (next) {
+                    mma_commit(&bars.kv_empty[slot_k]);
+                    ++seq;
+                }
+            }
+            if (!ok) record_timeout(bars, p.err);
+            mma_commit(&bars.o_final);
+            // all products must have landed before TMEM is released
+            mma_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        regs_decrease<56>();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        regs_increase<224>();
+        const int t = (warp - 4) / 4;
+        const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
+        const int lane_base = 32 * (warp % 4);
+        const int row = r0[t] + row_in_tile;
+        const bool tile_on = (t == 0) || active1;
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        if (tile_on) {
+            const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + col_s[t];
+            const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + col_o[t];
+            int it = 0;
+            for (int kb = lo[t]; kb <= hi[t]; ++kb, ++it) {
+                ok = mbar_wait(&bars.s_full[t], it & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                float s[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                }
+                // elementwise mask only on blocks that straddle the causal diagonal or the window edge
+                const int k0 = kb * kBN;
+                const bool full_block = (k0 + kBN - 1 <= r0[t]) && (k0 >= r0[t] + kBM - p.W);
+                if (!full_block) {
+#pragma unroll
+                    for (int j = 0; j < kBN; ++j) {
+                        const int key = k0 + j;
+                        if (key > row || row - key >= p.W) s[j] = -INFINITY;
+                    }
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int j = 4; j < kBN; j += 4) {
+                    mx0 = fmaxf(mx0, s[j]);
+                    mx1 = fmaxf(mx1, s[j + 1]);
+                    mx2 = fmaxf(mx2, s[j + 2]);
+                    mx3 = fmaxf(mx3, s[j + 3]);
+                }
+                const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                if (it == 0) {
+                    m_run = m_cand;
+                } else {
+                    const bool want = m_cand > m_run + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, want)) {
+                        const float m_new = fmaxf(m_run, m_cand);
+                        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
+                        m_run = m_new;
+                        l_run *= alpha;
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(o_addr + c * 32, r);
+                        }
+                    }
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN / 64; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float e0 = ex2_approx(fmaf(s[c * 64 + 2 * i], sl2, -m_use));
+                        const float e1 = ex2_approx(fmaf(s[c * 64 + 2 * i + 1], sl2, -m_use));
+                        sum0 += e0;
+                        sum1 += e1;
+                        pk[i] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st32(s_addr + c * 32, pk);
+                }
+                l_run += sum0 + sum1;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars.p_full[t]);
+            }
+            // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
+            if (ok) ok = mbar_wait(&bars.o_final, 0) && !aborted(bars);
+            if (!ok) {
+                record_timeout(bars, p.err);
+            } else {
+                tc_fence_after();
+                const float inv_l = 1.f / l_run;
+                const bool in_range = row < p.T;
+                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.T + row) * p.H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + c * 32, r);
+                    if (in_range) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 pkt;
+                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+                            reinterpret_cast<uint4*>(orow + c * 32)[v] = pkt;
+                        }
+                    }
+                }
+                if (in_range) p.lse[(static_cast<size_t>(b) * p.H + h) * p.T + row] = (m_run + __log2f(l_run)) * kLn2;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H,
+                          int window, float scale, int* err, cudaStream_t st) {
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBN) ||
+        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBN))
+        return cudaErrorInvalidValue;
+    FwdParams p;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.W = (window <= 0 || window >= T) ? T : window;
+    p.scale_log2 = scale * kLog2e;
+    p.n_pairs = (T + 2 * kBM - 1) / (2 * kBM);
+    p.err = err;
+    const int smem = FwdSmem<D>::kBytes + 1024;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set[dev] = true;
+    }
+    dim3 grid(p.n_pairs, H, B);
+    fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
+                       int window, float scale, int* err, cudaStream_t st) {
+    return D == 128 ? launch_fwd_tc<128>(q, k, v, o, lse, B, T, H, window, scale, err, st)
+                    : launch_fwd_tc<64>(q, k, v, o, lse, B, T, H, window, scale, err, st);
+}
+
+}  // namespace nc

@@ -1,10 +1,10 @@
-// Warp-per-row CUDA-core attention (forward and backward).
+// Warp-per-row CUDA-core attention backward.
 //
-// One warp owns one query row (forward, dQ) or one key row (dK/dV) and walks
-// the keys/queries that the causal window makes visible, recomputing scores
-// from the definition in fp32 (see the C ABI header for the operation and
-// its sources).  These kernels are the plain first CUDA path; the tensor-core
-// kernels replace them on the hot path.
+// One warp owns one query row (dQ) or one key row (dK/dV) and walks the
+// keys/queries that the causal window makes visible, recomputing the softmax
+// weights from the stored log-sum-exp in fp32 (see the C ABI header for the
+// operation and its sources).  This is the plain first CUDA path of the
+// backward; the tensor-core kernel replaces it on the hot path.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -45,45 +45,6 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* p, const float (&f)[E],
 }
 
 __device__ __forceinline__ int eff_window(int window, int T) { return (window <= 0 || window >= T) ? T : window; }
-
-template <int D>
-__global__ void __launch_bounds__(256) fwd_rowwarp(const __nv_bfloat16* __restrict__ q,
-                                                   const __nv_bfloat16* __restrict__ k,
-                                                   const __nv_bfloat16* __restrict__ v, __nv_bfloat16* __restrict__ o,
-                                                   float* __restrict__ lse, int B, int T, int H, int window,
-                                                   float scale_log2) {
-    constexpr int E = D / 32;
-    const long gw = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (gw >= (long)B * T * H) return;
-    const int h = gw % H;
-    const int i = (gw / H) % T;
-    const int b = gw / ((long)H * T);
-    const int W = eff_window(window, T);
-    const int lo = i - W + 1 < 0 ? 0 : i - W + 1;
-    const size_t rs = (size_t)H * D;
-    const size_t base = (size_t)b * T * rs + (size_t)h * D + lane * E;
-    float qf[E], acc[E];
-    load_row<E>(q + base + (size_t)i * rs, qf);
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    for (int j = lo; j <= i; ++j) {
-        float kf[E], vf[E];
-        load_row<E>(k + base + (size_t)j * rs, kf);
-        load_row<E>(v + base + (size_t)j * rs, vf);
-        const float s = warp_dot<E>(qf, kf) * scale_log2;
-        const float m_new = fmaxf(m, s);
-        const float alpha = exp2f(m - m_new);
-        const float p = exp2f(s - m_new);
-        l = l * alpha + p;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vf[e], acc[e] * alpha);
-        m = m_new;
-    }
-    store_row<E>(o + base + (size_t)i * rs, acc, 1.f / l);
-    if (lane == 0) lse[((size_t)b * H + h) * T + i] = (m + log2f(l)) * kLn2;
-}
 
 // Delta_i = sum_d dO_id * O_id for every row.
 template <int D>
@@ -189,18 +150,6 @@ __global__ void __launch_bounds__(256) bwd_dkdv_rowwarp(const __nv_bfloat16* __r
 }
 
 template <int D>
-cudaError_t fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H,
-                     int window, float scale, cudaStream_t st) {
-    const long rows = (long)B * T * H;
-    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-    fwd_rowwarp<D><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
-                                           (const __nv_bfloat16*)v, (__nv_bfloat16*)o, lse, B, T, H, window,
-                                           scale * kLog2e);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
-template <int D>
 cudaError_t bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                      void* dq, void* dk, void* dv, int B, int T, int H, int window, float scale, float* delta,
                      cudaStream_t st) {
@@ -220,13 +169,6 @@ cudaError_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
 }
 
 }  // namespace
-
-cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
-                       int window, float scale, int* err, cudaStream_t st) {
-    (void)err;
-    return D == 128 ? fwd_impl<128>(q, k, v, o, lse, B, T, H, window, scale, st)
-                    : fwd_impl<64>(q, k, v, o, lse, B, T, H, window, scale, st);
-}
 
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,

@@ -196,9 +196,12 @@ def test_decode_full_size_poisoned(nc, oracle_mod, window):
 @pytest.mark.parametrize("D,window", [(64, 1), (64, 100), (128, 5), (128, -1), (64, -1)])
 def test_decode_small(nc, oracle_mod, D, window):
     wl = workloads.DecodeWorkload("small", 7, 700, 3, D, 1, 700, (window,), 4242 + D)
-    q, kc, vc, lens = workloads.make_decode(wl, "cuda", poison_tail=True)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda")
     lens[0] = 1
     lens[1] = 700
+    dead = (torch.arange(wl.Tmax, device="cuda").view(1, -1) >= lens.view(-1, 1)).view(wl.N, wl.Tmax, 1, 1)
+    kc.masked_fill_(dead, float("nan"))
+    vc.masked_fill_(dead, float("nan"))
     o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
     assert nc.nc_get_device_error() == 0
     o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
