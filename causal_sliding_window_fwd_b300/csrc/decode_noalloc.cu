@@ -1,0 +1,92 @@
+// Decode entry point that allocates nothing and takes no workspace.
+//
+// Some callers cannot call cudaMalloc at the point where they decode:
+// inference engines whose own allocator has reserved the device memory up
+// front (a further cudaMalloc fails or fragments their pool), plug-ins that
+// are handed only their input and output buffers, and latency-critical token
+// loops that cannot afford the device-wide synchronisation cudaMalloc and
+// cudaFree may imply.  nc_attn_decode_noalloc serves them: its split-K partial
+// results go to a fixed scratch array in this library's own device memory (a
+// file-scope __device__ array, so every GPU that loads the library holds it
+// until the process exits).  It runs the same kernels as nc_attn_decode.
+//
+// The first call on each device looks up the array's device address
+// (cudaGetSymbolAddress) with that device current; make that first call
+// before any stream capture.  All calls on a device share the one array, so
+// calls whose work overlaps on the GPU (other streams, other host threads)
+// race on it and must be serialised by the caller.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nc_attn.h"
+#include "nc_decode.h"
+#include "nc_kernels.h"
+
+namespace {
+
+// Scratch for the partial (max, sum) pairs and unnormalised outputs of every
+// split.  Shared by all calls on a device; no part of it needs to start at
+// zero, because the combine pass reads only the splits the split pass wrote.
+static __device__ __align__(256) unsigned char g_decode_scratch[NC_DECODE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device.  Looked up once
+// per device: host code may not pass the symbol itself to a kernel, since in
+// host code it names a host-side stand-in, not device memory.
+void* scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t nc_attn_decode_noalloc_scratch_bytes(int N, int Tmax, int H, int D, int window) {
+    if (N <= 0 || Tmax <= 0 || H <= 0 || (D != 64 && D != 128) || (window < 1 && window != NC_WINDOW_FULL)) return 0;
+    const int chunk = nc::decode_chunk_rows(D);
+    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
+    const size_t parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
+    return round_up(parts * 2 * 4, 256) + parts * D * 4;
+}
+
+nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
+                                 void* o, float* lse, int N, int Tmax, int H, int D, int window, float scale,
+                                 cudaStream_t stream) {
+    if (N <= 0 || Tmax <= 0 || H <= 0 || D <= 0) return NC_ERR_INVALID;
+    if ((window < 1 && window != NC_WINDOW_FULL) || !(scale > 0.f) || scale > 3.4e38f) return NC_ERR_INVALID;
+    if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
+    if ((int64_t)N * H >= (int64_t(1) << 31) || (int64_t)Tmax * H * D >= (int64_t(1) << 40)) return NC_ERR_UNSUPPORTED;
+    if (!q || !kcache || !vcache || !cache_lens || !o) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return NC_ERR_INVALID;
+    if (o == q || o == kcache || o == vcache || (lse != nullptr && (void*)lse == o)) return NC_ERR_INVALID;
+    const size_t need = nc_attn_decode_noalloc_scratch_bytes(N, Tmax, H, D, window);
+    if (need > (size_t)NC_DECODE_NOALLOC_SCRATCH_BYTES) return NC_ERR_WORKSPACE;
+    unsigned char* scratch = static_cast<unsigned char*>(scratch_address());
+    int* err = nc::device_error_word();
+    if (scratch == nullptr || err == nullptr) return NC_ERR_CUDA;
+    const int chunk = nc::decode_chunk_rows(D);
+    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
+    const size_t parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
+    float* part_ml = reinterpret_cast<float*>(scratch);
+    float* part_o = reinterpret_cast<float*>(scratch + round_up(parts * 2 * 4, 256));
+    const cudaError_t e = nc::launch_decode(q, kcache, vcache, cache_lens, o, lse, N, Tmax, H, D, window, scale,
+                                            part_ml, part_o, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+}  // extern "C"

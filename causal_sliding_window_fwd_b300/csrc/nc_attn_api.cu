@@ -186,6 +186,7 @@ namespace nc {
 namespace {
 std::atomic<unsigned long long> g_launches{0};
 }
+int* device_error_word() { return error_word(); }
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 }  // namespace nc

@@ -8,6 +8,9 @@ namespace nc {
 void count_launches(unsigned n);
 unsigned long long launch_count();
 
+// Device address of the library's sticky error word on the current device (nullptr on failure).
+int* device_error_word();
+
 // Forward: o [B,T,H,D] bf16, lse [B,H,T] fp32.  `err` is the device error word.
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);

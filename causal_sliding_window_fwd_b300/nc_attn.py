@@ -28,7 +28,11 @@ NC_WINDOW_FULL = -1
 
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
-            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_get_device_error", "nc_launch_count")
+            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_get_device_error", "nc_launch_count",
+            "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc")
+
+# Size of the library's fixed decode scratch array (NC_DECODE_NOALLOC_SCRATCH_BYTES).
+NC_DECODE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class NcError(RuntimeError):
@@ -59,6 +63,10 @@ def _load():
     lib.nc_get_device_error.restype = i
     lib.nc_launch_count.argtypes = []
     lib.nc_launch_count.restype = ctypes.c_ulonglong
+    lib.nc_attn_decode_noalloc_scratch_bytes.argtypes = [i, i, i, i, i]
+    lib.nc_attn_decode_noalloc_scratch_bytes.restype = sz
+    lib.nc_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.nc_attn_decode_noalloc.restype = i
     return lib
 
 
@@ -148,6 +156,31 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: fl
     _check(lib.nc_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
                               N, Tmax, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
                               _stream(q.device, stream)), "nc_attn_decode")
+
+
+def nc_attn_decode_noalloc_scratch_bytes(N: int, Tmax: int, H: int, D: int, window: int) -> int:
+    return int(lib.nc_attn_decode_noalloc_scratch_bytes(N, Tmax, H, D, int(window)))
+
+
+def nc_attn_decode_noalloc(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, stream=None) -> None:
+    """Decode for callers that cannot allocate: no workspace argument, nothing allocated.
+
+    The partial results go to a fixed scratch array inside the library (see
+    NC_DECODE_NOALLOC_SCRATCH_BYTES); calls that would need more raise NcError
+    with NC_ERR_WORKSPACE.  Calls whose GPU work overlaps share that array and
+    race; keep them ordered (one stream).
+    """
+    N, Tmax, H, D = kcache.shape
+    _need(q, "q", torch.bfloat16, (N, H, D))
+    _need(kcache, "kcache", torch.bfloat16)
+    _need(vcache, "vcache", torch.bfloat16, (N, Tmax, H, D))
+    _need(cache_lens, "cache_lens", torch.int32, (N,))
+    _need(o, "o", torch.bfloat16, (N, H, D))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (N, H))
+    _check(lib.nc_attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
+                                      N, Tmax, H, D, int(window), float(scale), _stream(q.device, stream)),
+           "nc_attn_decode_noalloc")
 
 
 def nc_get_device_error(stream=None, device=None) -> int:

@@ -132,6 +132,36 @@ nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, 
 nc_status nc_get_device_error(int* code, cudaStream_t stream);
 
 /*
+ * Decode without a caller-provided workspace and without allocating.  The
+ * pages describe nothing of the kind: this entry point exists for callers
+ * that cannot allocate device memory when they decode (engines whose own
+ * allocator owns the device memory, plug-ins handed only their input and
+ * output buffers, token loops that cannot pay for the synchronisation that
+ * cudaMalloc/cudaFree may imply).
+ *
+ * Same arguments, layout and results as nc_attn_decode, minus the workspace.
+ * The split-K partials go to a fixed scratch array of
+ * NC_DECODE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  Calls needing more
+ * scratch than that (see nc_attn_decode_noalloc_scratch_bytes) return
+ * NC_ERR_WORKSPACE and launch nothing.  The call never allocates.
+ *
+ * The first call on a device looks up the scratch array's device address with
+ * that device current; make it before any stream capture.  All calls on a
+ * device share the array (it keeps the last call's contents; nothing in it
+ * needs to start at zero), so calls whose GPU work overlaps race on it: the
+ * caller must order them, e.g. on one stream.
+ */
+#define NC_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Scratch bytes nc_attn_decode_noalloc would use for these sizes (0 if invalid). */
+size_t nc_attn_decode_noalloc_scratch_bytes(int N, int Tmax, int H, int D, int window);
+
+nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
+                                 void* o, float* lse, int N, int Tmax, int H, int D, int window, float scale,
+                                 cudaStream_t stream);
+
+/*
  * Number of CUDA kernels this library has enqueued (all devices, all
  * streams) since it was loaded.  Host-side counter, for launch accounting in
  * benchmarks; it does not synchronise and never fails.
