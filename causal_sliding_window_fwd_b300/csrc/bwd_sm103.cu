@@ -1,0 +1,508 @@
+// Backward attention on 5th-generation tensor cores (tcgen05, TMEM, TMA) for sm_103a.
+//
+// Operation (see include/nc_attn.h): gradients of sum(O * dO) for exact causal
+// sliding-window softmax attention ("nanochat GPT-2 speedrun" post, page 2,
+// FlashAttention-3 window_size paragraph).  With P the softmax weights
+// recomputed from the forward's log-sum-exp and Delta_i = rowsum(dO_i * O_i):
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - Delta),  dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three launches on the caller's stream:
+//   bwd_pre   Delta = rowsum(dO * O) (fp32) and zeroing of the fp32 dQ accumulator
+//   bwd_main  one CTA per (128-key block, head, batch) walks the query blocks
+//             whose window reaches its keys; dK and dV accumulate in TMEM and
+//             the block's dQ contribution is added to the fp32 accumulator
+//   bwd_post  dq = bf16(scale * dQ accumulator)
+//
+// bwd_main warp roles:
+//   warp 0      TMA producer: K and V once, then Q and dO blocks through a
+//               2-stage ring (128-byte swizzle)
+//   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
+//   warps 4-7   one thread per key row: P^T and dS^T from S^T and dP^T, then
+//               the dK / dV epilogue
+//   warps 8-11  one thread per query row: dQ partial from TMEM into the fp32
+//               accumulator with vector atomics
+// TMEM: ST [0,128) holds S^T, then P^T (bf16) in its first 64 columns, then
+//       the block's dQ; DPT [128,256) holds dP^T, then dS^T (bf16);
+//       DV [256,256+D); DK [256+D,256+2D).
+// Products per query block m:
+//   dP^T = V dO_m^T, S^T = K Q_m^T            (both operands K-major in smem)
+//   dV += P^T dO_m, dK += dS^T Q_m            (A from TMEM, B MN-major in smem)
+//   dQ_m = dS K                                (A = dS MN-major in smem, B = K MN-major)
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "nc_attn.h"
+#include "nc_kernels.h"
+#include "nc_ptx.cuh"
+#include "nc_tma.h"
+
+namespace nc {
+namespace {
+
+constexpr int kBK = 128;       // keys per CTA
+constexpr int kBQ = 128;       // queries per block
+constexpr int kQStages = 2;
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdSmem {
+    static constexpr int kTile = kBQ * D * 2;            // 128 rows x D bf16
+    static constexpr int kK = 0;
+    static constexpr int kV = kK + kTile;
+    static constexpr int kQ = kV + kTile;                 // kQStages tiles
+    static constexpr int kDO = kQ + kQStages * kTile;     // kQStages tiles
+    static constexpr int kDS = kDO + kQStages * kTile;    // dS [key][query], 128 x 128 bf16
+    static constexpr int kDSBytes = kBK * kBQ * 2;
+    static constexpr int kLse = kDS + kDSBytes;           // [2][128] fp32 (log2 units)
+    static constexpr int kDelta = kLse + 2 * kBQ * 4;     // [2][128] fp32
+    static constexpr int kBars = kDelta + 2 * kBQ * 4;
+    static constexpr int kBytes = kBars + 256;
+};
+
+struct BwdBarriers {
+    uint64_t kv_full;
+    uint64_t qdo_full[kQStages];
+    uint64_t qdo_empty[kQStages];
+    uint64_t s_full;
+    uint64_t p_full;
+    uint64_t dq_full;
+    uint64_t dq_empty;
+    uint64_t final_;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct BwdParams {
+    const float* lse;      // [B, H, T]
+    const float* delta;    // [B, H, T]
+    float* dq_acc;         // [B, T, H, D]
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int B, T, H, W;        // W effective, 1 <= W <= T
+    float scale, scale_log2;
+    int n_kb, n_qb;
+    int* err;
+};
+
+__device__ __forceinline__ bool aborted(const BwdBarriers* bars) {
+    return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
+}
+
+__device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
+    set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
+    atomicExch(&bars->abort, 1);
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdParams p) {
+    using L = BwdSmem<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + L::kBars);
+    float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
+    float* s_delta = reinterpret_cast<float*>(smem + L::kDelta);
+
+    const int warp = warp_id(), lane = lane_id();
+    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int j0 = n * kBK;
+    const int m_lo = n;
+    const int m_hi = min(p.n_qb - 1, (j0 + kBK - 1 + p.W - 1) / kBQ);
+    const int n_it = m_hi - m_lo + 1;
+
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->kv_full, 1);
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(&bars->qdo_full[s], 1);
+            mbar_init(&bars->qdo_empty[s], 1);
+        }
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->p_full, kBK);
+        mbar_init(&bars->dq_full, 1);
+        mbar_init(&bars->dq_empty, kBQ);
+        mbar_init(&bars->final_, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
+
+    // registers: 384 x 168 at launch = 64512; producer/MMA warpgroup drops to 72,
+    // the P/dS warpgroup rises to 232 and the dQ warpgroup to 200 (64512 in all)
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        regs_decrease<72>();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTile);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_4d(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, h, j0, b);
+                tma_load_4d(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, h, j0, b);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % kQStages;
+                if (!mbar_wait(&bars->qdo_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
+                    record_timeout(bars, p.err);
+                    break;
+                }
+                const int i0 = (m_lo + it) * kBQ;
+                mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * L::kTile);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_4d(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->qdo_full[st], c * 64, h,
+                                i0, b);
+                    tma_load_4d(smem + L::kDO + st * L::kTile + c * kBQ * 128, &tm_do, &bars->qdo_full[st], c * 64,
+                                h, i0, b);
+                }
+                issued = it + 1;
+            }
+            for (int it = issued - kQStages < 0 ? 0 : issued - kQStages; it < issued; ++it)
+                mbar_wait(&bars->qdo_full[it % kQStages], (it / kQStages) & 1);
+            mbar_wait(&bars->kv_full, 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        regs_decrease<72>();
+        if (lane == 0) {
+            constexpr uint32_t id_kq = idesc_bf16(kBK, kBQ, false, false);  // S^T, dP^T
+            constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
+            constexpr uint32_t id_qd = idesc_bf16(kBQ, D, true, true);      // dQ (A and B MN-major)
+            const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+            const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+            const uint32_t sDS = smem_u32(smem + L::kDS);
+            bool ok = mbar_wait(&bars->kv_full, 0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it % kQStages;
+                ok = mbar_wait(&bars->qdo_full[st], (it / kQStages) & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t q_a = sQ + st * L::kTile, do_a = sDO + st * L::kTile;
+                // dP^T = V dO^T  (DPT is free: the previous dK product was issued before)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kBQ * 128) + (kk % 4) * 32;
+                    mma_ss(tmem + kColDPT, sdesc(sV + off, 16, 1024), sdesc(do_a + off, 16, 1024), id_kq, kk > 0);
+                }
+                // S^T = K Q^T once the previous dQ has been read out of ST
+                if (it > 0) {
+                    ok = mbar_wait(&bars->dq_empty, (it - 1) & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kBQ * 128) + (kk % 4) * 32;
+                    mma_ss(tmem + kColST, sdesc(sK + off, 16, 1024), sdesc(q_a + off, 16, 1024), id_kq, kk > 0);
+                }
+                mma_commit(&bars->s_full);
+                ok = mbar_wait(&bars->p_full, it & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                // dV += P^T dO ; dK += dS^T Q   (K = 128 queries, 16 per product)
+#pragma unroll
+                for (int kk = 0; kk < kBQ / 16; ++kk) {
+                    mma_ts(tmem + kColDV, tmem + kColST + kk * 8, sdesc(do_a + kk * 2048, kBQ * 128, 1024), id_kd,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + kColDK, tmem + kColDPT + kk * 8, sdesc(q_a + kk * 2048, kBQ * 128, 1024), id_kd,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->qdo_empty[st]);
+                // dQ_m = dS K  (M = queries, K = keys, N = D), into ST
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_ss(tmem + kColST, sdesc(sDS + kk * 2048, kBQ * 128, 1024),
+                           sdesc(sK + kk * 2048, kBK * 128, 1024), id_qd, kk > 0);
+                mma_commit(&bars->dq_full);
+            }
+            if (!ok) record_timeout(bars, p.err);
+            mma_commit(&bars->final_);
+            mma_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        regs_decrease<72>();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T / dS^T (thread = key row)
+        regs_increase<232>();
+        const int tid = threadIdx.x - 128;
+        const int lane_base = 32 * (warp % 4);
+        const int j = j0 + tid;
+        const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
+        const uint32_t dpt_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;
+        uint8_t* ds_row = smem + L::kDS + tid * 128;
+        const float sl2 = p.scale_log2;
+        const size_t rowvec = (static_cast<size_t>(b) * p.H + h) * p.T;
+        // row statistics of the next query block are loaded one iteration ahead
+        auto stat_lse = [&](int i) { return (i < p.T) ? p.lse[rowvec + i] * kLog2e : INFINITY; };
+        auto stat_delta = [&](int i) { return (i < p.T) ? p.delta[rowvec + i] : 0.f; };
+        float nx_lse = stat_lse(m_lo * kBQ + tid), nx_delta = stat_delta(m_lo * kBQ + tid);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int m = m_lo + it;
+            const int i0 = m * kBQ;
+            float* lbw = s_lse + (it & 1) * kBQ;
+            float* dbw = s_delta + (it & 1) * kBQ;
+            lbw[tid] = nx_lse;
+            dbw[tid] = nx_delta;
+            if (it + 1 < n_it) {
+                nx_lse = stat_lse(i0 + kBQ + tid);
+                nx_delta = stat_delta(i0 + kBQ + tid);
+            }
+            named_bar_sync(1, 128);
+            const float* lb = s_lse + (it & 1) * kBQ;
+            const float* db = s_delta + (it & 1) * kBQ;
+            ok = mbar_wait(&bars->s_full, it & 1) && !aborted(bars);
+            if (!ok) break;
+            tc_fence_after();
+            const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
+#pragma unroll 1
+            for (int hq = 0; hq < 2; ++hq) {  // 64-query halves
+                uint32_t sr[64], dr[64];
+                tmem_ld64x2(st_addr + hq * 64, dpt_addr + hq * 64, sr, dr);
+                uint32_t pk[32], dk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int qi = hq * 64 + 2 * x + y;
+                        float pr = ex2_approx(fmaf(__uint_as_float(sr[2 * x + y]), sl2, -lb[qi]));
+                        if (!full) {
+                            const int i = i0 + qi;
+                            if (j > i || i - j >= p.W) pr = 0.f;
+                        }
+                        pv[y] = pr;
+                        dsv[y] = pr * (__uint_as_float(dr[2 * x + y]) - db[qi]);
+                    }
+                    pk[x] = pack_bf16x2(pv[0], pv[1]);
+                    dk[x] = pack_bf16x2(dsv[0], dsv[1]);
+                }
+                // P^T and dS^T (bf16) over the TMEM columns this thread has already read
+                tmem_st32(st_addr + hq * 32, pk);
+                tmem_st32(dpt_addr + hq * 32, dk);
+                // dS row into the MN-major [key][query] tile: query chunk hq, eight 16-byte units
+                uint8_t* chunk = ds_row + hq * (kBK * 128);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint4 v;
+                    v.x = dk[4 * u + 0];
+                    v.y = dk[4 * u + 1];
+                    v.z = dk[4 * u + 2];
+                    v.w = dk[4 * u + 3];
+                    *reinterpret_cast<uint4*>(chunk + ((u ^ (tid & 7)) << 4)) = v;
+                }
+            }
+            tmem_wait_st();
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full);
+        }
+        // epilogue: dK = scale * DK, dV = DV  (rows of this key block)
+        if (ok) ok = mbar_wait(&bars->final_, 0) && !aborted(bars);
+        if (!ok) {
+            record_timeout(bars, p.err);
+        } else {
+            tc_fence_after();
+            const bool in_range = j < p.T;
+            const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.H + h) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (which ? kColDV : kColDK);
+                const float mul = which ? 1.f : p.scale;
+                __nv_bfloat16* dst = (which ? p.dv : p.dk) + off;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(a + c * 32, r);
+                    if (in_range) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 pkt;
+                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+                            reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ partials (thread = query row)
+        regs_increase<200>();
+        const int tid = threadIdx.x - 256;
+        const int lane_base = 32 * (warp % 4);
+        const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
+        for (int it = 0; it < n_it; ++it) {
+            const int i = (m_lo + it) * kBQ + tid;
+            if (!mbar_wait(&bars->dq_full, it & 1) || aborted(bars)) {
+                record_timeout(bars, p.err);
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[D];
+            if constexpr (D == 128) {
+                tmem_ld128(st_addr, r);
+            } else {
+                uint32_t a[32], c[32];
+                tmem_ld32(st_addr, a);
+                tmem_ld32(st_addr + 32, c);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    r[x] = a[x];
+                    r[32 + x] = c[x];
+                }
+            }
+            // the block's dQ is in registers: hand the TMEM columns back before the atomics
+            tc_fence_before();
+            mbar_arrive(&bars->dq_empty);
+            if (i < p.T) {
+                float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
+#pragma unroll
+                for (int v4 = 0; v4 < D / 4; ++v4)
+                    red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                                  __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Delta = rowsum(dO * O) per (b, h, i) and a zeroed dQ accumulator.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      float* __restrict__ delta, float* __restrict__ dq_acc, int B,
+                                                      int T, int H) {
+    constexpr int E = D / 32;
+    const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= (long)B * T * H) return;
+    const int h = row % H;
+    const int i = (row / H) % T;
+    const int b = row / ((long)H * T);
+    const size_t off = (size_t)row * D + lane * E;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + off + e));
+        const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dO + off + e));
+        acc = fmaf(a.x, g.x, fmaf(a.y, g.y, acc));
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) delta[((size_t)b * H + h) * T + i] = acc;
+    if constexpr (E == 4) {
+        reinterpret_cast<float4*>(dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        reinterpret_cast<float2*>(dq_acc + off)[0] = make_float2(0.f, 0.f);
+    }
+}
+
+// dq = bf16(scale * dQ accumulator), 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc,
+                                                       __nv_bfloat16* __restrict__ dq, size_t n8, float scale) {
+    const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n8) return;
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
+    const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
+    uint4 pkt;
+    pkt.x = pack_bf16x2(a.x * scale, a.y * scale);
+    pkt.y = pack_bf16x2(a.z * scale, a.w * scale);
+    pkt.z = pack_bf16x2(c.x * scale, c.y * scale);
+    pkt.w = pack_bf16x2(c.z * scale, c.w * scale);
+    reinterpret_cast<uint4*>(dq)[t] = pkt;
+}
+
+template <int D>
+cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
+                          float scale, float* dq_acc, float* delta, int* err, cudaStream_t st) {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
+        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ))
+        return cudaErrorInvalidValue;
+    const long rows = (long)B * T * H;
+    bwd_pre_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta, dq_acc, B, T, H);
+    BwdParams p;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq_acc = dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.W = (window <= 0 || window >= T) ? T : window;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.n_kb = (T + kBK - 1) / kBK;
+    p.n_qb = (T + kBQ - 1) / kBQ;
+    p.err = err;
+    const int smem = BwdSmem<D>::kBytes;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set[dev] = true;
+    }
+    dim3 grid(p.n_kb, H, B);
+    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, p);
+    const size_t n8 = (size_t)rows * D / 8;
+    bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
+                                                                 scale);
+    count_launches(3);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                       void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
+                       float* dq_acc, float* delta, int* err, cudaStream_t st) {
+    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, err,
+                                         st)
+                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, err,
+                                        st);
+}
+
+}  // namespace nc

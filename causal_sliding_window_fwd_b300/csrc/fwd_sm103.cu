@@ -131,14 +131,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    // 384 threads x 168 registers at launch = 128 x 56 (producer/MMA warpgroup) + 256 x 224 (softmax);
+    // 384 threads x 168 registers at launch = 128 x 72 (producer/MMA warpgroup) + 256 x 216 (softmax);
     // each role sets its budget at the top of its own branch
     const uint32_t col_s[2] = {0u, 128u};
     const uint32_t col_o[2] = {256u, 256u + D};
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        regs_decrease<56>();
+        regs_decrease<72>();
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -172,7 +172,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        regs_decrease<56>();
+        regs_decrease<72>();
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
@@ -251,37 +251,41 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         __syncwarp();
     } else if (warp < 4) {
-        regs_decrease<56>();
+        regs_decrease<72>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        regs_increase<224>();
+        regs_increase<216>();
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
-        const int row = r0[t] + row_in_tile;
+        const int tr0 = t ? r0[1] : r0[0];
+        const int t_lo = t ? lo[1] : lo[0];
+        const int t_hi = t ? hi[1] : hi[0];
+        const uint32_t t_col_s = t ? col_s[1] : col_s[0];
+        const uint32_t t_col_o = t ? col_o[1] : col_o[0];
+        const int row = tr0 + row_in_tile;
         const bool tile_on = (t == 0) || active1;
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         if (tile_on) {
-            const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + col_s[t];
-            const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + col_o[t];
+            const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_s;
+            const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_o;
             int it = 0;
-            for (int kb = lo[t]; kb <= hi[t]; ++kb, ++it) {
+            for (int kb = t_lo; kb <= t_hi; ++kb, ++it) {
                 ok = mbar_wait(&bars.s_full[t], it & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
                 float s[kBN];
+                {
+                    uint32_t r[kBN];
+                    tmem_ld128(s_addr, r);
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(s_addr + c * 32, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
                 }
                 // elementwise mask only on blocks that straddle the causal diagonal or the window edge
                 const int k0 = kb * kBN;
-                const bool full_block = (k0 + kBN - 1 <= r0[t]) && (k0 >= r0[t] + kBM - p.W);
+                const bool full_block = (k0 + kBN - 1 <= tr0) && (k0 >= tr0 + kBM - p.W);
                 if (!full_block) {
 #pragma unroll
                     for (int j = 0; j < kBN; ++j) {

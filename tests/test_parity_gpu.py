@@ -5,7 +5,11 @@ Tolerances, max over all compared elements:
   log-sum-exp     |L - L_ref|   <= 1e-3 (absolute)
   gradients       |dX - dX_ref| <= 3e-2 * max|dX_ref|   for X in q, k, v
 The inputs are bf16 and the kernels accumulate in fp32; the oracle sees the
-same bf16 tensors widened exactly to fp64.
+same bf16 tensors widened exactly to fp64.  Where the reference is identically
+zero (dQ and dK for a window of 1) the scale max|ref| is floored at 1e-4: the
+fp32 rounding noise of dP - Delta (two sums of D products in different
+orders) then has to stay below 3e-6.  Gradients of every other case are of
+order 0.1 to 1, so the floor never loosens them.
 """
 import math
 
@@ -32,7 +36,7 @@ def rel_err(got, ref):
     got = got.detach().float().cpu().numpy() if torch.is_tensor(got) else got
     ref = np.asarray(ref)
     assert np.isfinite(got).all(), "non-finite values in GPU output"
-    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
 
 
 def abs_err(got, ref):
@@ -96,6 +100,7 @@ def test_window_one_is_exact_identity(nc):
     o, lse, dq, dk, dv = run_fwd_bwd(nc, q, k, v, dO, 1, 0.088)
     assert torch.equal(o, v)
     torch.testing.assert_close(dv, dO, rtol=0, atol=0)
+    assert dq.float().abs().max().item() < 1e-5 and dk.float().abs().max().item() < 1e-5
 
 
 def test_scale_other_than_default(nc, oracle_mod):
