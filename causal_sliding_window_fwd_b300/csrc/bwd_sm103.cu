@@ -17,12 +17,15 @@
 //   warp 0      TMA producer: K and V once, then Q and dO blocks through a
 //               2-stage ring (128-byte swizzle)
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
-//   warps 4-7   one thread per key row: P^T and dS^T from S^T and dP^T, then
-//               the dK / dV epilogue
-//   warps 8-11  one thread per query row: dQ partial from TMEM into the fp32
+//   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T
+//               from S^T and dP^T; then the dK epilogue
+//   warps 8-11  the same for query columns [64, 128); then the dV epilogue
+//   warps 12-15 one thread per query row: dQ partial from TMEM into the fp32
 //               accumulator with vector atomics
-// TMEM: ST [0,128) holds S^T, then P^T (bf16) in its first 64 columns, then
-//       the block's dQ; DPT [128,256) holds dP^T, then dS^T (bf16);
+// TMEM: ST [0,128) holds S^T, then P^T (bf16, two per column) in columns
+//       [0,32) for queries 0-63 and [64,96) for queries 64-127, so each
+//       warpgroup overwrites only columns it has already read; then the
+//       block's dQ.  DPT [128,256) holds dP^T, then dS^T the same way.
 //       DV [256,256+D); DK [256+D,256+2D).
 // Products per query block m:
 //   dP^T = V dO_m^T, S^T = K Q_m^T            (both operands K-major in smem)
@@ -42,7 +45,7 @@ namespace {
 constexpr int kBK = 128;       // keys per CTA
 constexpr int kBQ = 128;       // queries per block
 constexpr int kQStages = 2;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -133,7 +136,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(&bars->qdo_empty[s], 1);
         }
         mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->p_full, kBK);
+        mbar_init(&bars->p_full, 2 * kBK);
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, kBQ);
         mbar_init(&bars->final_, 1);
@@ -151,133 +154,143 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tmem = bars->tmem_base;
     constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
 
-    // registers: 384 x 168 at launch = 64512; producer/MMA warpgroup drops to 72,
-    // the P/dS warpgroup rises to 232 and the dQ warpgroup to 200 (64512 in all)
+    // registers: 512 x 128 at launch = 65536; producer/MMA warpgroup drops to 96,
+    // the dQ warpgroup to 96, the two P/dS warpgroups rise to 160 (65536 in all)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        regs_decrease<72>();
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_do);
-            mbar_arrive_expect_tx(&bars->kv_full, 2 * L::kTile);
+        // the whole warp runs this loop converged; lane 0 issues each copy
+        regs_decrease<96>();
+        {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_do);
+            }
+            __syncwarp();
+            mbar_arrive_expect_tx_w(&bars->kv_full, 2 * L::kTile);
             for (int c = 0; c < D / 64; ++c) {
-                tma_load_4d(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, h, j0, b);
-                tma_load_4d(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, h, j0, b);
+                tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, h, j0, b);
+                tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, h, j0, b);
             }
             int issued = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int st = it % kQStages;
-                if (!mbar_wait(&bars->qdo_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
+                if (!mbar_wait_warp(&bars->qdo_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
                     record_timeout(bars, p.err);
                     break;
                 }
                 const int i0 = (m_lo + it) * kBQ;
-                mbar_arrive_expect_tx(&bars->qdo_full[st], 2 * L::kTile);
+                mbar_arrive_expect_tx_w(&bars->qdo_full[st], 2 * L::kTile);
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->qdo_full[st], c * 64, h,
+                    tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->qdo_full[st], c * 64, h,
                                 i0, b);
-                    tma_load_4d(smem + L::kDO + st * L::kTile + c * kBQ * 128, &tm_do, &bars->qdo_full[st], c * 64,
+                    tma_load_4d_w(smem + L::kDO + st * L::kTile + c * kBQ * 128, &tm_do, &bars->qdo_full[st], c * 64,
                                 h, i0, b);
                 }
                 issued = it + 1;
             }
             for (int it = issued - kQStages < 0 ? 0 : issued - kQStages; it < issued; ++it)
-                mbar_wait(&bars->qdo_full[it % kQStages], (it / kQStages) & 1);
-            mbar_wait(&bars->kv_full, 0);
+                mbar_wait_warp(&bars->qdo_full[it % kQStages], (it / kQStages) & 1);
+            mbar_wait_warp(&bars->kv_full, 0);
         }
-        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        regs_decrease<72>();
-        if (lane == 0) {
+        // the whole warp runs this loop converged; lane 0 issues each product
+        regs_decrease<96>();
+        {
             constexpr uint32_t id_kq = idesc_bf16(kBK, kBQ, false, false);  // S^T, dP^T
             constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
             constexpr uint32_t id_qd = idesc_bf16(kBQ, D, true, true);      // dQ (A and B MN-major)
             const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
             const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
             const uint32_t sDS = smem_u32(smem + L::kDS);
-            bool ok = mbar_wait(&bars->kv_full, 0);
+            // Descriptors are built once; each product adds a constant (bytes / 16) to the start field.
+            const uint64_t k_kmaj = sdesc(sK, 16, 1024), v_kmaj = sdesc(sV, 16, 1024);
+            const uint64_t q_kmaj = sdesc(sQ, 16, 1024), do_kmaj = sdesc(sDO, 16, 1024);
+            const uint64_t q_mn = sdesc(sQ, kBQ * 128, 1024), do_mn = sdesc(sDO, kBQ * 128, 1024);
+            const uint64_t ds_mn = sdesc(sDS, kBQ * 128, 1024), k_mn = sdesc(sK, kBK * 128, 1024);
+            constexpr uint64_t kTileStep = L::kTile >> 4;
+            constexpr uint64_t kChunk = (kBQ * 128) >> 4;
+            bool ok = mbar_wait_warp(&bars->kv_full, 0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % kQStages;
-                ok = mbar_wait(&bars->qdo_full[st], (it / kQStages) & 1) && !aborted(bars);
+                ok = mbar_wait_warp(&bars->qdo_full[st], (it / kQStages) & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t q_a = sQ + st * L::kTile, do_a = sDO + st * L::kTile;
+                const uint64_t q_k = q_kmaj + st * kTileStep, do_k = do_kmaj + st * kTileStep;
+                const uint64_t q_m = q_mn + st * kTileStep, do_m = do_mn + st * kTileStep;
                 // dP^T = V dO^T  (DPT is free: the previous dK product was issued before)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kBQ * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + kColDPT, sdesc(sV + off, 16, 1024), sdesc(do_a + off, 16, 1024), id_kq, kk > 0);
+                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                    mma_ss_w(tmem + kColDPT, v_kmaj + off, do_k + off, id_kq, kk > 0 ? 1u : 0u);
                 }
                 // S^T = K Q^T once the previous dQ has been read out of ST
                 if (it > 0) {
-                    ok = mbar_wait(&bars->dq_empty, (it - 1) & 1) && !aborted(bars);
+                    ok = mbar_wait_warp(&bars->dq_empty, (it - 1) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kBQ * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + kColST, sdesc(sK + off, 16, 1024), sdesc(q_a + off, 16, 1024), id_kq, kk > 0);
+                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                    mma_ss_w(tmem + kColST, k_kmaj + off, q_k + off, id_kq, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bars->s_full);
-                ok = mbar_wait(&bars->p_full, it & 1) && !aborted(bars);
+                mma_commit_w(&bars->s_full);
+                ok = mbar_wait_warp(&bars->p_full, it & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
                 // dV += P^T dO ; dK += dS^T Q   (K = 128 queries, 16 per product)
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk) {
-                    mma_ts(tmem + kColDV, tmem + kColST + kk * 8, sdesc(do_a + kk * 2048, kBQ * 128, 1024), id_kd,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem + kColDK, tmem + kColDPT + kk * 8, sdesc(q_a + kk * 2048, kBQ * 128, 1024), id_kd,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // packed P^T / dS^T columns
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts_w(tmem + kColDV, tmem + kColST + pc, do_m + kk * (2048 >> 4), id_kd, acc);
+                    mma_ts_w(tmem + kColDK, tmem + kColDPT + pc, q_m + kk * (2048 >> 4), id_kd, acc);
                 }
-                mma_commit(&bars->qdo_empty[st]);
+                mma_commit_w(&bars->qdo_empty[st]);
                 // dQ_m = dS K  (M = queries, K = keys, N = D), into ST
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_ss(tmem + kColST, sdesc(sDS + kk * 2048, kBQ * 128, 1024),
-                           sdesc(sK + kk * 2048, kBK * 128, 1024), id_qd, kk > 0);
-                mma_commit(&bars->dq_full);
+                    mma_ss_w(tmem + kColST, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bars->dq_full);
             }
             if (!ok) record_timeout(bars, p.err);
-            mma_commit(&bars->final_);
-            mma_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0);
+            mma_commit_w(&bars->final_);
+            mma_commit_w(&bars->drain);
+            mbar_wait_warp(&bars->drain, 0);
         }
-        __syncwarp();
     } else if (warp < 4) {
-        regs_decrease<72>();
-    } else if (warp >= 4 && warp < 8) {
+        regs_decrease<96>();
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ P^T / dS^T (thread = key row)
-        regs_increase<232>();
-        const int tid = threadIdx.x - 128;
+        regs_increase<160>();
+        const int g = (warp - 4) / 4;            // query columns [64 g, 64 g + 64)
+        const int tid = threadIdx.x - 128 * (g + 1);
         const int lane_base = 32 * (warp % 4);
         const int j = j0 + tid;
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
         const uint32_t dpt_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;
-        uint8_t* ds_row = smem + L::kDS + tid * 128;
+        uint8_t* ds_row = smem + L::kDS + g * (kBK * 128) + tid * 128;
         const float sl2 = p.scale_log2;
         const size_t rowvec = (static_cast<size_t>(b) * p.H + h) * p.T;
-        // row statistics of the next query block are loaded one iteration ahead
-        auto stat_lse = [&](int i) { return (i < p.T) ? p.lse[rowvec + i] * kLog2e : INFINITY; };
-        auto stat_delta = [&](int i) { return (i < p.T) ? p.delta[rowvec + i] : 0.f; };
-        float nx_lse = stat_lse(m_lo * kBQ + tid), nx_delta = stat_delta(m_lo * kBQ + tid);
+        // row statistics of this warpgroup's 64 queries, loaded one iteration ahead:
+        // threads 0-63 fetch lse, threads 64-127 fetch Delta
+        const bool fetch_lse = tid < 64;
+        const int qoff = 64 * g + (tid & 63);
+        auto stat = [&](int i) {
+            if (i >= p.T) return fetch_lse ? INFINITY : 0.f;
+            return fetch_lse ? p.lse[rowvec + i] * kLog2e : p.delta[rowvec + i];
+        };
+        float nx = stat(m_lo * kBQ + qoff);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int m = m_lo + it;
             const int i0 = m * kBQ;
-            float* lbw = s_lse + (it & 1) * kBQ;
-            float* dbw = s_delta + (it & 1) * kBQ;
-            lbw[tid] = nx_lse;
-            dbw[tid] = nx_delta;
-            if (it + 1 < n_it) {
-                nx_lse = stat_lse(i0 + kBQ + tid);
-                nx_delta = stat_delta(i0 + kBQ + tid);
-            }
-            named_bar_sync(1, 128);
+            (fetch_lse ? s_lse : s_delta)[(it & 1) * kBQ + qoff] = nx;
+            if (it + 1 < n_it) nx = stat(i0 + kBQ + qoff);
+            named_bar_sync(1 + g, 128);
             const float* lb = s_lse + (it & 1) * kBQ;
             const float* db = s_delta + (it & 1) * kBQ;
             ok = mbar_wait(&bars->s_full, it & 1) && !aborted(bars);
@@ -285,16 +298,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
 #pragma unroll 1
-            for (int hq = 0; hq < 2; ++hq) {  // 64-query halves
-                uint32_t sr[64], dr[64];
-                tmem_ld64x2(st_addr + hq * 64, dpt_addr + hq * 64, sr, dr);
-                uint32_t pk[32], dk[32];
+            for (int c = 0; c < 2; ++c) {  // 32-query chunks of this warpgroup's half
+                const int q0 = 64 * g + 32 * c;
+                uint32_t sr[32], dr[32];
+                tmem_ld32x2(st_addr + q0, dpt_addr + q0, sr, dr);
+                uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
+                for (int x = 0; x < 16; ++x) {
                     float pv[2], dsv[2];
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
-                        const int qi = hq * 64 + 2 * x + y;
+                        const int qi = q0 + 2 * x + y;
                         float pr = ex2_approx(fmaf(__uint_as_float(sr[2 * x + y]), sl2, -lb[qi]));
                         if (!full) {
                             const int i = i0 + qi;
@@ -306,19 +320,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     pk[x] = pack_bf16x2(pv[0], pv[1]);
                     dk[x] = pack_bf16x2(dsv[0], dsv[1]);
                 }
-                // P^T and dS^T (bf16) over the TMEM columns this thread has already read
-                tmem_st32(st_addr + hq * 32, pk);
-                tmem_st32(dpt_addr + hq * 32, dk);
-                // dS row into the MN-major [key][query] tile: query chunk hq, eight 16-byte units
-                uint8_t* chunk = ds_row + hq * (kBK * 128);
+                // packed into the first half of this warpgroup's own (already read) columns
+                tmem_st16(st_addr + 64 * g + 16 * c, pk);
+                tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
+                // dS row into the MN-major [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 4; ++u) {
+                    const int unit = 4 * c + u;
                     uint4 v;
                     v.x = dk[4 * u + 0];
                     v.y = dk[4 * u + 1];
                     v.z = dk[4 * u + 2];
                     v.w = dk[4 * u + 3];
-                    *reinterpret_cast<uint4*>(chunk + ((u ^ (tid & 7)) << 4)) = v;
+                    *reinterpret_cast<uint4*>(ds_row + ((unit ^ (tid & 7)) << 4)) = v;
                 }
             }
             tmem_wait_st();
@@ -326,7 +340,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before();
             mbar_arrive(&bars->p_full);
         }
-        // epilogue: dK = scale * DK, dV = DV  (rows of this key block)
+        // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV
         if (ok) ok = mbar_wait(&bars->final_, 0) && !aborted(bars);
         if (!ok) {
             record_timeout(bars, p.err);
@@ -334,33 +348,30 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             const bool in_range = j < p.T;
             const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.H + h) * D;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (which ? kColDV : kColDK);
-                const float mul = which ? 1.f : p.scale;
-                __nv_bfloat16* dst = (which ? p.dv : p.dk) + off;
+            const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
+            const float mul = g ? 1.f : p.scale;
+            __nv_bfloat16* dst = (g ? p.dv : p.dk) + off;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(a + c * 32, r);
-                    if (in_range) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(a + c * 32, r);
+                if (in_range) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
-                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
-                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
-                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
-                            reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
-                        }
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 pkt;
+                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+                        reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
                     }
                 }
             }
         }
-    } else if (warp >= 8) {
+    } else {
         // ------------------------------------------------------------ dQ partials (thread = query row)
-        regs_increase<200>();
-        const int tid = threadIdx.x - 256;
+        regs_decrease<96>();
+        const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
         for (int it = 0; it < n_it; ++it) {
@@ -370,28 +381,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             }
             tc_fence_after();
-            uint32_t r[D];
-            if constexpr (D == 128) {
-                tmem_ld128(st_addr, r);
-            } else {
-                uint32_t a[32], c[32];
-                tmem_ld32(st_addr, a);
-                tmem_ld32(st_addr + 32, c);
+            float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
+            const bool in_range = i < p.T;
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    r[x] = a[x];
-                    r[32 + x] = c[x];
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t r[64];
+                {
+                    uint32_t a[32], c2[32];
+                    tmem_ld32x2(st_addr + 64 * half, st_addr + 64 * half + 32, a, c2);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        r[x] = a[x];
+                        r[32 + x] = c2[x];
+                    }
                 }
-            }
-            // the block's dQ is in registers: hand the TMEM columns back before the atomics
-            tc_fence_before();
-            mbar_arrive(&bars->dq_empty);
-            if (i < p.T) {
-                float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
+                if (half == D / 64 - 1) {
+                    // the block's dQ is now in registers: hand the TMEM columns back before the last atomics
+                    tc_fence_before();
+                    mbar_arrive(&bars->dq_empty);
+                }
+                if (in_range) {
 #pragma unroll
-                for (int v4 = 0; v4 < D / 4; ++v4)
-                    red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                                  __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+                    for (int v4 = 0; v4 < 16; ++v4)
+                        red_add_f32x4(dst + 64 * half + 4 * v4, __uint_as_float(r[4 * v4]),
+                                      __uint_as_float(r[4 * v4 + 1]), __uint_as_float(r[4 * v4 + 2]),
+                                      __uint_as_float(r[4 * v4 + 3]));
+                }
             }
         }
     }

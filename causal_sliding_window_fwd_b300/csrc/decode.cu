@@ -24,6 +24,9 @@ namespace nc {
 
 namespace {
 
+// Up to 10 warps (one per head for the depth-20 shape); two CTAs fit per SM.
+constexpr int kDecodeMaxThreads = 320;
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -50,10 +53,18 @@ __device__ __forceinline__ int visible_lo(int L, int window) {
     return (window <= 0 || window >= L) ? 0 : L - window;
 }
 
-// One CTA = (split s, sequence n).  Warp w handles heads w, w + nwarps, ...
-// Lanes are grouped G = D / 8 per token; a warp handles 32 / G tokens per step.
+__device__ __forceinline__ float fast_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One CTA per (split s, sequence n) work item; item = s + n_splits * n.
+// Warp w handles heads w, w + nwarps, ...  Lanes are grouped G = D / 8 per token
+// row of one head; a warp covers TPS = 32 / G tokens per step and keeps U steps of
+// K and V loads in flight before it does any arithmetic on them.
 template <int D>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(kDecodeMaxThreads, 2)
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
                     float* __restrict__ part_ml, float* __restrict__ part_o, int N, int Tmax, int H,
@@ -61,87 +72,106 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     constexpr int G = D / 8;          // lanes per token row of one head
     constexpr int TPS = 32 / G;       // tokens per warp step
     constexpr int U = 4;              // steps in flight per iteration
-    const int s = blockIdx.x, n = blockIdx.y;
-    const int L = lens[n];
-    if (L < 1 || L > Tmax) return;  // reported by the combine kernel
-    const int lo = visible_lo(L, window);
-    const int t_begin = lo + s * chunk;
-    const int t_end = min(L, t_begin + chunk);
-    if (t_begin >= t_end) return;  // this split lies past the sequence's visible rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int g = lane / G;           // token slot within a step
     const int c = lane % G;           // 8-element column group
     const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
+    const int n_items = n_splits * N;
 
-    for (int h = warp; h < H; h += nwarps) {
-        float qf[8];
-        bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
-        float m = -INFINITY, l = 0.f, acc[8];
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int s = item % n_splits, n = item / n_splits;
+        const int L = lens[n];
+        if (L < 1 || L > Tmax) continue;  // reported by the combine kernel
+        const int lo = visible_lo(L, window);
+        const int t_begin = lo + s * chunk;
+        const int t_end = min(L, t_begin + chunk);
+        if (t_begin >= t_end) continue;  // this split lies past the sequence's visible rows
+        for (int h = warp; h < H; h += nwarps) {
+            float qf[8];
+            bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-        const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-        for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
-            uint4 kr[U], vr[U];
+            for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+            float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + u * TPS + g;
-                kr[u] = make_uint4(0, 0, 0, 0);
-                vr[u] = make_uint4(0, 0, 0, 0);
-                if (t < t_end) {
-                    kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
-                    vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+            const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+            for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
+                uint4 kr[U], vr[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int t = t0 + u * TPS + g;
+                    kr[u] = make_uint4(0, 0, 0, 0);
+                    vr[u] = make_uint4(0, 0, 0, 0);
+                    if (t < t_end) {
+                        kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
+                        vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
+                    }
                 }
-            }
+                // scores of the U tokens of this slot (log2 units), reduced across the G lanes
+                float sc[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + u * TPS + g;
-                float kf[8];
-                bf16x8_to_f32(kr[u], kf);
-                float dot = 0.f;
+                for (int u = 0; u < U; ++u) {
+                    float kf[8];
+                    bf16x8_to_f32(kr[u], kf);
+                    float dot = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+                    for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+                    sc[u] = dot;
+                }
 #pragma unroll
-                for (int off = G / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-                if (t < t_end) {
-                    const float sc = dot * scale_log2;
-                    const float m_new = fmaxf(m, sc);
-                    const float alpha = exp2f(m - m_new);
-                    const float p = exp2f(sc - m_new);
+                for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+                    for (int u = 0; u < U; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+                float mc = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (t0 + u * TPS + g >= t_end) sc[u] = -INFINITY;
+                    mc = fmaxf(mc, sc[u]);
+                }
+                const float m_new = fmaxf(m, mc);
+                if (m_new == -INFINITY) continue;  // every token of this slot lies past the end
+                const float alpha = fast_ex2(m - m_new);
+                l *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] *= alpha;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float p = fast_ex2(sc[u] - m_new);
                     float vf[8];
                     bf16x8_to_f32(vr[u], vf);
-                    l = l * alpha + p;
+                    l += p;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i] * alpha);
-                    m = m_new;
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
                 }
+                m = m_new;
             }
-        }
-        // merge the TPS token slots of this warp (lanes with equal c)
+            // merge the TPS token slots of this warp (lanes with equal c)
 #pragma unroll
-        for (int off = G; off < 32; off <<= 1) {
-            const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
-            const float l_o = __shfl_xor_sync(0xffffffffu, l, off);
-            const float m_new = fmaxf(m, m_o);
-            const float a_s = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
-            const float a_o = (m_o == -INFINITY) ? 0.f : exp2f(m_o - m_new);
+            for (int off = G; off < 32; off <<= 1) {
+                const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
+                const float l_o = __shfl_xor_sync(0xffffffffu, l, off);
+                const float m_new = fmaxf(m, m_o);
+                const float a_s = (m == -INFINITY) ? 0.f : fast_ex2(m - m_new);
+                const float a_o = (m_o == -INFINITY) ? 0.f : fast_ex2(m_o - m_new);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float o_o = __shfl_xor_sync(0xffffffffu, acc[i], off);
-                acc[i] = acc[i] * a_s + o_o * a_o;
+                for (int i = 0; i < 8; ++i) {
+                    const float o_o = __shfl_xor_sync(0xffffffffu, acc[i], off);
+                    acc[i] = acc[i] * a_s + o_o * a_o;
+                }
+                l = l * a_s + l_o * a_o;
+                m = m_new;
             }
-            l = l * a_s + l_o * a_o;
-            m = m_new;
-        }
-        const size_t pidx = ((size_t)n * n_splits + s) * H + h;
-        if (lane < G) {
-            float4* po = reinterpret_cast<float4*>(part_o + pidx * D + c * 8);
-            po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        if (lane == 0) {
-            part_ml[pidx * 2 + 0] = m;
-            part_ml[pidx * 2 + 1] = l;
+            const size_t pidx = ((size_t)n * n_splits + s) * H + h;
+            if (lane < G) {
+                float4* po = reinterpret_cast<float4*>(part_o + pidx * D + c * 8);
+                po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            if (lane == 0) {
+                part_ml[pidx * 2 + 0] = m;
+                part_ml[pidx * 2 + 1] = l;
+            }
         }
     }
 }
@@ -205,8 +235,9 @@ cudaError_t launch_decode(const void* q, const void* kcache, const void* vcache,
     const int n_splits = (w_eff + chunk - 1) / chunk;  // splits any sequence can need
     const float scale_log2 = scale * kLog2e;
     (void)max_splits;
-    dim3 grid(n_splits, N);
-    const int threads = 32 * (H < 16 ? H : 16);
+    const int threads = 32 * (H < kDecodeMaxThreads / 32 ? H : kDecodeMaxThreads / 32);
+    const long items = (long)n_splits * N;
+    const int grid = (int)items;
     const int cblocks = (N * H * 32 + 255) / 256;
     if (D == 128) {
         decode_split_kernel<128><<<grid, threads, 0, stream>>>(

@@ -131,88 +131,101 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    // 384 threads x 168 registers at launch = 128 x 72 (producer/MMA warpgroup) + 256 x 216 (softmax);
+    // 384 threads x 168 registers at launch = 128 x 88 (producer/MMA warpgroup) + 256 x 208 (softmax);
     // each role sets its budget at the top of its own branch
     const uint32_t col_s[2] = {0u, 128u};
     const uint32_t col_o[2] = {256u, 256u + D};
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        regs_decrease<72>();
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&bars.q_full, 2 * L::kTileBytes);
+        // the whole warp runs this loop converged; one elected lane issues each copy
+        regs_decrease<88>();
+        {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+            }
+            __syncwarp();
+            mbar_arrive_expect_tx_w(&bars.q_full, 2 * L::kTileBytes);
             for (int t = 0; t < 2; ++t)
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64, h,
+                    tma_load_4d_w(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64, h,
                                 r0[t], b);
             const int n_loads = 2 * (kb_hi - kb_lo + 1);
             int issued = 0;
             for (int seq = 0; seq < n_loads; ++seq) {
                 const int slot = seq % kStages;
-                if (!mbar_wait(&bars.kv_empty[slot], ((seq / kStages) & 1) ^ 1) || aborted(bars)) {
+                if (!mbar_wait_warp(&bars.kv_empty[slot], ((seq / kStages) & 1) ^ 1) || aborted(bars)) {
                     record_timeout(bars, p.err);
                     break;
                 }
                 const int kb = kb_lo + seq / 2;
                 const CUtensorMap* tm = (seq & 1) ? &tm_v : &tm_k;
                 uint8_t* dst = smem + L::kKVOff + slot * L::kTileBytes;
-                mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
+                mbar_arrive_expect_tx_w(&bars.kv_full[slot], L::kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, h, kb * kBN, b);
+                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, h, kb * kBN, b);
                 issued = seq + 1;
             }
             // never leave while a copy into this CTA's shared memory may still land
             for (int seq = issued - kStages < 0 ? 0 : issued - kStages; seq < issued; ++seq)
-                mbar_wait(&bars.kv_full[seq % kStages], (seq / kStages) & 1);
-            mbar_wait(&bars.q_full, 0);
+                mbar_wait_warp(&bars.kv_full[seq % kStages], (seq / kStages) & 1);
+            mbar_wait_warp(&bars.q_full, 0);
         }
-        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        regs_decrease<72>();
-        if (lane == 0) {
+        // the whole warp runs this loop converged; one elected lane issues each product
+        regs_decrease<88>();
+        {
             constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
             const uint32_t q_base = smem_u32(smem + L::kQOff);
             const uint32_t kv_base = smem_u32(smem + L::kKVOff);
             auto act = [&](int t, int kb) { return kb >= lo[t] && kb <= hi[t]; };
+            // Descriptors are built once; every product then only adds a constant
+            // (byte offset / 16) to the start-address field, which keeps the issue loop short.
+            const uint64_t q_desc = sdesc(q_base, 16, 1024);                // K-major, SW128
+            const uint64_t k_desc = sdesc(kv_base, 16, 1024);               // K-major, SW128
+            const uint64_t v_desc = sdesc(kv_base, kBN * 128, 1024);        // MN-major, SW128
+            constexpr uint64_t kTileStep = L::kTileBytes >> 4;
             auto issue_s = [&](int t, int slot) {
-                const uint32_t qa = q_base + t * L::kTileBytes;
-                const uint32_t ka = kv_base + slot * L::kTileBytes;
+                const uint64_t qd = q_desc + t * kTileStep;
+                const uint64_t kd = k_desc + slot * kTileStep;
+                const uint32_t d = tmem + (t ? col_s[1] : col_s[0]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + col_s[t], sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idesc_qk, kk > 0);
+                    constexpr int kChunk = (kBM * 128) >> 4;
+                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                    mma_ss_w(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bars.s_full[t]);
+                mma_commit_w(&bars.s_full[t]);
             };
             auto issue_pv = [&](int t, int slot, bool accumulate) {
-                const uint32_t va = kv_base + slot * L::kTileBytes;
+                const uint64_t vd = v_desc + slot * kTileStep;
+                const uint32_t d = tmem + (t ? col_o[1] : col_o[0]);
+                const uint32_t a = tmem + (t ? col_s[1] : col_s[0]);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8, sdesc(va + kk * 2048, kBN * 128, 1024),
-                           idesc_pv, accumulate || kk > 0);
+                    mma_ts_w(d, a + kk * 8, vd + kk * (2048 >> 4), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(&bars.q_full, 0);
+            bool ok = mbar_wait_warp(&bars.q_full, 0);
             int seq = 0;
             int n_pv[2] = {0, 0};
             if (ok) {
                 const int slot_k = seq % kStages;
-                ok = mbar_wait(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                 if (ok) {
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t)
                         if (act(t, kb_lo)) issue_s(t, slot_k);
-                    mma_commit(&bars.kv_empty[slot_k]);
+                    mma_commit_w(&bars.kv_empty[slot_k]);
                     ++seq;
                 }
             }
             for (int kb = kb_lo; ok && kb <= kb_hi; ++kb) {
                 const int slot_v = seq % kStages;
-                ok = mbar_wait(&bars.kv_full[slot_v], (seq / kStages) & 1);
+                ok = mbar_wait_warp(&bars.kv_full[slot_v], (seq / kStages) & 1);
                 if (!ok) break;
                 ++seq;
                 const bool next = kb + 1 <= kb_hi;
@@ -220,7 +233,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (act(t, kb)) {
-                        ok = mbar_wait(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
+                        ok = mbar_wait_warp(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, slot_v, n_pv[t] > 0);
@@ -228,7 +241,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                     if (next && act(t, kb + 1)) {
                         if (!k_ready) {
-                            ok = mbar_wait(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                            ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                             if (!ok) break;
                             tc_fence_after();
                             k_ready = true;
@@ -237,24 +250,23 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 if (!ok) break;
-                mma_commit(&bars.kv_empty[slot_v]);
+                mma_commit_w(&bars.kv_empty[slot_v]);
                 if (next) {
-                    mma_commit(&bars.kv_empty[slot_k]);
+                    mma_commit_w(&bars.kv_empty[slot_k]);
                     ++seq;
                 }
             }
             if (!ok) record_timeout(bars, p.err);
-            mma_commit(&bars.o_final);
+            mma_commit_w(&bars.o_final);
             // all products must have landed before TMEM is released
-            mma_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0);
+            mma_commit_w(&bars.drain);
+            mbar_wait_warp(&bars.drain, 0);
         }
-        __syncwarp();
     } else if (warp < 4) {
-        regs_decrease<72>();
+        regs_decrease<88>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        regs_increase<216>();
+        regs_increase<208>();
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
@@ -295,12 +307,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int j = 4; j < kBN; j += 4) {
-                    mx0 = fmaxf(mx0, s[j]);
-                    mx1 = fmaxf(mx1, s[j + 1]);
-                    mx2 = fmaxf(mx2, s[j + 2]);
-                    mx3 = fmaxf(mx3, s[j + 3]);
+                for (int j = 4; j + 8 <= kBN; j += 8) {  // s[4 .. kBN-5]
+                    mx0 = max3f(mx0, s[j], s[j + 1]);
+                    mx1 = max3f(mx1, s[j + 2], s[j + 3]);
+                    mx2 = max3f(mx2, s[j + 4], s[j + 5]);
+                    mx3 = max3f(mx3, s[j + 6], s[j + 7]);
                 }
+                mx0 = max3f(mx0, s[kBN - 4], s[kBN - 3]);
+                mx1 = max3f(mx1, s[kBN - 2], s[kBN - 1]);
                 const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
                 if (it == 0) {
                     m_run = m_cand;
@@ -322,21 +336,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                float sum0 = 0.f, sum1 = 0.f;
+                float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < kBN / 64; ++c) {
                     uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2_approx(fmaf(s[c * 64 + 2 * i], sl2, -m_use));
-                        const float e1 = ex2_approx(fmaf(s[c * 64 + 2 * i + 1], sl2, -m_use));
-                        sum0 += e0;
-                        sum1 += e1;
+                    for (int i = 0; i < 32; i += 2) {
+                        float x0, x1, x2, x3;
+                        const int j = c * 64 + 2 * i;
+                        fma_f32x2(x0, x1, s[j], s[j + 1], sl2, sl2, -m_use, -m_use);
+                        fma_f32x2(x2, x3, s[j + 2], s[j + 3], sl2, sl2, -m_use, -m_use);
+                        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                        const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+                        add_f32x2(sum0, sum1, sum0, sum1, e0, e1);
+                        add_f32x2(sum2, sum3, sum2, sum3, e2, e3);
                         pk[i] = pack_bf16x2(e0, e1);
+                        pk[i + 1] = pack_bf16x2(e2, e3);
                     }
                     tmem_st32(s_addr + c * 32, pk);
                 }
-                l_run += sum0 + sum1;
+                l_run += (sum0 + sum1) + (sum2 + sum3);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars.p_full[t]);
