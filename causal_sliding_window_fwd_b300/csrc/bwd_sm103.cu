@@ -20,8 +20,9 @@
 //   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T
 //               from S^T and dP^T; then the dK epilogue
 //   warps 8-11  the same for query columns [64, 128); then the dV epilogue
-//   warps 12-15 one thread per query row: dQ partial from TMEM into the fp32
-//               accumulator with vector atomics
+//   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator with
+//               atomics; for D = 128 the product is dQ^T (one thread per dQ
+//               column, so a warp's atomic covers 32 consecutive floats of a row)
 // TMEM: ST [0,128) holds S^T, then P^T (bf16, two per column) in columns
 //       [0,32) for queries 0-63 and [64,96) for queries 64-127, so each
 //       warpgroup overwrites only columns it has already read; then the
@@ -30,7 +31,7 @@
 // Products per query block m:
 //   dP^T = V dO_m^T, S^T = K Q_m^T            (both operands K-major in smem)
 //   dV += P^T dO_m, dK += dS^T Q_m            (A from TMEM, B MN-major in smem)
-//   dQ_m = dS K                                (A = dS MN-major in smem, B = K MN-major)
+//   dQ_m^T = K^T dS^T (D = 128) or dQ_m = dS K (D = 64), both operands MN-major in smem
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -48,16 +49,23 @@ constexpr int kQStages = 2;
 constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// D = 128: dQ partials leave through a TMA reduce-add from a 64-row fp32 staging tile,
+// which takes the place of the second dO stage.  D = 64: vector atomics, two dO stages.
 template <int D>
 struct BwdSmem {
+    static constexpr bool kTmaReduce = (D == 128);
+    static constexpr int kDOStages = kTmaReduce ? 1 : 2;
+    static constexpr int kStageRows = 64;                 // dQ rows per reduce-add
     static constexpr int kTile = kBQ * D * 2;            // 128 rows x D bf16
     static constexpr int kK = 0;
     static constexpr int kV = kK + kTile;
     static constexpr int kQ = kV + kTile;                 // kQStages tiles
-    static constexpr int kDO = kQ + kQStages * kTile;     // kQStages tiles
-    static constexpr int kDS = kDO + kQStages * kTile;    // dS [key][query], 128 x 128 bf16
+    static constexpr int kDO = kQ + kQStages * kTile;     // kDOStages tiles
+    static constexpr int kDS = kDO + kDOStages * kTile;   // dS [key][query], 128 x 128 bf16
     static constexpr int kDSBytes = kBK * kBQ * 2;
-    static constexpr int kLse = kDS + kDSBytes;           // [2][128] fp32 (log2 units)
+    static constexpr int kStage = kDS + kDSBytes;         // fp32 [kStageRows][D] (D = 128 only)
+    static constexpr int kStageBytes = kTmaReduce ? kStageRows * D * 4 : 0;
+    static constexpr int kLse = kStage + kStageBytes;     // [2][128] fp32 (log2 units)
     static constexpr int kDelta = kLse + 2 * kBQ * 4;     // [2][128] fp32
     static constexpr int kBars = kDelta + 2 * kBQ * 4;
     static constexpr int kBytes = kBars + 256;
@@ -65,10 +73,14 @@ struct BwdSmem {
 
 struct BwdBarriers {
     uint64_t kv_full;
-    uint64_t qdo_full[kQStages];
-    uint64_t qdo_empty[kQStages];
+    uint64_t q_full[kQStages];
+    uint64_t q_empty[kQStages];
+    uint64_t do_full[2];
+    uint64_t do_empty[2];
     uint64_t s_full;
+    uint64_t dp_full;
     uint64_t p_full;
+    uint64_t ds_full;
     uint64_t dq_full;
     uint64_t dq_empty;
     uint64_t final_;
@@ -102,6 +114,10 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ void red_add_f32(float* addr, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
 __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -111,7 +127,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using L = BwdSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + L::kBars);
@@ -132,11 +148,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) {
         mbar_init(&bars->kv_full, 1);
         for (int s = 0; s < kQStages; ++s) {
-            mbar_init(&bars->qdo_full[s], 1);
-            mbar_init(&bars->qdo_empty[s], 1);
+            mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->q_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->do_full[s], 1);
+            mbar_init(&bars->do_empty[s], 1);
         }
         mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->dp_full, 1);
         mbar_init(&bars->p_full, 2 * kBK);
+        mbar_init(&bars->ds_full, 2 * kBK);
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, kBQ);
         mbar_init(&bars->final_, 1);
@@ -173,25 +195,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, h, j0, b);
                 tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, h, j0, b);
             }
-            int issued = 0;
+            int issued_q = 0, issued_do = 0;
             for (int it = 0; it < n_it; ++it) {
-                const int st = it % kQStages;
-                if (!mbar_wait_warp(&bars->qdo_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
+                const int st = it % kQStages, so = it % L::kDOStages;
+                const int i0 = (m_lo + it) * kBQ;
+                if (!mbar_wait_warp(&bars->q_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
                     record_timeout(bars, p.err);
                     break;
                 }
-                const int i0 = (m_lo + it) * kBQ;
-                mbar_arrive_expect_tx_w(&bars->qdo_full[st], 2 * L::kTile);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->qdo_full[st], c * 64, h,
-                                i0, b);
-                    tma_load_4d_w(smem + L::kDO + st * L::kTile + c * kBQ * 128, &tm_do, &bars->qdo_full[st], c * 64,
-                                h, i0, b);
+                mbar_arrive_expect_tx_w(&bars->q_full[st], L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64, h,
+                                  i0, b);
+                issued_q = it + 1;
+                if (!mbar_wait_warp(&bars->do_empty[so], ((it / L::kDOStages) & 1) ^ 1) || aborted(bars)) {
+                    record_timeout(bars, p.err);
+                    break;
                 }
-                issued = it + 1;
+                mbar_arrive_expect_tx_w(&bars->do_full[so], L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kDO + so * L::kTile + c * kBQ * 128, &tm_do, &bars->do_full[so], c * 64,
+                                  h, i0, b);
+                issued_do = it + 1;
             }
-            for (int it = issued - kQStages < 0 ? 0 : issued - kQStages; it < issued; ++it)
-                mbar_wait_warp(&bars->qdo_full[it % kQStages], (it / kQStages) & 1);
+            // never leave while a copy into this CTA's shared memory may still land: the last
+            // use of each stage is the only one whose completion can still be outstanding
+            for (int it = issued_q - kQStages < 0 ? 0 : issued_q - kQStages; it < issued_q; ++it)
+                mbar_wait_warp(&bars->q_full[it % kQStages], (it / kQStages) & 1);
+            for (int it = issued_do - L::kDOStages < 0 ? 0 : issued_do - L::kDOStages; it < issued_do; ++it)
+                mbar_wait_warp(&bars->do_full[it % L::kDOStages], (it / L::kDOStages) & 1);
             mbar_wait_warp(&bars->kv_full, 0);
         }
     } else if (warp == 1) {
@@ -202,6 +234,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             constexpr uint32_t id_kq = idesc_bf16(kBK, kBQ, false, false);  // S^T, dP^T
             constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
             constexpr uint32_t id_qd = idesc_bf16(kBQ, D, true, true);      // dQ (A and B MN-major)
+            constexpr uint32_t id_dqt = idesc_bf16(D, kBQ, true, true);     // dQ^T (A and B MN-major)
             const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
             const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
             const uint32_t sDS = smem_u32(smem + L::kDS);
@@ -212,49 +245,86 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint64_t ds_mn = sdesc(sDS, kBQ * 128, 1024), k_mn = sdesc(sK, kBK * 128, 1024);
             constexpr uint64_t kTileStep = L::kTile >> 4;
             constexpr uint64_t kChunk = (kBQ * 128) >> 4;
-            bool ok = mbar_wait_warp(&bars->kv_full, 0);
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it % kQStages;
-                ok = mbar_wait_warp(&bars->qdo_full[st], (it / kQStages) & 1) && !aborted(bars);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t q_k = q_kmaj + st * kTileStep, do_k = do_kmaj + st * kTileStep;
-                const uint64_t q_m = q_mn + st * kTileStep, do_m = do_mn + st * kTileStep;
-                // dP^T = V dO^T  (DPT is free: the previous dK product was issued before)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
-                    mma_ss_w(tmem + kColDPT, v_kmaj + off, do_k + off, id_kq, kk > 0 ? 1u : 0u);
-                }
-                // S^T = K Q^T once the previous dQ has been read out of ST
-                if (it > 0) {
-                    ok = mbar_wait_warp(&bars->dq_empty, (it - 1) & 1) && !aborted(bars);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
+            auto issue_s = [&](int st) {  // S^T = K Q^T into ST
+                const uint64_t q_k = q_kmaj + st * kTileStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
                     mma_ss_w(tmem + kColST, k_kmaj + off, q_k + off, id_kq, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_w(&bars->s_full);
+            };
+            auto issue_dp = [&](int so) {  // dP^T = V dO^T into DPT
+                const uint64_t do_k = do_kmaj + so * kTileStep;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                    mma_ss_w(tmem + kColDPT, v_kmaj + off, do_k + off, id_kq, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_w(&bars->dp_full);
+            };
+            bool ok = mbar_wait_warp(&bars->kv_full, 0) && mbar_wait_warp(&bars->q_full[0], 0) &&
+                      mbar_wait_warp(&bars->do_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it % kQStages, so = it % L::kDOStages;
+                const uint64_t q_m = q_mn + st * kTileStep, do_m = do_mn + so * kTileStep;
+                // dV += P^T dO  (A = P^T packed in ST, K = 128 queries, 16 per product)
                 ok = mbar_wait_warp(&bars->p_full, it & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
-                // dV += P^T dO ; dK += dS^T Q   (K = 128 queries, 16 per product)
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk) {
                     const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // packed P^T / dS^T columns
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts_w(tmem + kColDV, tmem + kColST + pc, do_m + kk * (2048 >> 4), id_kd, acc);
-                    mma_ts_w(tmem + kColDK, tmem + kColDPT + pc, q_m + kk * (2048 >> 4), id_kd, acc);
+                    mma_ts_w(tmem + kColDV, tmem + kColST + pc, do_m + kk * (2048 >> 4), id_kd,
+                             (it > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit_w(&bars->qdo_empty[st]);
-                // dQ_m = dS K  (M = queries, K = keys, N = D), into ST
+                mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
+                // dK += dS^T Q  (A = dS^T packed in DPT)
+                ok = mbar_wait_warp(&bars->ds_full, it & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_ss_w(tmem + kColST, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < kBQ / 16; ++kk) {
+                    const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts_w(tmem + kColDK, tmem + kColDPT + pc, q_m + kk * (2048 >> 4), id_kd,
+                             (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_w(&bars->q_empty[st]);  // Q of this block: S^T and dK were its readers
+                // dQ of this block into DPT (issued after dK, which read dS^T from DPT)
+                if constexpr (D == 128) {
+                    // dQ_m^T = K^T dS^T  (M = D lanes, N = queries, K = keys): a warp then holds 32
+                    // consecutive dQ columns of one query row, so each atomic covers a full line
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_ss_w(tmem + kColDPT, k_mn + kk * (2048 >> 4), ds_mn + kk * (2048 >> 4), id_dqt,
+                                 kk > 0 ? 1u : 0u);
+                } else {
+                    // dQ_m = dS K  (M = queries, K = keys, N = D)
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_ss_w(tmem + kColDPT, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd,
+                                 kk > 0 ? 1u : 0u);
+                }
                 mma_commit_w(&bars->dq_full);
+                if (it + 1 < n_it) {
+                    // next block: S^T into ST right away (dV above was the last reader of P^T);
+                    // dP^T into DPT once this block's dQ has been read out
+                    const int st1 = (it + 1) % kQStages, so1 = (it + 1) % L::kDOStages;
+                    ok = mbar_wait_warp(&bars->q_full[st1], ((it + 1) / kQStages) & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(st1);
+                    ok = mbar_wait_warp(&bars->dq_empty, it & 1) &&
+                         mbar_wait_warp(&bars->do_full[so1], ((it + 1) / L::kDOStages) & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dp(so1);
+                }
             }
             if (!ok) record_timeout(bars, p.err);
             mma_commit_w(&bars->final_);
@@ -293,19 +363,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             named_bar_sync(1 + g, 128);
             const float* lb = s_lse + (it & 1) * kBQ;
             const float* db = s_delta + (it & 1) * kBQ;
+            const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
+            // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries
             ok = mbar_wait(&bars->s_full, it & 1) && !aborted(bars);
             if (!ok) break;
             tc_fence_after();
-            const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {  // 32-query chunks of this warpgroup's half
+            float pf[64];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 const int q0 = 64 * g + 32 * c;
-                uint32_t sr[32], dr[32];
-                tmem_ld32x2(st_addr + q0, dpt_addr + q0, sr, dr);
-                uint32_t pk[16], dk[16];
+                uint32_t sr[32];
+                tmem_ld32(st_addr + q0, sr);
+                uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    float pv[2], dsv[2];
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
                         const int qi = q0 + 2 * x + y;
@@ -314,14 +385,36 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const int i = i0 + qi;
                             if (j > i || i - j >= p.W) pr = 0.f;
                         }
-                        pv[y] = pr;
-                        dsv[y] = pr * (__uint_as_float(dr[2 * x + y]) - db[qi]);
+                        pf[32 * c + 2 * x + y] = pr;
                     }
-                    pk[x] = pack_bf16x2(pv[0], pv[1]);
-                    dk[x] = pack_bf16x2(dsv[0], dsv[1]);
+                    pk[x] = pack_bf16x2(pf[32 * c + 2 * x], pf[32 * c + 2 * x + 1]);
                 }
                 // packed into the first half of this warpgroup's own (already read) columns
                 tmem_st16(st_addr + 64 * g + 16 * c, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full);
+            // phase 2: dS^T = P^T (dP^T - Delta), to TMEM (for dK) and to shared memory (for dQ)
+            ok = mbar_wait(&bars->dp_full, it & 1) && !aborted(bars);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int q0 = 64 * g + 32 * c;
+                uint32_t dr[32];
+                tmem_ld32(dpt_addr + q0, dr);
+                uint32_t dk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    float dsv[2];
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int qi = q0 + 2 * x + y;
+                        dsv[y] = pf[32 * c + 2 * x + y] * (__uint_as_float(dr[2 * x + y]) - db[qi]);
+                    }
+                    dk[x] = pack_bf16x2(dsv[0], dsv[1]);
+                }
                 tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
                 // dS row into the MN-major [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
 #pragma unroll
@@ -338,7 +431,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_wait_st();
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars->p_full);
+            mbar_arrive(&bars->ds_full);
         }
         // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV
         if (ok) ok = mbar_wait(&bars->final_, 0) && !aborted(bars);
@@ -369,45 +462,77 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else {
-        // ------------------------------------------------------------ dQ partials (thread = query row)
+        // ------------------------------------------------------------ dQ partials into the fp32 accumulator
         regs_decrease<96>();
         const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
-        const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
+        const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
         for (int it = 0; it < n_it; ++it) {
-            const int i = (m_lo + it) * kBQ + tid;
+            const int i0 = (m_lo + it) * kBQ;
             if (!mbar_wait(&bars->dq_full, it & 1) || aborted(bars)) {
                 record_timeout(bars, p.err);
                 break;
             }
             tc_fence_after();
-            float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
-            const bool in_range = i < p.T;
+            if constexpr (L::kTmaReduce) {
+                // thread = dQ column d, TMEM columns = the block's 128 query rows.  Each half
+                // (64 rows) goes to the fp32 staging tile [row][d] and is added to the
+                // accumulator by one TMA reduce-add, which frees the SM's load/store path.
+                float* stage = reinterpret_cast<float*>(smem + L::kStage);
 #pragma unroll
-            for (int half = 0; half < D / 64; ++half) {
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[64];
+                    {
+                        uint32_t a[32], c2[32];
+                        tmem_ld32x2(st_addr + 64 * half, st_addr + 64 * half + 32, a, c2);
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            r[x] = a[x];
+                            r[32 + x] = c2[x];
+                        }
+                    }
+                    if (half == 1) {
+                        // the block's dQ is now in registers: hand the TMEM columns back
+                        tc_fence_before();
+                        mbar_arrive(&bars->dq_empty);
+                    }
+                    if (tid == 0) bulk_wait_read();  // the previous reduce-add has read the staging tile
+                    named_bar_sync(3, 128);
+#pragma unroll
+                    for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(r[x]);
+                    fence_async_smem();
+                    named_bar_sync(3, 128);
+                    if (tid == 0) {
+                        tma_reduce_add_4d(&tm_dq, stage, 0, h, i0 + 64 * half, b);
+                        bulk_commit();
+                    }
+                }
+            } else {
+                // thread = query row, TMEM columns = the D dQ columns
+                const int i = i0 + tid;
+                float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
                 uint32_t r[64];
                 {
                     uint32_t a[32], c2[32];
-                    tmem_ld32x2(st_addr + 64 * half, st_addr + 64 * half + 32, a, c2);
+                    tmem_ld32x2(st_addr, st_addr + 32, a, c2);
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         r[x] = a[x];
                         r[32 + x] = c2[x];
                     }
                 }
-                if (half == D / 64 - 1) {
-                    // the block's dQ is now in registers: hand the TMEM columns back before the last atomics
-                    tc_fence_before();
-                    mbar_arrive(&bars->dq_empty);
-                }
-                if (in_range) {
+                tc_fence_before();
+                mbar_arrive(&bars->dq_empty);
+                if (i < p.T) {
 #pragma unroll
                     for (int v4 = 0; v4 < 16; ++v4)
-                        red_add_f32x4(dst + 64 * half + 4 * v4, __uint_as_float(r[4 * v4]),
-                                      __uint_as_float(r[4 * v4 + 1]), __uint_as_float(r[4 * v4 + 2]),
-                                      __uint_as_float(r[4 * v4 + 3]));
+                        red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                                      __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
                 }
             }
+        }
+        if constexpr (L::kTmaReduce) {
+            if (tid == 0) bulk_wait_all();  // every reduce-add has landed before the CTA exits
         }
     }
     tc_fence_before();
@@ -468,9 +593,10 @@ template <int D>
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
                           float scale, float* dq_acc, float* delta, int* err, cudaStream_t st) {
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
-        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ))
+        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
+        !make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, D, BwdSmem<D>::kStageRows))
         return cudaErrorInvalidValue;
     const long rows = (long)B * T * H;
     bwd_pre_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
@@ -501,7 +627,7 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         if (dev < 64) attr_set[dev] = true;
     }
     dim3 grid(p.n_kb, H, B);
-    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, p);
+    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
     const size_t n8 = (size_t)rows * D / 8;
     bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
                                                                  scale);

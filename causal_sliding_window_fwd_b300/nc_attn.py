@@ -29,7 +29,7 @@ NC_WINDOW_FULL = -1
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
             "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_get_device_error", "nc_launch_count",
-            "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc")
+            "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
 
 # Size of the library's fixed decode scratch array (NC_DECODE_NOALLOC_SCRATCH_BYTES).
 NC_DECODE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -67,6 +67,8 @@ def _load():
     lib.nc_attn_decode_noalloc_scratch_bytes.restype = sz
     lib.nc_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.nc_attn_decode_noalloc.restype = i
+    lib.nc_debug_watchdog_selftest.argtypes = [ctypes.c_ulonglong, vp]
+    lib.nc_debug_watchdog_selftest.restype = i
     return lib
 
 
@@ -189,6 +191,12 @@ def nc_get_device_error(stream=None, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(lib.nc_get_device_error(ctypes.byref(code), _stream(dev, stream)), "nc_get_device_error")
     return code.value
+
+
+def nc_debug_watchdog_selftest(limit_cycles: int, stream=None, device=None) -> None:
+    """Run the bounded-wait self-test kernel; afterwards nc_get_device_error() reports the timeout."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib.nc_debug_watchdog_selftest(int(limit_cycles), _stream(dev, stream)), "nc_debug_watchdog_selftest")
 
 
 def nc_launch_count() -> int:

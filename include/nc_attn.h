@@ -132,6 +132,16 @@ nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, 
 nc_status nc_get_device_error(int* code, cudaStream_t stream);
 
 /*
+ * Failure-detection self-test (not part of the attention path).  Launches one
+ * CTA whose thread waits on an mbarrier that nothing completes, through the
+ * bounded wait all of the library's pipelines use, limited to `limit_cycles`
+ * SM clock cycles (1 .. 2^31).  The wait runs out, the kernel records
+ * NC_ERR_DEVICE_TIMEOUT in the device error word and returns; the context
+ * stays usable.  Read the result with nc_get_device_error().
+ */
+nc_status nc_debug_watchdog_selftest(unsigned long long limit_cycles, cudaStream_t stream);
+
+/*
  * Decode without a caller-provided workspace and without allocating.  The
  * pages describe nothing of the kind: this entry point exists for callers
  * that cannot allocate device memory when they decode (engines whose own

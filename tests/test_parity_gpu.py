@@ -240,3 +240,16 @@ def test_decode_bad_length_reports_and_nans(nc):
     assert torch.isnan(o[1].float()).all() and torch.isnan(o[2].float()).all()
     assert torch.isfinite(o[0].float()).all() and torch.isfinite(o[3].float()).all()
     assert nc.nc_get_device_error() == 0  # cleared by the read
+
+
+# ---------------------------------------------------------------- failure detection
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(nc):
+    """A wait on a barrier nothing completes runs out (about 1 ms), sets the error word, and returns."""
+    nc.nc_debug_watchdog_selftest(2_000_000)
+    assert nc.nc_get_device_error() == nc.NC_ERR_DEVICE_TIMEOUT
+    assert nc.nc_get_device_error() == 0
+    q, k, v, dO = workloads.make_qkvdo_shape(1, 128, 1, 64, seed=3, device="cuda")
+    o, lse = nc.attn_fwd(q, k, v, 16)
+    assert nc.nc_get_device_error() == 0 and torch.isfinite(o.float()).all()
