@@ -25,12 +25,13 @@
 //               column, so a warp's atomic covers 32 consecutive floats of a row)
 // TMEM: ST [0,128) holds S^T, then P^T (bf16, two per column) in columns
 //       [0,32) for queries 0-63 and [64,96) for queries 64-127, so each
-//       warpgroup overwrites only columns it has already read; then the
-//       block's dQ.  DPT [128,256) holds dP^T, then dS^T the same way.
-//       DV [256,256+D); DK [256+D,256+2D).
+//       warpgroup overwrites only columns it has already read.  DPT [128,256)
+//       holds dP^T, then dS^T packed the same way, then the block's dQ.
+//       DV [256,256+D); DK [256+D,256+2D).  dS also goes to a shared-memory
+//       tile [key][query], the MN-major operand of the dQ product.
 // Products per query block m:
 //   dP^T = V dO_m^T, S^T = K Q_m^T            (both operands K-major in smem)
-//   dV += P^T dO_m, dK += dS^T Q_m            (A from TMEM, B MN-major in smem)
+//   dV += P^T dO_m, dK += dS^T Q_m              (A from TMEM, B MN-major in smem)
 //   dQ_m^T = K^T dS^T (D = 128) or dQ_m = dS K (D = 64), both operands MN-major in smem
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -284,7 +285,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                              (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
-                // dK += dS^T Q  (A = dS^T packed in DPT)
+                // dK += dS^T Q  (A = dS^T packed in DPT: reading A from TMEM halves this
+                // product's shared-memory traffic, and shared-memory bandwidth is what the
+                // products of this kernel compete for)
                 ok = mbar_wait_warp(&bars->ds_full, it & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
@@ -360,34 +363,49 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int i0 = m * kBQ;
             (fetch_lse ? s_lse : s_delta)[(it & 1) * kBQ + qoff] = nx;
             if (it + 1 < n_it) nx = stat(i0 + kBQ + qoff);
-            named_bar_sync(1 + g, 128);
+            // the warpgroup leaves together if any of its warps saw a wait run out
+            if (!named_bar_and(1 + g, 128, ok)) break;
             const float* lb = s_lse + (it & 1) * kBQ;
             const float* db = s_delta + (it & 1) * kBQ;
             const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
             // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries
-            ok = mbar_wait(&bars->s_full, it & 1) && !aborted(bars);
-            if (!ok) break;
+            ok = mbar_wait_warp(&bars->s_full, it & 1) && !aborted(bars);
+            if (!ok) continue;
             tc_fence_after();
             float pf[64];
+            uint32_t sr[64];
+            {
+                uint32_t a[32], b2[32];
+                tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    sr[x] = a[x];
+                    sr[32 + x] = b2[x];
+                }
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int q0 = 64 * g + 32 * c;
-                uint32_t sr[32];
-                tmem_ld32(st_addr + q0, sr);
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
+                for (int x4 = 0; x4 < 8; ++x4) {
+                    const float4 L4 = *reinterpret_cast<const float4*>(lb + q0 + 4 * x4);
+                    float e[4];
+                    fma_f32x2(e[0], e[1], __uint_as_float(sr[32 * c + 4 * x4]), __uint_as_float(sr[32 * c + 4 * x4 + 1]),
+                              sl2, sl2, -L4.x, -L4.y);
+                    fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
+                              __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -L4.z, -L4.w);
 #pragma unroll
-                    for (int y = 0; y < 2; ++y) {
-                        const int qi = q0 + 2 * x + y;
-                        float pr = ex2_approx(fmaf(__uint_as_float(sr[2 * x + y]), sl2, -lb[qi]));
+                    for (int y = 0; y < 4; ++y) {
+                        float pr = ex2_approx(e[y]);
                         if (!full) {
-                            const int i = i0 + qi;
+                            const int i = i0 + q0 + 4 * x4 + y;
                             if (j > i || i - j >= p.W) pr = 0.f;
                         }
-                        pf[32 * c + 2 * x + y] = pr;
+                        pf[32 * c + 4 * x4 + y] = pr;
                     }
-                    pk[x] = pack_bf16x2(pf[32 * c + 2 * x], pf[32 * c + 2 * x + 1]);
+                    pk[2 * x4] = pack_bf16x2(pf[32 * c + 4 * x4], pf[32 * c + 4 * x4 + 1]);
+                    pk[2 * x4 + 1] = pack_bf16x2(pf[32 * c + 4 * x4 + 2], pf[32 * c + 4 * x4 + 3]);
                 }
                 // packed into the first half of this warpgroup's own (already read) columns
                 tmem_st16(st_addr + 64 * g + 16 * c, pk);
@@ -395,28 +413,41 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full);
-            // phase 2: dS^T = P^T (dP^T - Delta), to TMEM (for dK) and to shared memory (for dQ)
-            ok = mbar_wait(&bars->dp_full, it & 1) && !aborted(bars);
-            if (!ok) break;
+            // phase 2: dS^T = P^T (dP^T - Delta), packed into DPT (A operand of dK) and into the
+            // shared-memory tile [key][query] (MN-major operand of dQ)
+            ok = mbar_wait_warp(&bars->dp_full, it & 1) && !aborted(bars);
+            if (!ok) continue;
             tc_fence_after();
+            uint32_t drr[64];
+            {
+                uint32_t a[32], b2[32];
+                tmem_ld32x2(dpt_addr + 64 * g, dpt_addr + 64 * g + 32, a, b2);  // one wait for both chunks
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    drr[x] = a[x];
+                    drr[32 + x] = b2[x];
+                }
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int q0 = 64 * g + 32 * c;
-                uint32_t dr[32];
-                tmem_ld32(dpt_addr + q0, dr);
+                const uint32_t* dr = drr + 32 * c;
                 uint32_t dk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    float dsv[2];
-#pragma unroll
-                    for (int y = 0; y < 2; ++y) {
-                        const int qi = q0 + 2 * x + y;
-                        dsv[y] = pf[32 * c + 2 * x + y] * (__uint_as_float(dr[2 * x + y]) - db[qi]);
-                    }
-                    dk[x] = pack_bf16x2(dsv[0], dsv[1]);
+                for (int x4 = 0; x4 < 8; ++x4) {
+                    const float4 D4 = *reinterpret_cast<const float4*>(db + q0 + 4 * x4);
+                    float t[4], ds[4];
+                    add_f32x2(t[0], t[1], __uint_as_float(dr[4 * x4]), __uint_as_float(dr[4 * x4 + 1]), -D4.x, -D4.y);
+                    add_f32x2(t[2], t[3], __uint_as_float(dr[4 * x4 + 2]), __uint_as_float(dr[4 * x4 + 3]), -D4.z,
+                              -D4.w);
+                    mul_f32x2(ds[0], ds[1], pf[32 * c + 4 * x4], pf[32 * c + 4 * x4 + 1], t[0], t[1]);
+                    mul_f32x2(ds[2], ds[3], pf[32 * c + 4 * x4 + 2], pf[32 * c + 4 * x4 + 3], t[2], t[3]);
+                    dk[2 * x4] = pack_bf16x2(ds[0], ds[1]);
+                    dk[2 * x4 + 1] = pack_bf16x2(ds[2], ds[3]);
                 }
+                // dS^T (bf16) over this warpgroup's already-read DPT columns, for dK
                 tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
-                // dS row into the MN-major [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
+                // dS row into the [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int unit = 4 * c + u;
@@ -434,7 +465,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive(&bars->ds_full);
         }
         // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV
-        if (ok) ok = mbar_wait(&bars->final_, 0) && !aborted(bars);
+        if (ok) ok = mbar_wait_warp(&bars->final_, 0) && !aborted(bars);
         if (!ok) {
             record_timeout(bars, p.err);
         } else {
@@ -467,10 +498,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
+        const size_t row_stride = static_cast<size_t>(p.H) * D;
+        bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int i0 = (m_lo + it) * kBQ;
-            if (!mbar_wait(&bars->dq_full, it & 1) || aborted(bars)) {
+            const bool got = mbar_wait_warp(&bars->dq_full, it & 1) && !aborted(bars);
+            if (!named_bar_and(3, 128, got)) {  // leave together
                 record_timeout(bars, p.err);
+                ok = false;
                 break;
             }
             tc_fence_after();
@@ -510,7 +545,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             } else {
                 // thread = query row, TMEM columns = the D dQ columns
                 const int i = i0 + tid;
-                float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.T + i) * p.H + h) * D;
+                float* dst = p.dq_acc + (static_cast<size_t>(b) * p.T + i) * row_stride + static_cast<size_t>(h) * D;
                 uint32_t r[64];
                 {
                     uint32_t a[32], c2[32];
@@ -543,34 +578,41 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-// Delta = rowsum(dO * O) per (b, h, i) and a zeroed dQ accumulator.  One warp per row.
+// Delta = rowsum(dO * O) per (b, h, i) and a zeroed dQ accumulator.
+// D / 8 lanes per row, each with one 16-byte load of O and of dO.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       float* __restrict__ delta, float* __restrict__ dq_acc, int B,
                                                       int T, int H) {
-    constexpr int E = D / 32;
-    const long row = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (row >= (long)B * T * H) return;
-    const int h = row % H;
-    const int i = (row / H) % T;
-    const int b = row / ((long)H * T);
-    const size_t off = (size_t)row * D + lane * E;
+    constexpr int G = D / 8;          // lanes per row
+    constexpr int RPW = 32 / G;       // rows per warp
+    const long tid_g = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long row = (tid_g >> 5) * RPW + ((threadIdx.x & 31) / G);
+    const int c = threadIdx.x % G;
+    const long rows = (long)B * T * H;
     float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = reinterpret_cast<const uint4*>(o + (size_t)row * D)[c];
+        const uint4 g = reinterpret_cast<const uint4*>(dO + (size_t)row * D)[c];
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + off + e));
-        const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dO + off + e));
-        acc = fmaf(a.x, g.x, fmaf(a.y, g.y, acc));
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(g2[e]);
+            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+        float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D + c * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) delta[((size_t)b * H + h) * T + i] = acc;
-    if constexpr (E == 4) {
-        reinterpret_cast<float4*>(dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-        reinterpret_cast<float2*>(dq_acc + off)[0] = make_float2(0.f, 0.f);
+    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && c == 0) {
+        const int h = row % H;
+        const int i = (row / H) % T;
+        const int b = row / ((long)H * T);
+        delta[((size_t)b * H + h) * T + i] = acc;
     }
 }
 
@@ -599,7 +641,8 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         !make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, D, BwdSmem<D>::kStageRows))
         return cudaErrorInvalidValue;
     const long rows = (long)B * T * H;
-    bwd_pre_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
+    const long pre_threads = ((rows * (D / 8) + 31) / 32) * 32;
+    bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta, dq_acc, B, T, H);
     BwdParams p;
     p.lse = lse;

@@ -198,12 +198,35 @@ decode_combine_kernel(const float* __restrict__ part_ml, const float* __restrict
     }
     const int lo = visible_lo(L, window);
     const int used = (L - lo + chunk - 1) / chunk;
+    const float* ml = part_ml + ((size_t)n * n_splits * H + h) * 2;  // split s at ml[s * H * 2]
+    // running maximum over the splits, lanes striding over them
     float M = -INFINITY;
-    for (int s = 0; s < used; ++s) M = fmaxf(M, part_ml[(((size_t)n * n_splits + s) * H + h) * 2]);
+    for (int s = lane; s < used; s += 32) M = fmaxf(M, ml[(size_t)s * H * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float lsum = 0.f, acc[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) acc[i] = 0.f;
-    for (int s = 0; s < used; ++s) {
+    int s = 0;
+    for (; s + 4 <= used; s += 4) {  // four splits' loads in flight
+        float w[4], lp[4], ov[4][E];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t pidx = ((size_t)n * n_splits + s + u) * H + h;
+            w[u] = part_ml[pidx * 2];
+            lp[u] = part_ml[pidx * 2 + 1];
+#pragma unroll
+            for (int i = 0; i < E; ++i) ov[u][i] = part_o[pidx * D + lane * E + i];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float wu = exp2f(w[u] - M);
+            lsum = fmaf(lp[u], wu, lsum);
+#pragma unroll
+            for (int i = 0; i < E; ++i) acc[i] = fmaf(ov[u][i], wu, acc[i]);
+        }
+    }
+    for (; s < used; ++s) {
         const size_t pidx = ((size_t)n * n_splits + s) * H + h;
         const float w = exp2f(part_ml[pidx * 2] - M);
         lsum = fmaf(part_ml[pidx * 2 + 1], w, lsum);

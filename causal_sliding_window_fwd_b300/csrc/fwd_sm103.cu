@@ -285,7 +285,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_o;
             int it = 0;
             for (int kb = t_lo; kb <= t_hi; ++kb, ++it) {
-                ok = mbar_wait(&bars.s_full[t], it & 1) && !aborted(bars);
+                ok = mbar_wait_warp(&bars.s_full[t], it & 1) && !aborted(bars);  // warp-uniform
                 if (!ok) break;
                 tc_fence_after();
                 float s[kBN];
@@ -361,7 +361,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mbar_arrive(&bars.p_full[t]);
             }
             // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
-            if (ok) ok = mbar_wait(&bars.o_final, 0) && !aborted(bars);
+            if (ok) ok = mbar_wait_warp(&bars.o_final, 0) && !aborted(bars);
             if (!ok) {
                 record_timeout(bars, p.err);
             } else {

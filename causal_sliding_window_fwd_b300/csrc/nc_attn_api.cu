@@ -115,8 +115,10 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
     }
     int* err = error_word();
     if (err == nullptr) return NC_ERR_CUDA;
-    float* dq_acc = static_cast<float*>(workspace);
-    float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)B * T * H * D * 4, 256));
+    char* ws = static_cast<char*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)B * T * H * D * 4, 256);
+    float* delta = reinterpret_cast<float*>(ws);
     const cudaError_t e = nc::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc, delta,
                                          err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
