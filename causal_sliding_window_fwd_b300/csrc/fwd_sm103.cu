@@ -52,9 +52,11 @@ struct FwdBarriers {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full;
+    uint64_t q_empty;
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_final;
+    uint64_t o_free;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -86,6 +88,53 @@ __device__ __forceinline__ void record_timeout(FwdBarriers& bars, int* err) {
     atomicExch(&bars.abort, 1);
 }
 
+// Geometry of one work item: a pair of 128-row query tiles of one (batch, head).
+struct FwdItem {
+    int b, h;
+    int r0[2];
+    int lo[2], hi[2];   // key blocks each tile visits (empty range for an inactive tile 1)
+    int kb_lo, kb_hi;   // union of the two ranges
+    bool active1;
+};
+
+// Items are numbered heaviest first (query-tile pair descending, then (h, b)), so the
+// static round-robin over persistent CTAs hands out the long causal tiles first.
+__device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
+    FwdItem it;
+    const int bh = w % (p.B * p.H);
+    const int pair = p.n_pairs - 1 - w / (p.B * p.H);
+    it.h = bh % p.H;
+    it.b = bh / p.H;
+    it.r0[0] = pair * 2 * kBM;
+    it.r0[1] = pair * 2 * kBM + kBM;
+    it.active1 = it.r0[1] < p.T;
+    tile_blocks(it.r0[0], p.T, p.W, it.lo[0], it.hi[0]);
+    tile_blocks(it.r0[1], p.T, p.W, it.lo[1], it.hi[1]);
+    if (!it.active1) {
+        it.lo[1] = it.hi[0] + 1;
+        it.hi[1] = it.hi[0];
+    }
+    it.kb_lo = it.lo[0];
+    it.kb_hi = it.active1 ? it.hi[1] : it.hi[0];
+    return it;
+}
+
+// Work item ii of this CTA.  Round ii hands out items ii*G .. ii*G+G-1 (G = gridDim.x),
+// CTA c taking slot c on even rounds and slot G-1-c on odd ones: with items sorted heaviest
+// first, this zigzag evens out the total work per CTA far better than plain round-robin.
+__device__ __forceinline__ int fwd_item_index(int ii) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return ii * G + ((ii & 1) ? G - 1 - c : c);
+}
+
+// Number of items of this CTA: every full round, plus the last partial round if its slot is in it.
+__device__ __forceinline__ int fwd_items_of_cta(int n_items) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int full = n_items / G, rem = n_items % G;
+    const int slot = (full & 1) ? G - 1 - c : c;
+    return full + (slot < rem ? 1 : 0);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -96,17 +145,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __shared__ FwdBarriers bars;
 
     const int warp = warp_id(), lane = lane_id();
-    // heaviest query tiles first: they have the most key blocks under full causal masking
-    const int pair = p.n_pairs - 1 - blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int r0[2] = {pair * 2 * kBM, pair * 2 * kBM + kBM};
-    const bool active1 = r0[1] < p.T;
-    int lo[2], hi[2];
-    tile_blocks(r0[0], p.T, p.W, lo[0], hi[0]);
-    tile_blocks(r0[1], p.T, p.W, lo[1], hi[1]);
-    if (!active1) { lo[1] = hi[0] + 1; hi[1] = hi[0]; }
-    const int kb_lo = lo[0];
-    const int kb_hi = active1 ? hi[1] : hi[0];
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -114,11 +152,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars.kv_empty[i], 1);
         }
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars.s_full[t], 1);
             mbar_init(&bars.p_full[t], kBM);
         }
         mbar_init(&bars.o_final, 1);
+        mbar_init(&bars.o_free, 2 * kBM);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
         fence_barrier_init();
@@ -131,58 +171,69 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    // 384 threads x 168 registers at launch = 128 x 88 (producer/MMA warpgroup) + 256 x 208 (softmax);
+    // 384 threads x 168 registers at launch = 128 x 72 (producer/MMA warpgroup) + 256 x 216 (softmax);
     // each role sets its budget at the top of its own branch
     const uint32_t col_s[2] = {0u, 128u};
     const uint32_t col_o[2] = {256u, 256u + D};
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // the whole warp runs this loop converged; one elected lane issues each copy
-        regs_decrease<88>();
-        {
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
+        // the whole warp runs this loop converged; lane 0 issues each copy
+        regs_decrease<72>();
+        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        __syncwarp();
+        int seq = 0;          // K/V loads issued over all items (ring position)
+        int q_loads = 0;
+        bool ok = true;
+        for (int ii = 0; ok && ii < my_items; ++ii) {
+            const FwdItem it = fwd_item(fwd_item_index(ii), p);
+            // Q of this item once the previous item's S products have read theirs
+            if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                ok = false;
+                break;
             }
-            __syncwarp();
             mbar_arrive_expect_tx_w(&bars.q_full, 2 * L::kTileBytes);
             for (int t = 0; t < 2; ++t)
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64, h,
-                                r0[t], b);
-            const int n_loads = 2 * (kb_hi - kb_lo + 1);
-            int issued = 0;
-            for (int seq = 0; seq < n_loads; ++seq) {
+                    tma_load_4d_w(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64,
+                                  it.h, it.r0[t], it.b);
+            ++q_loads;
+            const int n_loads = 2 * (it.kb_hi - it.kb_lo + 1);
+            for (int x = 0; x < n_loads; ++x, ++seq) {
                 const int slot = seq % kStages;
                 if (!mbar_wait_warp(&bars.kv_empty[slot], ((seq / kStages) & 1) ^ 1) || aborted(bars)) {
-                    record_timeout(bars, p.err);
+                    ok = false;
                     break;
                 }
-                const int kb = kb_lo + seq / 2;
-                const CUtensorMap* tm = (seq & 1) ? &tm_v : &tm_k;
+                const int kb = it.kb_lo + x / 2;
+                const CUtensorMap* tm = (x & 1) ? &tm_v : &tm_k;
                 uint8_t* dst = smem + L::kKVOff + slot * L::kTileBytes;
                 mbar_arrive_expect_tx_w(&bars.kv_full[slot], L::kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, h, kb * kBN, b);
-                issued = seq + 1;
+                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, it.h, kb * kBN, it.b);
             }
-            // never leave while a copy into this CTA's shared memory may still land
-            for (int seq = issued - kStages < 0 ? 0 : issued - kStages; seq < issued; ++seq)
-                mbar_wait_warp(&bars.kv_full[seq % kStages], (seq / kStages) & 1);
-            mbar_wait_warp(&bars.q_full, 0);
         }
+        if (!ok) record_timeout(bars, p.err);
+        // never leave while a copy into this CTA's shared memory may still land: only the
+        // last use of each slot (and of Q) can still be outstanding
+        for (int x = seq - kStages < 0 ? 0 : seq - kStages; x < seq; ++x)
+            mbar_wait_warp(&bars.kv_full[x % kStages], (x / kStages) & 1);
+        if (q_loads > 0) mbar_wait_warp(&bars.q_full, (q_loads - 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // the whole warp runs this loop converged; one elected lane issues each product
-        regs_decrease<88>();
+        // the whole warp runs this loop converged; lane 0 issues each product
+        regs_decrease<72>();
+        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
         {
             constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
             const uint32_t q_base = smem_u32(smem + L::kQOff);
             const uint32_t kv_base = smem_u32(smem + L::kKVOff);
-            auto act = [&](int t, int kb) { return kb >= lo[t] && kb <= hi[t]; };
             // Descriptors are built once; every product then only adds a constant
             // (byte offset / 16) to the start-address field, which keeps the issue loop short.
             const uint64_t q_desc = sdesc(q_base, 16, 1024);                // K-major, SW128
@@ -209,166 +260,184 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_ts_w(d, a + kk * 8, vd + kk * (2048 >> 4), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait_warp(&bars.q_full, 0);
-            int seq = 0;
-            int n_pv[2] = {0, 0};
-            if (ok) {
-                const int slot_k = seq % kStages;
-                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
-                if (ok) {
+            bool ok = true;
+            int seq = 0;                 // K/V ring position over all items
+            int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
+            for (int ii = 0; ok && ii < my_items; ++ii) {
+                const FwdItem it = fwd_item(fwd_item_index(ii), p);
+                auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
+                ok = mbar_wait_warp(&bars.q_full, ii & 1);
+                if (!ok) break;
+                {
+                    const int slot_k = seq % kStages;
+                    ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                    if (!ok) break;
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t)
-                        if (act(t, kb_lo)) issue_s(t, slot_k);
+                        if (act(t, it.kb_lo)) issue_s(t, slot_k);
                     mma_commit_w(&bars.kv_empty[slot_k]);
                     ++seq;
+                    if (it.kb_lo == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
                 }
-            }
-            for (int kb = kb_lo; ok && kb <= kb_hi; ++kb) {
-                const int slot_v = seq % kStages;
-                ok = mbar_wait_warp(&bars.kv_full[slot_v], (seq / kStages) & 1);
-                if (!ok) break;
-                ++seq;
-                const bool next = kb + 1 <= kb_hi;
-                const int slot_k = seq % kStages;
-                bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (act(t, kb)) {
-                        ok = mbar_wait_warp(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, slot_v, n_pv[t] > 0);
-                        ++n_pv[t];
-                    }
-                    if (next && act(t, kb + 1)) {
-                        if (!k_ready) {
-                            ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                bool first_pv = true;
+                for (int kb = it.kb_lo; ok && kb <= it.kb_hi; ++kb) {
+                    const int slot_v = seq % kStages;
+                    ok = mbar_wait_warp(&bars.kv_full[slot_v], (seq / kStages) & 1);
+                    if (!ok) break;
+                    ++seq;
+                    const bool next = kb + 1 <= it.kb_hi;
+                    const int slot_k = seq % kStages;
+                    bool k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (act(t, kb)) {
+                            if (first_pv && ii > 0) {
+                                // the epilogue of the previous item has read both O tiles
+                                ok = mbar_wait_warp(&bars.o_free, (ii - 1) & 1) && !aborted(bars);
+                                if (!ok) break;
+                            }
+                            first_pv = false;
+                            ok = mbar_wait_warp(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
                             if (!ok) break;
                             tc_fence_after();
-                            k_ready = true;
+                            issue_pv(t, slot_v, kb > it.lo[t]);
+                            ++n_pv[t];
                         }
-                        issue_s(t, slot_k);
+                        if (next && act(t, kb + 1)) {
+                            if (!k_ready) {
+                                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
+                                if (!ok) break;
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(t, slot_k);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_w(&bars.kv_empty[slot_v]);
+                    if (next) {
+                        mma_commit_w(&bars.kv_empty[slot_k]);
+                        ++seq;
+                        if (kb + 1 == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
                     }
                 }
-                if (!ok) break;
-                mma_commit_w(&bars.kv_empty[slot_v]);
-                if (next) {
-                    mma_commit_w(&bars.kv_empty[slot_k]);
-                    ++seq;
-                }
+                if (ok) mma_commit_w(&bars.o_final);
             }
             if (!ok) record_timeout(bars, p.err);
-            mma_commit_w(&bars.o_final);
             // all products must have landed before TMEM is released
             mma_commit_w(&bars.drain);
             mbar_wait_warp(&bars.drain, 0);
         }
     } else if (warp < 4) {
-        regs_decrease<88>();
+        regs_decrease<72>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        regs_increase<208>();
+        regs_increase<216>();
+        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
-        const int tr0 = t ? r0[1] : r0[0];
-        const int t_lo = t ? lo[1] : lo[0];
-        const int t_hi = t ? hi[1] : hi[0];
         const uint32_t t_col_s = t ? col_s[1] : col_s[0];
         const uint32_t t_col_o = t ? col_o[1] : col_o[0];
-        const int row = tr0 + row_in_tile;
-        const bool tile_on = (t == 0) || active1;
+        const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_s;
+        const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_o;
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        if (tile_on) {
-            const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_s;
-            const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_o;
-            int it = 0;
-            for (int kb = t_lo; kb <= t_hi; ++kb, ++it) {
-                ok = mbar_wait_warp(&bars.s_full[t], it & 1) && !aborted(bars);  // warp-uniform
-                if (!ok) break;
-                tc_fence_after();
-                float s[kBN];
-                {
-                    uint32_t r[kBN];
-                    tmem_ld128(s_addr, r);
+        int n_s = 0;  // S tiles of this query tile consumed over all items
+        for (int ii = 0; ok && ii < my_items; ++ii) {
+            const FwdItem item = fwd_item(fwd_item_index(ii), p);
+            const int tr0 = t ? item.r0[1] : item.r0[0];
+            const int t_lo = t ? item.lo[1] : item.lo[0];
+            const int t_hi = t ? item.hi[1] : item.hi[0];
+            const int row = tr0 + row_in_tile;
+            const bool tile_on = (t == 0) || item.active1;
+            float m_run = -INFINITY, l_run = 0.f;
+            if (tile_on) {
+                int it = 0;
+                for (int kb = t_lo; kb <= t_hi; ++kb, ++it, ++n_s) {
+                    ok = mbar_wait_warp(&bars.s_full[t], n_s & 1) && !aborted(bars);  // warp-uniform
+                    if (!ok) break;
+                    tc_fence_after();
+                    float s[kBN];
+                    {
+                        uint32_t r[kBN];
+                        tmem_ld128(s_addr, r);
 #pragma unroll
-                    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
-                }
-                // elementwise mask only on blocks that straddle the causal diagonal or the window edge
-                const int k0 = kb * kBN;
-                const bool full_block = (k0 + kBN - 1 <= tr0) && (k0 >= tr0 + kBM - p.W);
-                if (!full_block) {
-#pragma unroll
-                    for (int j = 0; j < kBN; ++j) {
-                        const int key = k0 + j;
-                        if (key > row || row - key >= p.W) s[j] = -INFINITY;
+                        for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
                     }
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                    // elementwise mask only on blocks that straddle the causal diagonal or the window edge
+                    const int k0 = kb * kBN;
+                    const bool full_block = (k0 + kBN - 1 <= tr0) && (k0 >= tr0 + kBM - p.W);
+                    if (!full_block) {
 #pragma unroll
-                for (int j = 4; j + 8 <= kBN; j += 8) {  // s[4 .. kBN-5]
-                    mx0 = max3f(mx0, s[j], s[j + 1]);
-                    mx1 = max3f(mx1, s[j + 2], s[j + 3]);
-                    mx2 = max3f(mx2, s[j + 4], s[j + 5]);
-                    mx3 = max3f(mx3, s[j + 6], s[j + 7]);
-                }
-                mx0 = max3f(mx0, s[kBN - 4], s[kBN - 3]);
-                mx1 = max3f(mx1, s[kBN - 2], s[kBN - 1]);
-                const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-                if (it == 0) {
-                    m_run = m_cand;
-                } else {
-                    const bool want = m_cand > m_run + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, want)) {
-                        const float m_new = fmaxf(m_run, m_cand);
-                        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
-                        m_run = m_new;
-                        l_run *= alpha;
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t r[32];
-                            tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_st32(o_addr + c * 32, r);
+                        for (int j = 0; j < kBN; ++j) {
+                            const int key = k0 + j;
+                            if (key > row || row - key >= p.W) s[j] = -INFINITY;
                         }
                     }
-                }
-                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+                    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 0; c < kBN / 64; ++c) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float x0, x1, x2, x3;
-                        const int j = c * 64 + 2 * i;
-                        fma_f32x2(x0, x1, s[j], s[j + 1], sl2, sl2, -m_use, -m_use);
-                        fma_f32x2(x2, x3, s[j + 2], s[j + 3], sl2, sl2, -m_use, -m_use);
-                        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-                        const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
-                        add_f32x2(sum0, sum1, sum0, sum1, e0, e1);
-                        add_f32x2(sum2, sum3, sum2, sum3, e2, e3);
-                        pk[i] = pack_bf16x2(e0, e1);
-                        pk[i + 1] = pack_bf16x2(e2, e3);
+                    for (int j = 4; j + 8 <= kBN; j += 8) {  // s[4 .. kBN-5]
+                        mx0 = max3f(mx0, s[j], s[j + 1]);
+                        mx1 = max3f(mx1, s[j + 2], s[j + 3]);
+                        mx2 = max3f(mx2, s[j + 4], s[j + 5]);
+                        mx3 = max3f(mx3, s[j + 6], s[j + 7]);
                     }
-                    tmem_st32(s_addr + c * 32, pk);
+                    mx0 = max3f(mx0, s[kBN - 4], s[kBN - 3]);
+                    mx1 = max3f(mx1, s[kBN - 2], s[kBN - 1]);
+                    const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                    if (it == 0) {
+                        m_run = m_cand;
+                    } else {
+                        const bool want = m_cand > m_run + kRescaleThreshold;
+                        if (__any_sync(0xffffffffu, want)) {
+                            const float m_new = fmaxf(m_run, m_cand);
+                            const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
+                            m_run = m_new;
+                            l_run *= alpha;
+#pragma unroll
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t r[32];
+                                tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(o_addr + c * 32, r);
+                            }
+                        }
+                    }
+                    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                    float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kBN / 64; ++c) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float x0, x1, x2, x3;
+                            const int j = c * 64 + 2 * i;
+                            fma_f32x2(x0, x1, s[j], s[j + 1], sl2, sl2, -m_use, -m_use);
+                            fma_f32x2(x2, x3, s[j + 2], s[j + 3], sl2, sl2, -m_use, -m_use);
+                            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                            const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+                            add_f32x2(sum0, sum1, sum0, sum1, e0, e1);
+                            add_f32x2(sum2, sum3, sum2, sum3, e2, e3);
+                            pk[i] = pack_bf16x2(e0, e1);
+                            pk[i + 1] = pack_bf16x2(e2, e3);
+                        }
+                        tmem_st32(s_addr + c * 32, pk);
+                    }
+                    l_run += (sum0 + sum1) + (sum2 + sum3);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars.p_full[t]);
                 }
-                l_run += (sum0 + sum1) + (sum2 + sum3);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars.p_full[t]);
             }
-            // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
-            if (ok) ok = mbar_wait_warp(&bars.o_final, 0) && !aborted(bars);
-            if (!ok) {
-                record_timeout(bars, p.err);
-            } else {
-                tc_fence_after();
+            // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2; then hand both O tiles back
+            if (ok) ok = mbar_wait_warp(&bars.o_final, ii & 1) && !aborted(bars);
+            if (!ok) break;
+            tc_fence_after();
+            if (tile_on) {
                 const float inv_l = 1.f / l_run;
                 const bool in_range = row < p.T;
-                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.T + row) * p.H + h) * D;
+                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(item.b) * p.T + row) * p.H + item.h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -385,9 +454,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         }
                     }
                 }
-                if (in_range) p.lse[(static_cast<size_t>(b) * p.H + h) * p.T + row] = (m_run + __log2f(l_run)) * kLn2;
+                if (in_range)
+                    p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.T + row] = (m_run + __log2f(l_run)) * kLn2;
             }
+            tc_fence_before();
+            mbar_arrive(&bars.o_free);
         }
+        if (!ok) record_timeout(bars, p.err);
     }
     tc_fence_before();
     __syncthreads();
@@ -424,7 +497,15 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
-    dim3 grid(p.n_pairs, H, B);
+    // persistent: one CTA per SM (shared memory and TMEM allow one), looping over the items
+    static int sms[64] = {0};
+    if (dev < 64 && sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const long n_items = (long)p.n_pairs * H * B;
+    const int n_sm = dev < 64 ? sms[dev] : 148;
+    const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
     count_launches(1);
     return cudaGetLastError();

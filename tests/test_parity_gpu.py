@@ -84,6 +84,9 @@ SWEEP = [
     (1, 200, 2, 128, 127), (1, 200, 1, 128, 128), (1, 257, 1, 128, 129), (1, 333, 2, 64, 332),
     (1, 333, 1, 128, 333), (1, 333, 1, 128, 338), (2, 384, 3, 128, -1), (1, 513, 2, 64, 100),
     (1, 640, 1, 128, 256), (1, 700, 1, 128, 512),
+    # more (query-tile pair, head, batch) work items than SMs, so persistent CTAs run several
+    # items each, including items whose second query tile lies past T
+    (2, 800, 48, 64, 300), (1, 1100, 40, 128, 200),
 ]
 
 
