@@ -177,12 +177,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tmem = bars->tmem_base;
     constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
 
-    // registers: 512 x 128 at launch = 65536; producer/MMA warpgroup drops to 96,
-    // the dQ warpgroup to 96, the two P/dS warpgroups rise to 160 (65536 in all)
+    // registers: 512 x 128 at launch = 65536; producer/MMA warpgroup drops to 56, the two
+    // P/dS warpgroups rise to 152 and the dQ warpgroup to 152 (65536 in all), which lets
+    // the dQ warpgroup hold a whole 128 x 128 fp32 dQ block and release TMEM at once
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
-        regs_decrease<96>();
+        regs_decrease<56>();
         {
             if (lane == 0) {
                 tma_prefetch_desc(&tm_q);
@@ -230,7 +231,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
-        regs_decrease<96>();
+        regs_decrease<56>();
         {
             constexpr uint32_t id_kq = idesc_bf16(kBK, kBQ, false, false);  // S^T, dP^T
             constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
@@ -335,10 +336,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_wait_warp(&bars->drain, 0);
         }
     } else if (warp < 4) {
-        regs_decrease<96>();
+        regs_decrease<56>();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ P^T / dS^T (thread = key row)
-        regs_increase<160>();
+        regs_increase<152>();
         const int g = (warp - 4) / 4;            // query columns [64 g, 64 g + 64)
         const int tid = threadIdx.x - 128 * (g + 1);
         const int lane_base = 32 * (warp % 4);
@@ -368,53 +369,67 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float* lb = s_lse + (it & 1) * kBQ;
             const float* db = s_delta + (it & 1) * kBQ;
             const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
-            // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries
+            // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries.
+            // The row statistics of the first 32 queries are read before the wait so that their
+            // shared-memory latency hides behind it; the second 32 are read while the first are used.
+            float4 L4[8];
+#pragma unroll
+            for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(lb + 64 * g + 4 * x4);
             ok = mbar_wait_warp(&bars->s_full, it & 1) && !aborted(bars);
             if (!ok) continue;
             tc_fence_after();
-            float pf[64];
-            uint32_t sr[64];
+            // P^T in bf16, two per word: the same values feed the dV product (through TMEM)
+            // and dS below, so both use one rounding of P
+            uint32_t pp[32];
             {
-                uint32_t a[32], b2[32];
-                tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
+                uint32_t sr[64];
+                {
+                    uint32_t a[32], b2[32];
+                    tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    sr[x] = a[x];
-                    sr[32 + x] = b2[x];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int q0 = 64 * g + 32 * c;
-                uint32_t pk[16];
-#pragma unroll
-                for (int x4 = 0; x4 < 8; ++x4) {
-                    const float4 L4 = *reinterpret_cast<const float4*>(lb + q0 + 4 * x4);
-                    float e[4];
-                    fma_f32x2(e[0], e[1], __uint_as_float(sr[32 * c + 4 * x4]), __uint_as_float(sr[32 * c + 4 * x4 + 1]),
-                              sl2, sl2, -L4.x, -L4.y);
-                    fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
-                              __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -L4.z, -L4.w);
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) {
-                        float pr = ex2_approx(e[y]);
-                        if (!full) {
-                            const int i = i0 + q0 + 4 * x4 + y;
-                            if (j > i || i - j >= p.W) pr = 0.f;
-                        }
-                        pf[32 * c + 4 * x4 + y] = pr;
+                    for (int x = 0; x < 32; ++x) {
+                        sr[x] = a[x];
+                        sr[32 + x] = b2[x];
                     }
-                    pk[2 * x4] = pack_bf16x2(pf[32 * c + 4 * x4], pf[32 * c + 4 * x4 + 1]);
-                    pk[2 * x4 + 1] = pack_bf16x2(pf[32 * c + 4 * x4 + 2], pf[32 * c + 4 * x4 + 3]);
                 }
-                // packed into the first half of this warpgroup's own (already read) columns
-                tmem_st16(st_addr + 64 * g + 16 * c, pk);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int q0 = 64 * g + 32 * c;
+#pragma unroll
+                    for (int x4 = 0; x4 < 8; ++x4) {
+                        const float4 Lq = L4[x4];
+                        if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(lb + q0 + 32 + 4 * x4);
+                        float e[4];
+                        fma_f32x2(e[0], e[1], __uint_as_float(sr[32 * c + 4 * x4]),
+                                  __uint_as_float(sr[32 * c + 4 * x4 + 1]), sl2, sl2, -Lq.x, -Lq.y);
+                        fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
+                                  __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -Lq.z, -Lq.w);
+                        float pr[4];
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {
+                            pr[y] = ex2_approx(e[y]);
+                            if (!full) {
+                                const int i = i0 + q0 + 4 * x4 + y;
+                                if (j > i || i - j >= p.W) pr[y] = 0.f;
+                            }
+                        }
+                        pp[16 * c + 2 * x4] = pack_bf16x2(pr[0], pr[1]);
+                        pp[16 * c + 2 * x4 + 1] = pack_bf16x2(pr[2], pr[3]);
+                    }
+                    // packed into the first half of this warpgroup's own (already read) columns
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) pk[x] = pp[16 * c + x];
+                    tmem_st16(st_addr + 64 * g + 16 * c, pk);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full);
             // phase 2: dS^T = P^T (dP^T - Delta), packed into DPT (A operand of dK) and into the
             // shared-memory tile [key][query] (MN-major operand of dQ)
+#pragma unroll
+            for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(db + 64 * g + 4 * x4);
             ok = mbar_wait_warp(&bars->dp_full, it & 1) && !aborted(bars);
             if (!ok) continue;
             tc_fence_after();
@@ -435,13 +450,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 uint32_t dk[16];
 #pragma unroll
                 for (int x4 = 0; x4 < 8; ++x4) {
-                    const float4 D4 = *reinterpret_cast<const float4*>(db + q0 + 4 * x4);
+                    const float4 Dq = L4[x4];
+                    if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(db + q0 + 32 + 4 * x4);
+                    const uint32_t w0 = pp[16 * c + 2 * x4], w1 = pp[16 * c + 2 * x4 + 1];
                     float t[4], ds[4];
-                    add_f32x2(t[0], t[1], __uint_as_float(dr[4 * x4]), __uint_as_float(dr[4 * x4 + 1]), -D4.x, -D4.y);
-                    add_f32x2(t[2], t[3], __uint_as_float(dr[4 * x4 + 2]), __uint_as_float(dr[4 * x4 + 3]), -D4.z,
-                              -D4.w);
-                    mul_f32x2(ds[0], ds[1], pf[32 * c + 4 * x4], pf[32 * c + 4 * x4 + 1], t[0], t[1]);
-                    mul_f32x2(ds[2], ds[3], pf[32 * c + 4 * x4 + 2], pf[32 * c + 4 * x4 + 3], t[2], t[3]);
+                    add_f32x2(t[0], t[1], __uint_as_float(dr[4 * x4]), __uint_as_float(dr[4 * x4 + 1]), -Dq.x, -Dq.y);
+                    add_f32x2(t[2], t[3], __uint_as_float(dr[4 * x4 + 2]), __uint_as_float(dr[4 * x4 + 3]), -Dq.z,
+                              -Dq.w);
+                    mul_f32x2(ds[0], ds[1], __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), t[0], t[1]);
+                    mul_f32x2(ds[2], ds[3], __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u), t[2], t[3]);
                     dk[2 * x4] = pack_bf16x2(ds[0], ds[1]);
                     dk[2 * x4 + 1] = pack_bf16x2(ds[2], ds[3]);
                 }
@@ -494,7 +511,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ dQ partials into the fp32 accumulator
-        regs_decrease<96>();
+        regs_increase<152>();
         const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
@@ -510,31 +527,24 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tc_fence_after();
             if constexpr (L::kTmaReduce) {
-                // thread = dQ column d, TMEM columns = the block's 128 query rows.  Each half
-                // (64 rows) goes to the fp32 staging tile [row][d] and is added to the
-                // accumulator by one TMA reduce-add, which frees the SM's load/store path.
+                // thread = dQ column d, TMEM columns = the block's 128 query rows.  The whole
+                // block is read into registers first, so the TMEM columns go back to the MMA
+                // warp (for the next dP^T) before any of the staging work.  Each half (64 rows)
+                // then goes to the fp32 staging tile [row][d] and is added to the accumulator by
+                // one TMA reduce-add, which keeps the SM's load/store path free.
                 float* stage = reinterpret_cast<float*>(smem + L::kStage);
+                uint32_t r0[64], r1[64];
+                tmem_ld64_nowait(st_addr, r0);
+                tmem_ld64_nowait(st_addr + 64, r1);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars->dq_empty);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    uint32_t r[64];
-                    {
-                        uint32_t a[32], c2[32];
-                        tmem_ld32x2(st_addr + 64 * half, st_addr + 64 * half + 32, a, c2);
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            r[x] = a[x];
-                            r[32 + x] = c2[x];
-                        }
-                    }
-                    if (half == 1) {
-                        // the block's dQ is now in registers: hand the TMEM columns back
-                        tc_fence_before();
-                        mbar_arrive(&bars->dq_empty);
-                    }
                     if (tid == 0) bulk_wait_read();  // the previous reduce-add has read the staging tile
                     named_bar_sync(3, 128);
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(r[x]);
+                    for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(half ? r1[x] : r0[x]);
                     fence_async_smem();
                     named_bar_sync(3, 128);
                     if (tid == 0) {
