@@ -48,6 +48,9 @@ constexpr int kBK = 128;       // keys per CTA
 constexpr int kBQ = 128;       // queries per block
 constexpr int kQStages = 2;
 constexpr int kThreads = 512;
+constexpr int kItemSlots = 2;   // work-item ring between the producer and the other roles
+// warps that read each work-item slot: the MMA warp, the 8 P/dS warps and the 4 dQ warps
+constexpr int kItemReaders = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // D = 128: dQ partials leave through a TMA reduce-add from a 64-row fp32 staging tile,
@@ -74,6 +77,7 @@ struct BwdSmem {
 
 struct BwdBarriers {
     uint64_t kv_full;
+    uint64_t kv_empty;
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
     uint64_t do_full[2];
@@ -86,9 +90,13 @@ struct BwdBarriers {
     uint64_t dq_empty;
     uint64_t final_;
     uint64_t drain;
+    uint64_t item_full[kItemSlots];
+    uint64_t item_empty[kItemSlots];
+    int item[kItemSlots];
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(BwdBarriers) <= 256, "barrier block outgrew its shared-memory slot");
 
 struct BwdParams {
     const float* lse;      // [B, H, T]
@@ -99,11 +107,66 @@ struct BwdParams {
     int B, T, H, W;        // W effective, 1 <= W <= T
     float scale, scale_log2;
     int n_kb, n_qb;
+    int group;             // (batch, head) pairs per scheduling group
+    int* work;             // work-item counter, zero on entry
     int* err;
 };
 
+// One work item: a 128-key block n of one (batch, head), walked over query blocks
+// m_lo .. m_lo + n_it - 1 (the blocks whose causal window reaches its keys).
+//
+// Items are handed out in index order by an atomic counter.  The (batch, head) pairs are cut
+// into groups of p.group (about one wave of CTAs' worth of items); inside a group the index
+// runs over n outermost, so the longest causal walks (small n) go first, while the CTAs that
+// run at the same time share the Q and dO blocks of a few heads in L2.
+struct BwdItem {
+    int n, h, b, j0, m_lo, n_it;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(int w, const BwdParams& p) {
+    BwdItem it;
+    const int per_group = p.n_kb * p.group;
+    const int grp = w / per_group, r = w - grp * per_group;
+    const int in_grp = min(p.group, p.B * p.H - grp * p.group);  // the last group may be short
+    const int bh = grp * p.group + r % in_grp;
+    it.n = r / in_grp;
+    it.h = bh % p.H;
+    it.b = bh / p.H;
+    it.j0 = it.n * kBK;
+    it.m_lo = it.n;  // kBQ == kBK: query block n holds the first queries at or after key j0
+    const int m_hi = min(p.n_qb - 1, (it.j0 + kBK - 1 + p.W - 1) / kBQ);
+    it.n_it = m_hi - it.m_lo + 1;
+    return it;
+}
+
 __device__ __forceinline__ bool aborted(const BwdBarriers* bars) {
     return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
+}
+
+// Producer warp (converged): take the next item index from the global counter and publish it
+// in ring slot k % kItemSlots; -1 once every item is taken.  Returns what it published, or -2
+// if the wait for the slot ran out.
+__device__ __forceinline__ int publish_item(BwdBarriers* bars, int k, int n_items, int* work) {
+    const int slot = k % kItemSlots;
+    if (!mbar_wait_warp(&bars->item_empty[slot], ((k / kItemSlots) & 1) ^ 1)) return -2;
+    int w = 0;
+    if (lane_id() == 0) {
+        w = atomicAdd(work, 1);
+        if (w >= n_items) w = -1;
+        bars->item[slot] = w;
+        mbar_arrive(&bars->item_full[slot]);  // release: the index is visible to whoever sees the phase
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+}
+
+// Any other warp (converged): the index in ring slot k % kItemSlots, or -2 if the wait ran out.
+__device__ __forceinline__ int read_item(BwdBarriers* bars, int k) {
+    const int slot = k % kItemSlots;
+    if (!mbar_wait_warp(&bars->item_full[slot], (k / kItemSlots) & 1)) return -2;
+    const int w = *reinterpret_cast<volatile const int*>(&bars->item[slot]);
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(&bars->item_empty[slot]);
+    return w;
 }
 
 __device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
@@ -113,10 +176,6 @@ __device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
 
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float* addr, float a) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
@@ -136,11 +195,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* s_delta = reinterpret_cast<float*>(smem + L::kDelta);
 
     const int warp = warp_id(), lane = lane_id();
-    const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int j0 = n * kBK;
-    const int m_lo = n;
-    const int m_hi = min(p.n_qb - 1, (j0 + kBK - 1 + p.W - 1) / kBQ);
-    const int n_it = m_hi - m_lo + 1;
+    const int n_items = p.n_kb * p.H * p.B;
 
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
@@ -148,6 +203,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (threadIdx.x == 0) {
         mbar_init(&bars->kv_full, 1);
+        mbar_init(&bars->kv_empty, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars->q_full[s], 1);
             mbar_init(&bars->q_empty[s], 1);
@@ -164,6 +220,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bars->dq_empty, kBQ);
         mbar_init(&bars->final_, 1);
         mbar_init(&bars->drain, 1);
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(&bars->item_full[s], 1);
+            mbar_init(&bars->item_empty[s], kItemReaders);
+        }
         bars->abort = 0;
         fence_barrier_init();
     }
@@ -192,41 +252,59 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tma_prefetch_desc(&tm_do);
             }
             __syncwarp();
-            mbar_arrive_expect_tx_w(&bars->kv_full, 2 * L::kTile);
-            for (int c = 0; c < D / 64; ++c) {
-                tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, h, j0, b);
-                tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, h, j0, b);
-            }
-            int issued_q = 0, issued_do = 0;
-            for (int it = 0; it < n_it; ++it) {
-                const int st = it % kQStages, so = it % L::kDOStages;
-                const int i0 = (m_lo + it) * kBQ;
-                if (!mbar_wait_warp(&bars->q_empty[st], ((it / kQStages) & 1) ^ 1) || aborted(bars)) {
-                    record_timeout(bars, p.err);
+            int gq = 0, gd = 0;  // Q and dO blocks loaded over all items (ring positions)
+            int kv_loads = 0;
+            bool ok = true;
+            for (int ii = 0; ok; ++ii) {
+                const int w = publish_item(bars, ii, n_items, p.work);
+                if (w == -2 || aborted(bars)) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_w(&bars->q_full[st], L::kTile);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64, h,
-                                  i0, b);
-                issued_q = it + 1;
-                if (!mbar_wait_warp(&bars->do_empty[so], ((it / L::kDOStages) & 1) ^ 1) || aborted(bars)) {
-                    record_timeout(bars, p.err);
+                if (w < 0) break;
+                const BwdItem item = bwd_item(w, p);
+                // K and V of this item once every product of the previous item has read theirs
+                if (!mbar_wait_warp(&bars->kv_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_w(&bars->do_full[so], L::kTile);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(smem + L::kDO + so * L::kTile + c * kBQ * 128, &tm_do, &bars->do_full[so], c * 64,
-                                  h, i0, b);
-                issued_do = it + 1;
+                mbar_arrive_expect_tx_w(&bars->kv_full, 2 * L::kTile);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, item.h, item.j0, item.b);
+                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, item.h, item.j0, item.b);
+                }
+                ++kv_loads;
+                for (int it = 0; it < item.n_it; ++it) {
+                    const int st = gq % kQStages, so = gd % L::kDOStages;
+                    const int i0 = (item.m_lo + it) * kBQ;
+                    if (!mbar_wait_warp(&bars->q_empty[st], ((gq / kQStages) & 1) ^ 1) || aborted(bars)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_w(&bars->q_full[st], L::kTile);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64,
+                                      item.h, i0, item.b);
+                    ++gq;
+                    if (!mbar_wait_warp(&bars->do_empty[so], ((gd / L::kDOStages) & 1) ^ 1) || aborted(bars)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_w(&bars->do_full[so], L::kTile);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d_w(smem + L::kDO + so * L::kTile + c * kBQ * 128, &tm_do, &bars->do_full[so],
+                                      c * 64, item.h, i0, item.b);
+                    ++gd;
+                }
             }
+            if (!ok) record_timeout(bars, p.err);
             // never leave while a copy into this CTA's shared memory may still land: the last
             // use of each stage is the only one whose completion can still be outstanding
-            for (int it = issued_q - kQStages < 0 ? 0 : issued_q - kQStages; it < issued_q; ++it)
-                mbar_wait_warp(&bars->q_full[it % kQStages], (it / kQStages) & 1);
-            for (int it = issued_do - L::kDOStages < 0 ? 0 : issued_do - L::kDOStages; it < issued_do; ++it)
-                mbar_wait_warp(&bars->do_full[it % L::kDOStages], (it / L::kDOStages) & 1);
-            mbar_wait_warp(&bars->kv_full, 0);
+            for (int x = gq - kQStages < 0 ? 0 : gq - kQStages; x < gq; ++x)
+                mbar_wait_warp(&bars->q_full[x % kQStages], (x / kQStages) & 1);
+            for (int x = gd - L::kDOStages < 0 ? 0 : gd - L::kDOStages; x < gd; ++x)
+                mbar_wait_warp(&bars->do_full[x % L::kDOStages], (x / L::kDOStages) & 1);
+            if (kv_loads > 0) mbar_wait_warp(&bars->kv_full, (kv_loads - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -265,73 +343,93 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 mma_commit_w(&bars->dp_full);
             };
-            bool ok = mbar_wait_warp(&bars->kv_full, 0) && mbar_wait_warp(&bars->q_full[0], 0) &&
-                      mbar_wait_warp(&bars->do_full[0], 0);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it % kQStages, so = it % L::kDOStages;
-                const uint64_t q_m = q_mn + st * kTileStep, do_m = do_mn + so * kTileStep;
-                // dV += P^T dO  (A = P^T packed in ST, K = 128 queries, 16 per product)
-                ok = mbar_wait_warp(&bars->p_full, it & 1) && !aborted(bars);
+            bool ok = true;
+            int gi = 0;  // query blocks processed over all items: the phase of every per-block barrier
+            for (int ii = 0; ok; ++ii) {
+                const int w = read_item(bars, ii);
+                if (w == -2) {
+                    ok = false;
+                    break;
+                }
+                if (w < 0) break;
+                const BwdItem item = bwd_item(w, p);
+                ok = mbar_wait_warp(&bars->kv_full, ii & 1) && !aborted(bars);
                 if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk) {
-                    const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // packed P^T / dS^T columns
-                    mma_ts_w(tmem + kColDV, tmem + kColST + pc, do_m + kk * (2048 >> 4), id_kd,
-                             (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
-                // dK += dS^T Q  (A = dS^T packed in DPT: reading A from TMEM halves this
-                // product's shared-memory traffic, and shared-memory bandwidth is what the
-                // products of this kernel compete for)
-                ok = mbar_wait_warp(&bars->ds_full, it & 1) && !aborted(bars);
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk) {
-                    const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_ts_w(tmem + kColDK, tmem + kColDPT + pc, q_m + kk * (2048 >> 4), id_kd,
-                             (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_w(&bars->q_empty[st]);  // Q of this block: S^T and dK were its readers
-                // dQ of this block into DPT (issued after dK, which read dS^T from DPT)
-                if constexpr (D == 128) {
-                    // dQ_m^T = K^T dS^T  (M = D lanes, N = queries, K = keys): a warp then holds 32
-                    // consecutive dQ columns of one query row, so each atomic covers a full line
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_ss_w(tmem + kColDPT, k_mn + kk * (2048 >> 4), ds_mn + kk * (2048 >> 4), id_dqt,
-                                 kk > 0 ? 1u : 0u);
-                } else {
-                    // dQ_m = dS K  (M = queries, K = keys, N = D)
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_ss_w(tmem + kColDPT, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd,
-                                 kk > 0 ? 1u : 0u);
-                }
-                mma_commit_w(&bars->dq_full);
-                if (it + 1 < n_it) {
-                    // next block: S^T into ST right away (dV above was the last reader of P^T);
-                    // dP^T into DPT once this block's dQ has been read out
-                    const int st1 = (it + 1) % kQStages, so1 = (it + 1) % L::kDOStages;
-                    ok = mbar_wait_warp(&bars->q_full[st1], ((it + 1) / kQStages) & 1) && !aborted(bars);
+                {
+                    // first block of the item: S^T, then dP^T once the previous block's dQ has left DPT
+                    const int st = gi % kQStages, so = gi % L::kDOStages;
+                    ok = mbar_wait_warp(&bars->q_full[st], (gi / kQStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(st1);
-                    ok = mbar_wait_warp(&bars->dq_empty, it & 1) &&
-                         mbar_wait_warp(&bars->do_full[so1], ((it + 1) / L::kDOStages) & 1) && !aborted(bars);
+                    issue_s(st);
+                    ok = (gi == 0 || mbar_wait_warp(&bars->dq_empty, (gi - 1) & 1)) &&
+                         mbar_wait_warp(&bars->do_full[so], (gi / L::kDOStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_dp(so1);
+                    issue_dp(so);
                 }
+                for (int it = 0; it < item.n_it; ++it, ++gi) {
+                    const int st = gi % kQStages, so = gi % L::kDOStages;
+                    const uint64_t q_m = q_mn + st * kTileStep, do_m = do_mn + so * kTileStep;
+                    // dV += P^T dO  (A = P^T packed in ST, K = 128 queries, 16 per product)
+                    ok = mbar_wait_warp(&bars->p_full, gi & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBQ / 16; ++kk) {
+                        const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // packed P^T / dS^T columns
+                        mma_ts_w(tmem + kColDV, tmem + kColST + pc, do_m + kk * (2048 >> 4), id_kd,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
+                    // dK += dS^T Q  (A = dS^T packed in DPT: reading A from TMEM halves this
+                    // product's shared-memory traffic, and shared-memory bandwidth is what the
+                    // products of this kernel compete for)
+                    ok = mbar_wait_warp(&bars->ds_full, gi & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBQ / 16; ++kk) {
+                        const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                        mma_ts_w(tmem + kColDK, tmem + kColDPT + pc, q_m + kk * (2048 >> 4), id_kd,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit_w(&bars->q_empty[st]);  // Q of this block: S^T and dK were its readers
+                    // dQ of this block into DPT (issued after dK, which read dS^T from DPT)
+                    if constexpr (D == 128) {
+                        // dQ_m^T = K^T dS^T  (M = D lanes, N = queries, K = keys)
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_ss_w(tmem + kColDPT, k_mn + kk * (2048 >> 4), ds_mn + kk * (2048 >> 4), id_dqt,
+                                     kk > 0 ? 1u : 0u);
+                    } else {
+                        // dQ_m = dS K  (M = queries, K = keys, N = D)
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_ss_w(tmem + kColDPT, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd,
+                                     kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit_w(&bars->dq_full);
+                    if (it + 1 < item.n_it) {
+                        // next block: S^T into ST right away (dV above was the last reader of P^T);
+                        // dP^T into DPT once this block's dQ has been read out
+                        const int st1 = (gi + 1) % kQStages, so1 = (gi + 1) % L::kDOStages;
+                        ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(st1);
+                        ok = mbar_wait_warp(&bars->dq_empty, gi & 1) &&
+                             mbar_wait_warp(&bars->do_full[so1], ((gi + 1) / L::kDOStages) & 1) && !aborted(bars);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_dp(so1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_w(&bars->kv_empty);  // every product that reads this item's K and V is issued
+                mma_commit_w(&bars->final_);    // DK and DV of this item are complete once these land
             }
             if (!ok) record_timeout(bars, p.err);
-            mma_commit_w(&bars->final_);
             mma_commit_w(&bars->drain);
             mbar_wait_warp(&bars->drain, 0);
         }
@@ -343,168 +441,186 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int g = (warp - 4) / 4;            // query columns [64 g, 64 g + 64)
         const int tid = threadIdx.x - 128 * (g + 1);
         const int lane_base = 32 * (warp % 4);
-        const int j = j0 + tid;
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColST;
         const uint32_t dpt_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;
         uint8_t* ds_row = smem + L::kDS + g * (kBK * 128) + tid * 128;
         const float sl2 = p.scale_log2;
-        const size_t rowvec = (static_cast<size_t>(b) * p.H + h) * p.T;
-        // row statistics of this warpgroup's 64 queries, loaded one iteration ahead:
-        // threads 0-63 fetch lse, threads 64-127 fetch Delta
+        // row statistics of this warpgroup's 64 queries, loaded one block ahead (across item
+        // boundaries too): threads 0-63 fetch lse, threads 64-127 fetch Delta
         const bool fetch_lse = tid < 64;
         const int qoff = 64 * g + (tid & 63);
-        auto stat = [&](int i) {
+        auto stat = [&](const BwdItem& item, int i) {
             if (i >= p.T) return fetch_lse ? INFINITY : 0.f;
+            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T;
             return fetch_lse ? p.lse[rowvec + i] * kLog2e : p.delta[rowvec + i];
         };
-        float nx = stat(m_lo * kBQ + qoff);
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int m = m_lo + it;
-            const int i0 = m * kBQ;
-            (fetch_lse ? s_lse : s_delta)[(it & 1) * kBQ + qoff] = nx;
-            if (it + 1 < n_it) nx = stat(i0 + kBQ + qoff);
-            // the warpgroup leaves together if any of its warps saw a wait run out
-            if (!named_bar_and(1 + g, 128, ok)) break;
-            const float* lb = s_lse + (it & 1) * kBQ;
-            const float* db = s_delta + (it & 1) * kBQ;
-            const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
-            // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries.
-            // The row statistics of the first 32 queries are read before the wait so that their
-            // shared-memory latency hides behind it; the second 32 are read while the first are used.
-            float4 L4[8];
-#pragma unroll
-            for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(lb + 64 * g + 4 * x4);
-            ok = mbar_wait_warp(&bars->s_full, it & 1) && !aborted(bars);
-            if (!ok) continue;
-            tc_fence_after();
-            // P^T in bf16, two per word: the same values feed the dV product (through TMEM)
-            // and dS below, so both use one rounding of P
-            uint32_t pp[32];
-            {
-                uint32_t sr[64];
+        int gi = 0;  // query blocks processed over all items: the phase of every per-block barrier
+        for (int ii = 0;; ++ii) {
+            const int w = read_item(bars, ii);
+            // every warp read the same slot; leave together if any of them timed out
+            if (!named_bar_and(1 + g, 128, ok && w != -2)) {
+                ok = false;
+                record_timeout(bars, p.err);
+                break;
+            }
+            if (w < 0) break;
+            const BwdItem item = bwd_item(w, p);
+            const int n = item.n, h = item.h, b = item.b, j0 = item.j0;
+            const int j = j0 + tid;
+            float nx = stat(item, item.m_lo * kBQ + qoff);
+            for (int it = 0; it < item.n_it; ++it, ++gi) {
+                const int m = item.m_lo + it;
+                const int i0 = m * kBQ;
+                (fetch_lse ? s_lse : s_delta)[(gi & 1) * kBQ + qoff] = nx;
+                if (it + 1 < item.n_it) nx = stat(item, i0 + kBQ + qoff);
+                // the warpgroup leaves together if any of its warps saw a wait run out
+                if (!named_bar_and(1 + g, 128, ok)) break;
+                const float* lb = s_lse + (gi & 1) * kBQ;
+                const float* db = s_delta + (gi & 1) * kBQ;
+                const bool full = (n < m) && (i0 + kBQ - 1 - j0 < p.W);
+                // phase 1: P^T = exp2(S^T scale log2e - lse log2e) on this warpgroup's 64 queries.
+                // The row statistics of the first 32 queries are read before the wait so that their
+                // shared-memory latency hides behind it; the second 32 are read while the first are used.
+                float4 L4[8];
+    #pragma unroll
+                for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(lb + 64 * g + 4 * x4);
+                ok = mbar_wait_warp(&bars->s_full, gi & 1) && !aborted(bars);
+                if (!ok) continue;
+                tc_fence_after();
+                // P^T in bf16, two per word: the same values feed the dV product (through TMEM)
+                // and dS below, so both use one rounding of P
+                uint32_t pp[32];
+                {
+                    uint32_t sr[64];
+                    {
+                        uint32_t a[32], b2[32];
+                        tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
+    #pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            sr[x] = a[x];
+                            sr[32 + x] = b2[x];
+                        }
+                    }
+    #pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int q0 = 64 * g + 32 * c;
+    #pragma unroll
+                        for (int x4 = 0; x4 < 8; ++x4) {
+                            const float4 Lq = L4[x4];
+                            if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(lb + q0 + 32 + 4 * x4);
+                            float e[4];
+                            fma_f32x2(e[0], e[1], __uint_as_float(sr[32 * c + 4 * x4]),
+                                      __uint_as_float(sr[32 * c + 4 * x4 + 1]), sl2, sl2, -Lq.x, -Lq.y);
+                            fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
+                                      __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -Lq.z, -Lq.w);
+                            float pr[4];
+    #pragma unroll
+                            for (int y = 0; y < 4; ++y) {
+                                pr[y] = ex2_approx(e[y]);
+                                if (!full) {
+                                    const int i = i0 + q0 + 4 * x4 + y;
+                                    if (j > i || i - j >= p.W) pr[y] = 0.f;
+                                }
+                            }
+                            pp[16 * c + 2 * x4] = pack_bf16x2(pr[0], pr[1]);
+                            pp[16 * c + 2 * x4 + 1] = pack_bf16x2(pr[2], pr[3]);
+                        }
+                        // packed into the first half of this warpgroup's own (already read) columns
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int x = 0; x < 16; ++x) pk[x] = pp[16 * c + x];
+                        tmem_st16(st_addr + 64 * g + 16 * c, pk);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full);
+                // phase 2: dS^T = P^T (dP^T - Delta), packed into DPT (A operand of dK) and into the
+                // shared-memory tile [key][query] (MN-major operand of dQ)
+    #pragma unroll
+                for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(db + 64 * g + 4 * x4);
+                ok = mbar_wait_warp(&bars->dp_full, gi & 1) && !aborted(bars);
+                if (!ok) continue;
+                tc_fence_after();
+                uint32_t drr[64];
                 {
                     uint32_t a[32], b2[32];
-                    tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
-#pragma unroll
+                    tmem_ld32x2(dpt_addr + 64 * g, dpt_addr + 64 * g + 32, a, b2);  // one wait for both chunks
+    #pragma unroll
                     for (int x = 0; x < 32; ++x) {
-                        sr[x] = a[x];
-                        sr[32 + x] = b2[x];
+                        drr[x] = a[x];
+                        drr[32 + x] = b2[x];
                     }
                 }
-#pragma unroll
+    #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int q0 = 64 * g + 32 * c;
-#pragma unroll
+                    const uint32_t* dr = drr + 32 * c;
+                    uint32_t dk[16];
+    #pragma unroll
                     for (int x4 = 0; x4 < 8; ++x4) {
-                        const float4 Lq = L4[x4];
-                        if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(lb + q0 + 32 + 4 * x4);
-                        float e[4];
-                        fma_f32x2(e[0], e[1], __uint_as_float(sr[32 * c + 4 * x4]),
-                                  __uint_as_float(sr[32 * c + 4 * x4 + 1]), sl2, sl2, -Lq.x, -Lq.y);
-                        fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
-                                  __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -Lq.z, -Lq.w);
-                        float pr[4];
-#pragma unroll
-                        for (int y = 0; y < 4; ++y) {
-                            pr[y] = ex2_approx(e[y]);
-                            if (!full) {
-                                const int i = i0 + q0 + 4 * x4 + y;
-                                if (j > i || i - j >= p.W) pr[y] = 0.f;
-                            }
-                        }
-                        pp[16 * c + 2 * x4] = pack_bf16x2(pr[0], pr[1]);
-                        pp[16 * c + 2 * x4 + 1] = pack_bf16x2(pr[2], pr[3]);
+                        const float4 Dq = L4[x4];
+                        if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(db + q0 + 32 + 4 * x4);
+                        const uint32_t w0 = pp[16 * c + 2 * x4], w1 = pp[16 * c + 2 * x4 + 1];
+                        float t[4], ds[4];
+                        add_f32x2(t[0], t[1], __uint_as_float(dr[4 * x4]), __uint_as_float(dr[4 * x4 + 1]), -Dq.x, -Dq.y);
+                        add_f32x2(t[2], t[3], __uint_as_float(dr[4 * x4 + 2]), __uint_as_float(dr[4 * x4 + 3]), -Dq.z,
+                                  -Dq.w);
+                        mul_f32x2(ds[0], ds[1], __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), t[0], t[1]);
+                        mul_f32x2(ds[2], ds[3], __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u), t[2], t[3]);
+                        dk[2 * x4] = pack_bf16x2(ds[0], ds[1]);
+                        dk[2 * x4 + 1] = pack_bf16x2(ds[2], ds[3]);
                     }
-                    // packed into the first half of this warpgroup's own (already read) columns
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) pk[x] = pp[16 * c + x];
-                    tmem_st16(st_addr + 64 * g + 16 * c, pk);
+                    // dS^T (bf16) over this warpgroup's already-read DPT columns, for dK
+                    tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
+                    // dS row into the [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int unit = 4 * c + u;
+                        uint4 v;
+                        v.x = dk[4 * u + 0];
+                        v.y = dk[4 * u + 1];
+                        v.z = dk[4 * u + 2];
+                        v.w = dk[4 * u + 3];
+                        *reinterpret_cast<uint4*>(ds_row + ((unit ^ (tid & 7)) << 4)) = v;
+                    }
                 }
+                tmem_wait_st();
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars->ds_full);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full);
-            // phase 2: dS^T = P^T (dP^T - Delta), packed into DPT (A operand of dK) and into the
-            // shared-memory tile [key][query] (MN-major operand of dQ)
-#pragma unroll
-            for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(db + 64 * g + 4 * x4);
-            ok = mbar_wait_warp(&bars->dp_full, it & 1) && !aborted(bars);
-            if (!ok) continue;
-            tc_fence_after();
-            uint32_t drr[64];
+            // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV.  The next
+            // item's first dV / dK products overwrite these accumulators only after this
+            // warpgroup's next P^T / dS^T arrivals, which come after the reads below.
+            if (ok) ok = mbar_wait_warp(&bars->final_, ii & 1) && !aborted(bars);
+            if (!named_bar_and(1 + g, 128, ok)) {  // leave together
+                ok = false;
+                record_timeout(bars, p.err);
+                break;
+            }
             {
-                uint32_t a[32], b2[32];
-                tmem_ld32x2(dpt_addr + 64 * g, dpt_addr + 64 * g + 32, a, b2);  // one wait for both chunks
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    drr[x] = a[x];
-                    drr[32 + x] = b2[x];
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int q0 = 64 * g + 32 * c;
-                const uint32_t* dr = drr + 32 * c;
-                uint32_t dk[16];
-#pragma unroll
-                for (int x4 = 0; x4 < 8; ++x4) {
-                    const float4 Dq = L4[x4];
-                    if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(db + q0 + 32 + 4 * x4);
-                    const uint32_t w0 = pp[16 * c + 2 * x4], w1 = pp[16 * c + 2 * x4 + 1];
-                    float t[4], ds[4];
-                    add_f32x2(t[0], t[1], __uint_as_float(dr[4 * x4]), __uint_as_float(dr[4 * x4 + 1]), -Dq.x, -Dq.y);
-                    add_f32x2(t[2], t[3], __uint_as_float(dr[4 * x4 + 2]), __uint_as_float(dr[4 * x4 + 3]), -Dq.z,
-                              -Dq.w);
-                    mul_f32x2(ds[0], ds[1], __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u), t[0], t[1]);
-                    mul_f32x2(ds[2], ds[3], __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u), t[2], t[3]);
-                    dk[2 * x4] = pack_bf16x2(ds[0], ds[1]);
-                    dk[2 * x4 + 1] = pack_bf16x2(ds[2], ds[3]);
-                }
-                // dS^T (bf16) over this warpgroup's already-read DPT columns, for dK
-                tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
-                // dS row into the [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int unit = 4 * c + u;
-                    uint4 v;
-                    v.x = dk[4 * u + 0];
-                    v.y = dk[4 * u + 1];
-                    v.z = dk[4 * u + 2];
-                    v.w = dk[4 * u + 3];
-                    *reinterpret_cast<uint4*>(ds_row + ((unit ^ (tid & 7)) << 4)) = v;
-                }
-            }
-            tmem_wait_st();
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars->ds_full);
-        }
-        // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV
-        if (ok) ok = mbar_wait_warp(&bars->final_, 0) && !aborted(bars);
-        if (!ok) {
-            record_timeout(bars, p.err);
-        } else {
-            tc_fence_after();
-            const bool in_range = j < p.T;
-            const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.H + h) * D;
-            const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
-            const float mul = g ? 1.f : p.scale;
-            __nv_bfloat16* dst = (g ? p.dv : p.dk) + off;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(a + c * 32, r);
-                if (in_range) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 pkt;
-                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
-                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
-                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
-                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
-                        reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
+                tc_fence_after();
+                const bool in_range = j < p.T;
+                const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.H + h) * D;
+                const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
+                const float mul = g ? 1.f : p.scale;
+                __nv_bfloat16* dst = (g ? p.dv : p.dk) + off;
+    #pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(a + c * 32, r);
+                    if (in_range) {
+    #pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 pkt;
+                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+                            reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
+                        }
                     }
                 }
             }
@@ -517,62 +633,74 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
         const size_t row_stride = static_cast<size_t>(p.H) * D;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int i0 = (m_lo + it) * kBQ;
-            const bool got = mbar_wait_warp(&bars->dq_full, it & 1) && !aborted(bars);
-            if (!named_bar_and(3, 128, got)) {  // leave together
+        int gi = 0;  // query blocks processed over all items
+        for (int ii = 0; ok; ++ii) {
+            const int w = read_item(bars, ii);
+            if (!named_bar_and(3, 128, w != -2)) {  // leave together
                 record_timeout(bars, p.err);
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            if constexpr (L::kTmaReduce) {
-                // thread = dQ column d, TMEM columns = the block's 128 query rows.  The whole
-                // block is read into registers first, so the TMEM columns go back to the MMA
-                // warp (for the next dP^T) before any of the staging work.  Each half (64 rows)
-                // then goes to the fp32 staging tile [row][d] and is added to the accumulator by
-                // one TMA reduce-add, which keeps the SM's load/store path free.
-                float* stage = reinterpret_cast<float*>(smem + L::kStage);
-                uint32_t r0[64], r1[64];
-                tmem_ld64_nowait(st_addr, r0);
-                tmem_ld64_nowait(st_addr + 64, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bars->dq_empty);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    if (tid == 0) bulk_wait_read();  // the previous reduce-add has read the staging tile
-                    named_bar_sync(3, 128);
-#pragma unroll
-                    for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(half ? r1[x] : r0[x]);
-                    fence_async_smem();
-                    named_bar_sync(3, 128);
-                    if (tid == 0) {
-                        tma_reduce_add_4d(&tm_dq, stage, 0, h, i0 + 64 * half, b);
-                        bulk_commit();
-                    }
+            if (w < 0) break;
+            const BwdItem item = bwd_item(w, p);
+            const int h = item.h, b = item.b;
+            for (int it = 0; it < item.n_it; ++it, ++gi) {
+                const int i0 = (item.m_lo + it) * kBQ;
+                const bool got = mbar_wait_warp(&bars->dq_full, gi & 1) && !aborted(bars);
+                if (!named_bar_and(3, 128, got)) {  // leave together
+                    record_timeout(bars, p.err);
+                    ok = false;
+                    break;
                 }
-            } else {
-                // thread = query row, TMEM columns = the D dQ columns
-                const int i = i0 + tid;
-                float* dst = p.dq_acc + (static_cast<size_t>(b) * p.T + i) * row_stride + static_cast<size_t>(h) * D;
-                uint32_t r[64];
-                {
-                    uint32_t a[32], c2[32];
-                    tmem_ld32x2(st_addr, st_addr + 32, a, c2);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        r[x] = a[x];
-                        r[32 + x] = c2[x];
+                tc_fence_after();
+                if constexpr (L::kTmaReduce) {
+                    // thread = dQ column d, TMEM columns = the block's 128 query rows.  The whole
+                    // block is read into registers first, so the TMEM columns go back to the MMA
+                    // warp (for the next dP^T) before any of the staging work.  Each half (64 rows)
+                    // then goes to the fp32 staging tile [row][d] and is added to the accumulator by
+                    // one TMA reduce-add, which keeps the SM's load/store path free.
+                    float* stage = reinterpret_cast<float*>(smem + L::kStage);
+                    uint32_t r0[64], r1[64];
+                    tmem_ld64_nowait(st_addr, r0);
+                    tmem_ld64_nowait(st_addr + 64, r1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&bars->dq_empty);
+    #pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        if (tid == 0) bulk_wait_read();  // the previous reduce-add has read the staging tile
+                        named_bar_sync(3, 128);
+    #pragma unroll
+                        for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(half ? r1[x] : r0[x]);
+                        fence_async_smem();
+                        named_bar_sync(3, 128);
+                        if (tid == 0) {
+                            tma_reduce_add_4d(&tm_dq, stage, 0, h, i0 + 64 * half, b);
+                            bulk_commit();
+                        }
                     }
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->dq_empty);
-                if (i < p.T) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 16; ++v4)
-                        red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                                      __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+                } else {
+                    // thread = query row, TMEM columns = the D dQ columns
+                    const int i = i0 + tid;
+                    float* dst = p.dq_acc + (static_cast<size_t>(b) * p.T + i) * row_stride + static_cast<size_t>(h) * D;
+                    uint32_t r[64];
+                    {
+                        uint32_t a[32], c2[32];
+                        tmem_ld32x2(st_addr, st_addr + 32, a, c2);
+    #pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            r[x] = a[x];
+                            r[32 + x] = c2[x];
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&bars->dq_empty);
+                    if (i < p.T) {
+    #pragma unroll
+                        for (int v4 = 0; v4 < 16; ++v4)
+                            red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                                          __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+                    }
                 }
             }
         }
@@ -593,14 +721,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
-                                                      float* __restrict__ delta, float* __restrict__ dq_acc, int B,
-                                                      int T, int H) {
+                                                      float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                      int* __restrict__ work, int B, int T, int H) {
     constexpr int G = D / 8;          // lanes per row
     constexpr int RPW = 32 / G;       // rows per warp
     const long tid_g = (long)blockIdx.x * blockDim.x + threadIdx.x;
     const long row = (tid_g >> 5) * RPW + ((threadIdx.x & 31) / G);
     const int c = threadIdx.x % G;
     const long rows = (long)B * T * H;
+    if (tid_g == 0) *work = 0;  // the main kernel's work-item counter
     float acc = 0.f;
     if (row < rows) {
         const uint4 a = reinterpret_cast<const uint4*>(o + (size_t)row * D)[c];
@@ -644,7 +773,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
 template <int D>
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
-                          float scale, float* dq_acc, float* delta, int* err, cudaStream_t st) {
+                          float scale, float* dq_acc, float* delta, int* work, int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
@@ -653,7 +782,7 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     const long rows = (long)B * T * H;
     const long pre_threads = ((rows * (D / 8) + 31) / 32) * 32;
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta, dq_acc, B, T, H);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta, dq_acc, work, B, T, H);
     BwdParams p;
     p.lse = lse;
     p.delta = delta;
@@ -668,6 +797,7 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     p.scale_log2 = scale * kLog2e;
     p.n_kb = (T + kBK - 1) / kBK;
     p.n_qb = (T + kBQ - 1) / kBQ;
+    p.work = work;
     p.err = err;
     const int smem = BwdSmem<D>::kBytes;
     static bool attr_set[64] = {false};
@@ -679,7 +809,18 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
-    dim3 grid(p.n_kb, H, B);
+    // persistent: one CTA per SM (its shared memory and TMEM allow one), looping over the items
+    static int sms[64] = {0};
+    if (dev < 64 && sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const long n_items = (long)p.n_kb * H * B;
+    const int n_sm = dev < 64 ? sms[dev] : 148;
+    const int grid = (int)(n_items < n_sm ? n_items : n_sm);
+    // a scheduling group holds about one wave of items
+    p.group = (n_sm + p.n_kb - 1) / p.n_kb;
+    if (p.group > B * H) p.group = B * H;
     bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
     const size_t n8 = (size_t)rows * D / 8;
     bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
@@ -692,11 +833,11 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
 
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
-                       float* dq_acc, float* delta, int* err, cudaStream_t st) {
-    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, err,
-                                         st)
-                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, err,
-                                        st);
+                       float* dq_acc, float* delta, int* work, int* err, cudaStream_t st) {
+    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
+                                         err, st)
+                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
+                                        err, st);
 }
 
 }  // namespace nc

@@ -27,6 +27,7 @@
 #include "nc_attn.h"
 #include "nc_kernels.h"
 #include "nc_ptx.cuh"
+#include "nc_sched.cuh"
 #include "nc_tma.h"
 
 namespace nc {
@@ -98,7 +99,7 @@ struct FwdItem {
 };
 
 // Items are numbered heaviest first (query-tile pair descending, then (h, b)), so the
-// static round-robin over persistent CTAs hands out the long causal tiles first.
+// static zigzag assignment over persistent CTAs (nc_sched.cuh) hands out the long causal tiles first.
 __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     FwdItem it;
     const int bh = w % (p.B * p.H);
@@ -117,22 +118,6 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     it.kb_lo = it.lo[0];
     it.kb_hi = it.active1 ? it.hi[1] : it.hi[0];
     return it;
-}
-
-// Work item ii of this CTA.  Round ii hands out items ii*G .. ii*G+G-1 (G = gridDim.x),
-// CTA c taking slot c on even rounds and slot G-1-c on odd ones: with items sorted heaviest
-// first, this zigzag evens out the total work per CTA far better than plain round-robin.
-__device__ __forceinline__ int fwd_item_index(int ii) {
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    return ii * G + ((ii & 1) ? G - 1 - c : c);
-}
-
-// Number of items of this CTA: every full round, plus the last partial round if its slot is in it.
-__device__ __forceinline__ int fwd_items_of_cta(int n_items) {
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const int full = n_items / G, rem = n_items % G;
-    const int slot = (full & 1) ? G - 1 - c : c;
-    return full + (slot < rem ? 1 : 0);
 }
 
 template <int D>
@@ -180,7 +165,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
         regs_decrease<72>();
-        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -191,7 +176,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int q_loads = 0;
         bool ok = true;
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem it = fwd_item(fwd_item_index(ii), p);
+            const FwdItem it = fwd_item(sched_item_index(ii), p);
             // Q of this item once the previous item's S products have read theirs
             if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
                 ok = false;
@@ -228,7 +213,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
         regs_decrease<72>();
-        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
         {
             constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
@@ -264,7 +249,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int seq = 0;                 // K/V ring position over all items
             int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
             for (int ii = 0; ok && ii < my_items; ++ii) {
-                const FwdItem it = fwd_item(fwd_item_index(ii), p);
+                const FwdItem it = fwd_item(sched_item_index(ii), p);
                 auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
                 ok = mbar_wait_warp(&bars.q_full, ii & 1);
                 if (!ok) break;
@@ -332,7 +317,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         regs_increase<216>();
-        const int my_items = fwd_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
@@ -344,7 +329,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         int n_s = 0;  // S tiles of this query tile consumed over all items
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem item = fwd_item(fwd_item_index(ii), p);
+            const FwdItem item = fwd_item(sched_item_index(ii), p);
             const int tr0 = t ? item.r0[1] : item.r0[0];
             const int t_lo = t ? item.lo[1] : item.lo[0];
             const int t_hi = t ? item.hi[1] : item.hi[0];

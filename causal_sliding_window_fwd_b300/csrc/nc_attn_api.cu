@@ -87,7 +87,7 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 
 size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D) {
     if (B <= 0 || T <= 0 || H <= 0 || D <= 0) return 0;
-    return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256);
+    return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256) + 256;
 }
 
 nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
@@ -119,8 +119,10 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
     float* dq_acc = reinterpret_cast<float*>(ws);
     ws += round_up((size_t)B * T * H * D * 4, 256);
     float* delta = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)B * H * T * 4, 256);
+    int* work = reinterpret_cast<int*>(ws);
     const cudaError_t e = nc::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc, delta,
-                                         err, stream);
+                                         work, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

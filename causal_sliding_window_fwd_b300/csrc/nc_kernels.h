@@ -15,9 +15,9 @@ int* device_error_word();
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);
 
-// Backward: dq_acc fp32 [B,T,H,D] and delta fp32 [B,H,T] are workspace.
+// Backward: dq_acc fp32 [B,T,H,D], delta fp32 [B,H,T] and the work-item counter are workspace.
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
-                       float* dq_acc, float* delta, int* err, cudaStream_t st);
+                       float* dq_acc, float* delta, int* work, int* err, cudaStream_t st);
 
 }  // namespace nc

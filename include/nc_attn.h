@@ -81,7 +81,8 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       int B, int T, int H, int D, int window, float scale, cudaStream_t stream);
 
 /* Bytes of device workspace nc_attn_bwd needs: an fp32 dQ accumulator
- * [B, T, H, D] plus the fp32 row term Delta = rowsum(dO * O) [B, H, T]. */
+ * [B, T, H, D], the fp32 row term Delta = rowsum(dO * O) [B, H, T] and a
+ * work-item counter for the main kernel's scheduler. */
 size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D);
 
 /*
