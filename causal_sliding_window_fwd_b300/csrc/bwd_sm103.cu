@@ -90,6 +90,8 @@ struct BwdBarriers {
     uint64_t dq_empty;
     uint64_t final_;
     uint64_t drain;
+    uint64_t epi_done;    // dK / dV epilogue tiles in the dS region have been read by their TMA stores
+    uint64_t stage_free;  // the last dQ reduce-add of an item has read the staging tile (D = 128)
     uint64_t item_full[kItemSlots];
     uint64_t item_empty[kItemSlots];
     int item[kItemSlots];
@@ -187,7 +189,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
     using L = BwdSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + L::kBars);
@@ -220,6 +223,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bars->dq_empty, kBQ);
         mbar_init(&bars->final_, 1);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->epi_done, L::kTmaReduce ? 1 : 2);
+        mbar_init(&bars->stage_free, 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&bars->item_full[s], 1);
             mbar_init(&bars->item_empty[s], kItemReaders);
@@ -483,7 +488,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // The row statistics of the first 32 queries are read before the wait so that their
                 // shared-memory latency hides behind it; the second 32 are read while the first are used.
                 float4 L4[8];
-    #pragma unroll
+#pragma unroll
                 for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(lb + 64 * g + 4 * x4);
                 ok = mbar_wait_warp(&bars->s_full, gi & 1) && !aborted(bars);
                 if (!ok) continue;
@@ -496,16 +501,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     {
                         uint32_t a[32], b2[32];
                         tmem_ld32x2(st_addr + 64 * g, st_addr + 64 * g + 32, a, b2);  // one wait for both chunks
-    #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 32; ++x) {
                             sr[x] = a[x];
                             sr[32 + x] = b2[x];
                         }
                     }
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const int q0 = 64 * g + 32 * c;
-    #pragma unroll
+#pragma unroll
                         for (int x4 = 0; x4 < 8; ++x4) {
                             const float4 Lq = L4[x4];
                             if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(lb + q0 + 32 + 4 * x4);
@@ -515,7 +520,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             fma_f32x2(e[2], e[3], __uint_as_float(sr[32 * c + 4 * x4 + 2]),
                                       __uint_as_float(sr[32 * c + 4 * x4 + 3]), sl2, sl2, -Lq.z, -Lq.w);
                             float pr[4];
-    #pragma unroll
+#pragma unroll
                             for (int y = 0; y < 4; ++y) {
                                 pr[y] = ex2_approx(e[y]);
                                 if (!full) {
@@ -528,7 +533,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                         // packed into the first half of this warpgroup's own (already read) columns
                         uint32_t pk[16];
-    #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 16; ++x) pk[x] = pp[16 * c + x];
                         tmem_st16(st_addr + 64 * g + 16 * c, pk);
                     }
@@ -538,27 +543,30 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive(&bars->p_full);
                 // phase 2: dS^T = P^T (dP^T - Delta), packed into DPT (A operand of dK) and into the
                 // shared-memory tile [key][query] (MN-major operand of dQ)
-    #pragma unroll
+#pragma unroll
                 for (int x4 = 0; x4 < 8; ++x4) L4[x4] = *reinterpret_cast<const float4*>(db + 64 * g + 4 * x4);
                 ok = mbar_wait_warp(&bars->dp_full, gi & 1) && !aborted(bars);
+                // the first dS of an item goes where the previous item's dK (and for D = 64 dV)
+                // tile was staged: wait until those TMA stores have read it
+                if (ok && it == 0 && ii > 0) ok = mbar_wait_warp(&bars->epi_done, (ii - 1) & 1) && !aborted(bars);
                 if (!ok) continue;
                 tc_fence_after();
                 uint32_t drr[64];
                 {
                     uint32_t a[32], b2[32];
                     tmem_ld32x2(dpt_addr + 64 * g, dpt_addr + 64 * g + 32, a, b2);  // one wait for both chunks
-    #pragma unroll
+#pragma unroll
                     for (int x = 0; x < 32; ++x) {
                         drr[x] = a[x];
                         drr[32 + x] = b2[x];
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int q0 = 64 * g + 32 * c;
                     const uint32_t* dr = drr + 32 * c;
                     uint32_t dk[16];
-    #pragma unroll
+#pragma unroll
                     for (int x4 = 0; x4 < 8; ++x4) {
                         const float4 Dq = L4[x4];
                         if (c == 0) L4[x4] = *reinterpret_cast<const float4*>(db + q0 + 32 + 4 * x4);
@@ -575,7 +583,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // dS^T (bf16) over this warpgroup's already-read DPT columns, for dK
                     tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
                     // dS row into the [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int unit = 4 * c + u;
                         uint4 v;
@@ -591,10 +599,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_before();
                 mbar_arrive(&bars->ds_full);
             }
-            // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV.  The next
-            // item's first dV / dK products overwrite these accumulators only after this
+            // epilogue: warpgroup 0 writes dK = scale * DK, warpgroup 1 writes dV = DV, each as a
+            // 128 x D bf16 tile in shared memory (the 128-byte swizzled layout of the TMA maps)
+            // sent out by TMA stores, so the global writes leave as whole lines.  The next
+            // item's first dV / dK products overwrite the accumulators only after this
             // warpgroup's next P^T / dS^T arrivals, which come after the reads below.
             if (ok) ok = mbar_wait_warp(&bars->final_, ii & 1) && !aborted(bars);
+            // warpgroup 0 uses the dS tile (free once final_ has landed: dQ and dK were its last
+            // readers); for D = 128 warpgroup 1 uses the dQ staging tile once the last reduce-add
+            // of this item has read it, for D = 64 the second half of the dS tile
+            if (g == 1 && L::kTmaReduce && ok) ok = mbar_wait_warp(&bars->stage_free, ii & 1) && !aborted(bars);
             if (!named_bar_and(1 + g, 128, ok)) {  // leave together
                 ok = false;
                 record_timeout(bars, p.err);
@@ -602,26 +616,34 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             {
                 tc_fence_after();
-                const bool in_range = j < p.T;
-                const size_t off = ((static_cast<size_t>(b) * p.T + j) * p.H + h) * D;
                 const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
                 const float mul = g ? 1.f : p.scale;
-                __nv_bfloat16* dst = (g ? p.dv : p.dk) + off;
-    #pragma unroll
+                uint8_t* tile = g == 0 ? smem + L::kDS : (L::kTmaReduce ? smem + L::kStage : smem + L::kDS + kBK * 128);
+#pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(a + c * 32, r);
-                    if (in_range) {
-    #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
-                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
-                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
-                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
-                            reinterpret_cast<uint4*>(dst + c * 32)[v4] = pkt;
-                        }
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 pkt;
+                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+                        // columns 32c + 8 v4 .. +7: 16-byte unit 4 (c % 2) + v4 of the row's 64-column chunk c / 2
+                        const int unit = 4 * (c % 2) + v4;
+                        *reinterpret_cast<uint4*>(tile + (c / 2) * (kBK * 128) + tid * 128 + ((unit ^ (tid & 7)) << 4)) = pkt;
                     }
+                }
+                fence_async_smem();
+                named_bar_sync(1 + g, 128);
+                if (tid == 0) {
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_store_4d(g ? &tm_dv : &tm_dk, tile + c * (kBK * 128), c * 64, h, j0, b);
+                    bulk_commit();
+                    bulk_wait_read();
+                    // the dS tile may be written again (the next item's first dS) once this is set
+                    if (g == 0 || !L::kTmaReduce) mbar_arrive(&bars->epi_done);
                 }
             }
         }
@@ -666,11 +688,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(&bars->dq_empty);
-    #pragma unroll
+#pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         if (tid == 0) bulk_wait_read();  // the previous reduce-add has read the staging tile
                         named_bar_sync(3, 128);
-    #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 64; ++x) stage[x * D + tid] = __uint_as_float(half ? r1[x] : r0[x]);
                         fence_async_smem();
                         named_bar_sync(3, 128);
@@ -678,6 +700,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             tma_reduce_add_4d(&tm_dq, stage, 0, h, i0 + 64 * half, b);
                             bulk_commit();
                         }
+                    }
+                    if (it + 1 == item.n_it && tid == 0) {
+                        // the dV epilogue of this item reuses the staging tile
+                        bulk_wait_read();
+                        mbar_arrive(&bars->stage_free);
                     }
                 } else {
                     // thread = query row, TMEM columns = the D dQ columns
@@ -687,7 +714,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     {
                         uint32_t a[32], c2[32];
                         tmem_ld32x2(st_addr, st_addr + 32, a, c2);
-    #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 32; ++x) {
                             r[x] = a[x];
                             r[32 + x] = c2[x];
@@ -696,7 +723,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_before();
                     mbar_arrive(&bars->dq_empty);
                     if (i < p.T) {
-    #pragma unroll
+#pragma unroll
                         for (int v4 = 0; v4 < 16; ++v4)
                             red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
                                           __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
@@ -708,6 +735,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (tid == 0) bulk_wait_all();  // every reduce-add has landed before the CTA exits
         }
     }
+    if (warp >= 4 && warp < 12 && (threadIdx.x & 127) == 0) bulk_wait_all();  // epilogue stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -774,9 +802,10 @@ template <int D>
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
                           float scale, float* dq_acc, float* delta, int* work, int* err, cudaStream_t st) {
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
+        !make_tmap_bthd(&tdk, dk, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdv, dv, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, D, BwdSmem<D>::kStageRows))
         return cudaErrorInvalidValue;
     const long rows = (long)B * T * H;
@@ -821,7 +850,7 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_kb - 1) / p.n_kb;
     if (p.group > B * H) p.group = B * H;
-    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     const size_t n8 = (size_t)rows * D / 8;
     bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
                                                                  scale);
