@@ -174,6 +174,9 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
             }
         }
     }
+    // this CTA's partials are written: once every CTA is here the combine kernel may be scheduled
+    // (it still waits for this grid's completion before reading them)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One warp per (sequence, head): merge the partials of the splits that saw rows.
@@ -185,6 +188,8 @@ decode_combine_kernel(const float* __restrict__ part_ml, const float* __restrict
     constexpr int E = D / 32;  // elements per lane
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    // launched as a programmatic dependent of the split kernel: wait for its partials
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (gw >= N * H) return;
     const int n = gw / H, h = gw % H;
     const int L = lens[n];
@@ -242,6 +247,23 @@ decode_combine_kernel(const float* __restrict__ part_ml, const float* __restrict
 
 }  // namespace
 
+// Launch the combine as a programmatic dependent of the split kernel on the same stream, so its
+// launch overlaps the split kernel's tail (it waits for the split results on the device).
+template <typename... KArgs, typename... Args>
+static void launch_combine(void (*kern)(KArgs...), int blocks, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int decode_chunk_rows(int D) { return D == 64 ? 128 : 64; }
 
 int decode_max_splits(int Tmax, int D) {
@@ -266,14 +288,14 @@ cudaError_t launch_decode(const void* q, const void* kcache, const void* vcache,
         decode_split_kernel<128><<<grid, threads, 0, stream>>>(
             (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
             part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
-        decode_combine_kernel<128><<<cblocks, 256, 0, stream>>>(part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
-                                                                Tmax, H, window, n_splits, chunk, err);
+        launch_combine(decode_combine_kernel<128>, cblocks, stream, part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
+                       Tmax, H, window, n_splits, chunk, err);
     } else {
         decode_split_kernel<64><<<grid, threads, 0, stream>>>(
             (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
             part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
-        decode_combine_kernel<64><<<cblocks, 256, 0, stream>>>(part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
-                                                               Tmax, H, window, n_splits, chunk, err);
+        launch_combine(decode_combine_kernel<64>, cblocks, stream, part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
+                       Tmax, H, window, n_splits, chunk, err);
     }
     count_launches(2);
     return cudaGetLastError();
