@@ -39,6 +39,7 @@
 #include "nc_attn.h"
 #include "nc_kernels.h"
 #include "nc_ptx.cuh"
+#include "nc_sched.cuh"
 #include "nc_tma.h"
 
 namespace nc {
@@ -48,7 +49,6 @@ constexpr int kBK = 128;       // keys per CTA
 constexpr int kBQ = 128;       // queries per block
 constexpr int kQStages = 2;
 constexpr int kThreads = 512;
-constexpr int kItemSlots = 2;   // work-item ring between the producer and the other roles
 // warps that read each work-item slot: the MMA warp, the 8 P/dS warps and the 4 dQ warps
 constexpr int kItemReaders = 13;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -145,30 +145,12 @@ __device__ __forceinline__ bool aborted(const BwdBarriers* bars) {
     return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
 }
 
-// Producer warp (converged): take the next item index from the global counter and publish it
-// in ring slot k % kItemSlots; -1 once every item is taken.  Returns what it published, or -2
-// if the wait for the slot ran out.
 __device__ __forceinline__ int publish_item(BwdBarriers* bars, int k, int n_items, int* work) {
-    const int slot = k % kItemSlots;
-    if (!mbar_wait_warp(&bars->item_empty[slot], ((k / kItemSlots) & 1) ^ 1)) return -2;
-    int w = 0;
-    if (lane_id() == 0) {
-        w = atomicAdd(work, 1);
-        if (w >= n_items) w = -1;
-        bars->item[slot] = w;
-        mbar_arrive(&bars->item_full[slot]);  // release: the index is visible to whoever sees the phase
-    }
-    return __shfl_sync(0xffffffffu, w, 0);
+    return ring_publish_item(bars->item_full, bars->item_empty, bars->item, k, n_items, work);
 }
 
-// Any other warp (converged): the index in ring slot k % kItemSlots, or -2 if the wait ran out.
 __device__ __forceinline__ int read_item(BwdBarriers* bars, int k) {
-    const int slot = k % kItemSlots;
-    if (!mbar_wait_warp(&bars->item_full[slot], (k / kItemSlots) & 1)) return -2;
-    const int w = *reinterpret_cast<volatile const int*>(&bars->item[slot]);
-    __syncwarp();
-    if (lane_id() == 0) mbar_arrive(&bars->item_empty[slot]);
-    return w;
+    return ring_read_item(bars->item_full, bars->item_empty, bars->item, k);
 }
 
 __device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
