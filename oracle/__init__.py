@@ -50,6 +50,9 @@ class OracleLib:
         lib.oracle_decode.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_int), dp, dp,
                                       L, L, L, L, L, ctypes.c_double]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_prefill.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_int), dp, dp,
+                                       L, L, L, L, L, L, ctypes.c_double]
+        lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -85,6 +88,21 @@ class OracleLib:
         rc = self.lib.oracle_decode(_ptr(q), _ptr(kc), _ptr(vc),
                                     lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
                                     _ptr(o), _ptr(lse), N, Tmax, H, D, int(window), float(scale))
+        return o, lse, rc == 0
+
+    def prefill(self, q, kcache, vcache, cache_lens, window: int, scale: float):
+        q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+        if hasattr(cache_lens, "detach"):
+            cache_lens = cache_lens.detach().to("cpu").numpy()
+        lens = np.ascontiguousarray(cache_lens, dtype=np.int32)
+        N, Tq, H, D = q.shape
+        Tmax = kc.shape[1]
+        assert kc.shape == (N, Tmax, H, D) and vc.shape == kc.shape and lens.shape == (N,)
+        o = np.empty_like(q)
+        lse = np.empty((N, H, Tq), dtype=np.float64)
+        rc = self.lib.oracle_prefill(_ptr(q), _ptr(kc), _ptr(vc),
+                                     lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                     _ptr(o), _ptr(lse), N, Tq, Tmax, H, D, int(window), float(scale))
         return o, lse, rc == 0
 
 
@@ -124,6 +142,16 @@ def fwd(q, k, v, window: int, scale: float):
 def bwd(q, k, v, dO, window: int, scale: float):
     """Exact gradients of sum(O * dO) w.r.t. q, k, v.  Returns (dq, dk, dv), each [B, T, H, D]."""
     return _load().bwd(q, k, v, dO, window, scale)
+
+
+def prefill(q, kcache, vcache, cache_lens, window: int, scale: float):
+    """Prefill (append) over a KV cache.  q [N,Tq,H,D]; caches [N,Tmax,H,D]; cache_lens [N] (int),
+    each counting the Tq new tokens, whose keys/values are already in the cache.
+
+    Returns (o [N,Tq,H,D], lse [N,H,Tq], ok).  ok is False when some length is outside
+    [Tq, Tmax]; that sequence's rows are NaN.
+    """
+    return _load().prefill(q, kcache, vcache, cache_lens, window, scale)
 
 
 def decode(q, kcache, vcache, cache_lens, window: int, scale: float):

@@ -16,7 +16,8 @@
  *   - "nanochat" walkthrough (page 4, inference paragraph closing the
  *     pretraining section; page 1 launch post): inference uses an Engine with
  *     a KV cache and a prefill/decode split, so decode is one query token
- *     attending over the cached keys/values.
+ *     attending over the cached keys/values, and prefill is a run of new
+ *     query tokens appended after the cached ones.
  *
  * Readings where the pages are silent (each one is restated in the design
  * notes of the repository):
@@ -28,7 +29,9 @@
  *     of the *scaled* scores;
  *   - decode: the query of sequence n is position L_n - 1 whose key/value
  *     already sit in the cache; cache rows max(0, L_n - W) .. L_n - 1 are
- *     visible.
+ *     visible;
+ *   - prefill: the same cache layout; the last Tq of a sequence's L_n rows are
+ *     the new tokens, and new token t is the query at position L_n - Tq + t.
  *
  * Everything is computed from the definition in double precision with plain
  * loops: no tiling, no online softmax, no reordering beyond the sums as
@@ -209,6 +212,61 @@ int oracle_decode(const double* q, const double* kc, const double* vc, const int
             }
             free(p);
         }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Prefill (append) over a KV cache: sequence n holds L_n = lens[n] cache rows, the last Tq of
+ * which are the new tokens, whose keys and values are already in the cache.  New token t
+ * (0 <= t < Tq) is the query at position i = L_n - Tq + t; it sees cache rows
+ * max(0, i - W + 1) .. i (all rows up to i for W <= 0).  With Tq = 1 this is oracle_decode.
+ * q [N,Tq,H,D]; caches [N,Tmax,H,D]; o [N,Tq,H,D]; lse [N,H,Tq].  A length outside [Tq, Tmax]
+ * gives NaN rows for that sequence, and the call returns -1. */
+int oracle_prefill(const double* q, const double* kc, const double* vc, const int* lens,
+                   double* o, double* lse, long N, long Tq, long Tmax, long H, long D, long window,
+                   double scale) {
+    int bad = 0;
+    for (long n = 0; n < N; ++n)
+        if (lens[n] < Tq || lens[n] > Tmax) bad = 1;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)Tmax);
+#pragma omp for schedule(dynamic, 1) collapse(2)
+        for (long n = 0; n < N; ++n)
+            for (long h = 0; h < H; ++h) {
+                long L = lens[n];
+                for (long t = 0; t < Tq; ++t) {
+                    double* orow = o + ((size_t)(n * Tq + t) * H + h) * D;
+                    double* lrow = lse + ((size_t)n * H + h) * Tq + t;
+                    if (L < Tq || L > Tmax) {
+                        *lrow = NAN;
+                        for (long d = 0; d < D; ++d) orow[d] = NAN;
+                        continue;
+                    }
+                    long i = L - Tq + t;
+                    long lo = (window <= 0 || i - window + 1 < 0) ? 0 : i - window + 1;
+                    const double* qrow = q + ((size_t)(n * Tq + t) * H + h) * D;
+                    double M = -INFINITY;
+                    for (long j = lo; j <= i; ++j) {
+                        double s = 0.0;
+                        for (long d = 0; d < D; ++d) s += qrow[d] * kc[idx_bthd(n, j, h, d, Tmax, H, D)];
+                        s *= scale;
+                        p[j - lo] = s;
+                        if (s > M) M = s;
+                    }
+                    double sum = 0.0;
+                    for (long j = lo; j <= i; ++j) sum += exp(p[j - lo] - M);
+                    double l = M + log(sum);
+                    *lrow = l;
+                    for (long j = lo; j <= i; ++j) p[j - lo] = exp(p[j - lo] - l);
+                    for (long d = 0; d < D; ++d) {
+                        double acc = 0.0;
+                        for (long j = lo; j <= i; ++j) acc += p[j - lo] * vc[idx_bthd(n, j, h, d, Tmax, H, D)];
+                        orow[d] = acc;
+                    }
+                }
+            }
+        free(p);
     }
     return bad ? -1 : 0;
 }

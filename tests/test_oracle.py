@@ -297,3 +297,116 @@ def test_backward_matches_finite_differences(oracle_mod, window):
             lm = (oracle_mod.fwd(*minus, window, scale)[0] * G).sum()
             fd = (lp - lm) / (2 * eps)
             assert abs(fd - grads[which][idx]) < 1e-7, (which, idx, fd, grads[which][idx])
+
+
+# ---------------------------------------------------------------- prefill over a KV cache
+
+
+@pytest.mark.parametrize("window", [1, 4, 9, -1])
+def test_prefill_rows_equal_forward_rows(oracle_mod, window):
+    """Appending Tq tokens to a cache equals the last Tq rows of the forward over the whole sequence."""
+    N, Tq, Tmax, H, D = 3, 5, 24, 2, 8
+    kc, vc = _rand((N, Tmax, H, D), 300), _rand((N, Tmax, H, D), 301)
+    qs = _rand((N, Tmax, H, D), 302)
+    lens = np.array([5, 13, 24], dtype=np.int32)
+    q = np.stack([qs[n, lens[n] - Tq:lens[n]] for n in range(N)])
+    o, lse, ok = oracle_mod.prefill(q, kc, vc, lens, window, 0.4)
+    assert ok
+    for n in range(N):
+        L = lens[n]
+        of, lf = oracle_mod.fwd(qs[n:n + 1, :L], kc[n:n + 1, :L], vc[n:n + 1, :L], window, 0.4)
+        np.testing.assert_allclose(o[n], of[0, L - Tq:L], atol=1e-13)
+        np.testing.assert_allclose(lse[n], lf[0, :, L - Tq:L], atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [1, 6, -1])
+def test_prefill_of_one_token_is_decode(oracle_mod, window):
+    N, Tmax, H, D = 4, 16, 2, 4
+    kc, vc = _rand((N, Tmax, H, D), 310), _rand((N, Tmax, H, D), 311)
+    q = _rand((N, 1, H, D), 312)
+    lens = np.array([1, 2, 9, 16], dtype=np.int32)
+    o, lse, ok = oracle_mod.prefill(q, kc, vc, lens, window, 0.7)
+    od, ld, okd = oracle_mod.decode(q[:, 0], kc, vc, lens, window, 0.7)
+    assert ok and okd
+    np.testing.assert_allclose(o[:, 0], od, atol=1e-14)
+    np.testing.assert_allclose(lse[:, :, 0], ld, atol=1e-14)
+
+
+def _dense_prefill_reference(q, kc, lens, vc, window, scale):
+    """Explicit (query, cache row) visibility matrix per sequence, pure Python loops."""
+    N, Tq, H, D = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((N, H, Tq))
+    for n in range(N):
+        L = int(lens[n])
+        for h in range(H):
+            for t in range(Tq):
+                i = L - Tq + t
+                vis = [1 if (j <= i and (window <= 0 or i - j < window)) else 0 for j in range(kc.shape[1])]
+                logits = [scale * sum(q[n, t, h, d] * kc[n, j, h, d] for d in range(D)) if vis[j] else -math.inf
+                          for j in range(kc.shape[1])]
+                m = max(logits)
+                z = sum(math.exp(x - m) for x in logits)
+                lse[n, h, t] = m + math.log(z)
+                for d in range(D):
+                    o[n, t, h, d] = sum(math.exp(logits[j] - m) / z * vc[n, j, h, d] for j in range(kc.shape[1])
+                                        if vis[j])
+    return o, lse
+
+
+@pytest.mark.parametrize("Tq,window", [(1, 2), (3, 2), (4, -1), (6, 3)])
+def test_prefill_brute_force_tiny(oracle_mod, Tq, window):
+    N, Tmax, H, D = 2, 9, 2, 3
+    q = _rand((N, Tq, H, D), 320)
+    kc, vc = _rand((N, Tmax, H, D), 321), _rand((N, Tmax, H, D), 322)
+    lens = np.array([Tq, Tmax], dtype=np.int32)
+    o, lse, ok = oracle_mod.prefill(q, kc, vc, lens, window, 0.8)
+    ob, lb = _dense_prefill_reference(q, kc, lens, vc, window, 0.8)
+    assert ok
+    np.testing.assert_allclose(o, ob, atol=1e-13)
+    np.testing.assert_allclose(lse, lb, atol=1e-13)
+
+
+@pytest.mark.parametrize("Tq,L,window", [(8, 8, -1), (7, 30, 5), (16, 40, 16), (1, 33, -1)])
+def test_prefill_matches_torch_sdpa_fp64(oracle_mod, Tq, L, window):
+    """torch SDPA with a band mask offset to the queries' cache positions."""
+    H, D = 3, 8
+    scale = 1.0 / math.sqrt(D)
+    q = torch.from_numpy(_rand((1, Tq, H, D), 330))
+    kc, vc = (torch.from_numpy(_rand((1, L, H, D), 331 + s)) for s in range(2))
+    i = torch.arange(L - Tq, L).view(Tq, 1)
+    j = torch.arange(L).view(1, L)
+    mask = (j <= i) & ((i - j < window) if window > 0 else torch.ones_like(j, dtype=torch.bool))
+    out = torch.nn.functional.scaled_dot_product_attention(q.transpose(1, 2), kc.transpose(1, 2), vc.transpose(1, 2),
+                                                           attn_mask=mask, scale=scale)
+    logits = scale * q.transpose(1, 2) @ kc.transpose(1, 2).transpose(-1, -2)
+    lse_ref = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1)
+    o, lse, ok = oracle_mod.prefill(q, kc, vc, np.array([L], dtype=np.int32), window, scale)
+    assert ok
+    np.testing.assert_allclose(o, out.transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref.numpy(), atol=1e-12)
+
+
+def test_prefill_ignores_slots_outside_window_and_length(oracle_mod):
+    N, Tq, Tmax, H, D, W = 2, 4, 20, 1, 4, 6
+    q = _rand((N, Tq, H, D), 340)
+    kc, vc = _rand((N, Tmax, H, D), 341), _rand((N, Tmax, H, D), 342)
+    lens = np.array([11, 20], dtype=np.int32)
+    o0, l0, _ = oracle_mod.prefill(q, kc, vc, lens, W, 0.5)
+    kp, vp = kc.copy(), vc.copy()
+    for n, L in enumerate(lens):
+        kp[n, L:] = np.nan; vp[n, L:] = np.nan
+        first = L - Tq - W + 1  # the first query's earliest visible row
+        kp[n, :first] = np.nan; vp[n, :first] = np.nan
+    o1, l1, _ = oracle_mod.prefill(q, kp, vp, lens, W, 0.5)
+    np.testing.assert_array_equal(o1, o0)
+    np.testing.assert_array_equal(l1, l0)
+
+
+def test_prefill_bad_length_is_reported(oracle_mod):
+    q = _rand((2, 3, 1, 4), 350)
+    kc, vc = _rand((2, 8, 1, 4), 351), _rand((2, 8, 1, 4), 352)
+    o, lse, ok = oracle_mod.prefill(q, kc, vc, np.array([2, 8], dtype=np.int32), -1, 0.5)
+    assert not ok
+    assert np.isnan(o[0]).all() and np.isnan(lse[0]).all()
+    assert np.isfinite(o[1]).all()

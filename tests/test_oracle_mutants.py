@@ -25,7 +25,11 @@ MUTANTS = {
     "dv weighted by ds": ("+= p[t] * dO[", "+= ds * dO["),
     "Delta omitted": ("delta += p[j - lo] * s;", "delta += 0.0 * s;"),
     "decode window one key short": ("long lo = L - W;", "long lo = L - W + 1;"),
-    "decode reads value of the key row": ("acc += p[j - lo] * vc[", "acc += p[j - lo] * kc["),
+    "decode reads value of the key row": ("j < L; ++j) acc += p[j - lo] * vc[", "j < L; ++j) acc += p[j - lo] * kc["),
+    "prefill query one position late": ("long i = L - Tq + t;", "long i = L - Tq + t + 1;\n                    if (i > L - 1) i = L - 1;"),
+    "prefill window one key short": (": i - window + 1;\n                    const double* qrow",
+                                     ": i - window + 2;\n                    const double* qrow"),
+    "prefill reads value of the key row": ("j <= i; ++j) acc += p[j - lo] * vc[", "j <= i; ++j) acc += p[j - lo] * kc["),
 }
 
 PIN_SUITE = [
@@ -35,6 +39,8 @@ PIN_SUITE = [
     (pins.test_backward_matches_finite_differences, {"window": 3}),
     (pins.test_gradient_sums, {"window": 3}),
     (pins.test_decode_equals_last_forward_row, {"window": 5}),
+    (pins.test_prefill_rows_equal_forward_rows, {"window": 4}),
+    (pins.test_prefill_brute_force_tiny, {"Tq": 3, "window": 2}),
 ]
 
 
