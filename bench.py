@@ -313,6 +313,7 @@ def run_ours(args, dist: Dist):
         out["e2e"] = run_e2e(calls, bufs, stream, dist, nc_attn, args)
     if not args.no_decode:
         out["decode"] = run_decode(dev, stream, nc_attn, peaks, peak_kind)
+        out["prefill"] = run_prefill(dev, stream, nc_attn, peaks, peak_kind)
     return out
 
 
@@ -358,6 +359,39 @@ def decode_bytes(lens, wl, window):
     W = wl.Tmax if window <= 0 else window
     rows = sum(min(int(L), W) for L in lens.tolist())
     return rows * wl.H * wl.D * 2 * 2 + wl.N * wl.H * wl.D * 2 * 2 + wl.N * wl.H * 4 + wl.N * 4
+
+
+def run_prefill(dev, stream, nc_attn, peaks, peak_kind):
+    """Prefill over a KV cache: TFLOP/s of the 4*D flops per visible pair, L2 flushed before each call."""
+    wl = workloads.PREFILL
+    q, kc, vc, lens = workloads.make_prefill(wl, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.N, wl.H, wl.Tq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {"workload": wl.name, "l2": "flushed (256 MB write) before every timed call"}
+    for window in wl.windows:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                nc_attn.nc_attn_prefill(q, kc, vc, lens, o, lse, window, wl.scale, stream)
+            evs = []
+            for _ in range(20):
+                flush.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                nc_attn.nc_attn_prefill(q, kc, vc, lens, o, lse, window, wl.scale, stream)
+                e.record(stream)
+                evs.append((s, e))
+            torch.cuda.synchronize()
+        ms = statistics.median([s.elapsed_time(e) for s, e in evs])
+        flops = 4.0 * wl.D * wl.H * workloads.prefill_pairs(lens.cpu(), wl.Tq, window)
+        tf = flops / (ms * 1e-3) / 1e12
+        key = "w1024" if window > 0 else "full"
+        res[key] = {"window": window, "us": round(ms * 1e3, 2), "TFLOP_s": round(tf, 1),
+                    "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                 "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
+    assert nc_attn.nc_get_device_error(stream) == 0
+    return res
 
 
 def run_decode(dev, stream, nc_attn, peaks, peak_kind):

@@ -64,20 +64,27 @@ struct FwdBarriers {
 };
 
 struct FwdParams {
-    __nv_bfloat16* o;
-    float* lse;
-    int B, T, H, W;       // W: effective window, 1 <= W <= T
+    __nv_bfloat16* o;     // [B, Tq, H, D]
+    float* lse;           // [B, H, Tq]
+    int B, H, W;          // W: effective window, 1 <= W <= Tk
+    int Tq;               // query rows per sequence (q, o, lse)
+    int Tk;               // rows of the K/V tensors per sequence
+    // Plain forward: nullptr, the queries are positions 0 .. Tq-1 of K/V (Tq == Tk).
+    // Prefill over a cache: per-sequence lengths L_b that count the Tq new tokens; query t
+    // of sequence b is position L_b - Tq + t.  A length outside [Tq, Tk] gives NaN rows and
+    // NC_ERR_BAD_CACHE_LEN.
+    const int* lens;
     float scale_log2;
     int n_pairs;          // query-tile pairs per (b, h)
     int* err;
 };
 
-// Key blocks [lo, hi] that intersect the window of some row of the tile starting at r0.
-__device__ __forceinline__ void tile_blocks(int r0, int T, int W, int& lo, int& hi) {
-    const int first_key = r0 - W + 1;
+// Key blocks [lo, hi] that intersect the window of some query of the tile whose first query sits at
+// position pos0; the last query of the sequence sits at position last.
+__device__ __forceinline__ void tile_blocks(int pos0, int last, int W, int& lo, int& hi) {
+    const int first_key = pos0 - W + 1;
     lo = first_key <= 0 ? 0 : first_key / kBN;
-    const int last_row = min(r0 + kBM - 1, T - 1);
-    hi = last_row / kBN;
+    hi = min(pos0 + kBM - 1, last) / kBN;
 }
 
 __device__ __forceinline__ bool aborted(const FwdBarriers& bars) {
@@ -92,6 +99,8 @@ __device__ __forceinline__ void record_timeout(FwdBarriers& bars, int* err) {
 // Geometry of one work item: a pair of 128-row query tiles of one (batch, head).
 struct FwdItem {
     int b, h;
+    int off;            // position of query row 0 (0 for the plain forward)
+    bool bad;           // the sequence's cache length is out of range: its rows become NaN
     int r0[2];
     int lo[2], hi[2];   // key blocks each tile visits (empty range for an inactive tile 1)
     int kb_lo, kb_hi;   // union of the two ranges
@@ -100,6 +109,7 @@ struct FwdItem {
 
 // Items are numbered heaviest first (query-tile pair descending, then (h, b)), so the
 // static zigzag assignment over persistent CTAs (nc_sched.cuh) hands out the long causal tiles first.
+template <bool kCache>
 __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     FwdItem it;
     const int bh = w % (p.B * p.H);
@@ -108,9 +118,19 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     it.b = bh / p.H;
     it.r0[0] = pair * 2 * kBM;
     it.r0[1] = pair * 2 * kBM + kBM;
-    it.active1 = it.r0[1] < p.T;
-    tile_blocks(it.r0[0], p.T, p.W, it.lo[0], it.hi[0]);
-    tile_blocks(it.r0[1], p.T, p.W, it.lo[1], it.hi[1]);
+    it.off = 0;
+    it.bad = false;
+    if (kCache) {
+        // a bad length still runs (clamped into range) so every role keeps the same schedule;
+        // the epilogue then writes NaN rows instead
+        const int L = p.lens[it.b];
+        it.bad = L < p.Tq || L > p.Tk;
+        it.off = min(max(L, p.Tq), p.Tk) - p.Tq;
+    }
+    const int last = it.off + p.Tq - 1;
+    it.active1 = it.r0[1] < p.Tq;
+    tile_blocks(it.off + it.r0[0], last, p.W, it.lo[0], it.hi[0]);
+    tile_blocks(it.off + it.r0[1], last, p.W, it.lo[1], it.hi[1]);
     if (!it.active1) {
         it.lo[1] = it.hi[0] + 1;
         it.hi[1] = it.hi[0];
@@ -120,7 +140,8 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     return it;
 }
 
-template <int D>
+// kCache: prefill over a KV cache (per-sequence query offsets from p.lens); otherwise the plain forward.
+template <int D, bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -176,7 +197,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int q_loads = 0;
         bool ok = true;
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem it = fwd_item(sched_item_index(ii), p);
+            const FwdItem it = fwd_item<kCache>(sched_item_index(ii), p);
             // Q of this item once the previous item's S products have read theirs
             if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
                 ok = false;
@@ -249,7 +270,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int seq = 0;                 // K/V ring position over all items
             int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
             for (int ii = 0; ok && ii < my_items; ++ii) {
-                const FwdItem it = fwd_item(sched_item_index(ii), p);
+                const FwdItem it = fwd_item<kCache>(sched_item_index(ii), p);
                 auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
                 ok = mbar_wait_warp(&bars.q_full, ii & 1);
                 if (!ok) break;
@@ -329,11 +350,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         int n_s = 0;  // S tiles of this query tile consumed over all items
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem item = fwd_item(sched_item_index(ii), p);
+            const FwdItem item = fwd_item<kCache>(sched_item_index(ii), p);
             const int tr0 = t ? item.r0[1] : item.r0[0];
             const int t_lo = t ? item.lo[1] : item.lo[0];
             const int t_hi = t ? item.hi[1] : item.hi[0];
-            const int row = tr0 + row_in_tile;
+            const int row = tr0 + row_in_tile;      // query row (q, o, lse coordinates)
+            const int pos = item.off + row;         // its position among the keys
+            const int tpos0 = item.off + tr0;
             const bool tile_on = (t == 0) || item.active1;
             float m_run = -INFINITY, l_run = 0.f;
             if (tile_on) {
@@ -351,12 +374,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                     // elementwise mask only on blocks that straddle the causal diagonal or the window edge
                     const int k0 = kb * kBN;
-                    const bool full_block = (k0 + kBN - 1 <= tr0) && (k0 >= tr0 + kBM - p.W);
+                    const bool full_block = (k0 + kBN - 1 <= tpos0) && (k0 >= tpos0 + kBM - p.W);
                     if (!full_block) {
 #pragma unroll
                         for (int j = 0; j < kBN; ++j) {
                             const int key = k0 + j;
-                            if (key > row || row - key >= p.W) s[j] = -INFINITY;
+                            if (key > pos || pos - key >= p.W) s[j] = -INFINITY;
                         }
                     }
                     float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
@@ -420,9 +443,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!ok) break;
             tc_fence_after();
             if (tile_on) {
-                const float inv_l = 1.f / l_run;
-                const bool in_range = row < p.T;
-                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(item.b) * p.T + row) * p.H + item.h) * D;
+                const float inv_l = item.bad ? __int_as_float(0x7fc00000) : 1.f / l_run;  // NaN rows for a bad length
+                const bool in_range = row < p.Tq;
+                if (item.bad && row_in_tile == 0 && t == 0) set_device_error(p.err, NC_ERR_BAD_CACHE_LEN);
+                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(item.b) * p.Tq + row) * p.H + item.h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -440,7 +464,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 if (in_range)
-                    p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.T + row] = (m_run + __log2f(l_run)) * kLn2;
+                    p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.Tq + row] =
+                        item.bad ? __int_as_float(0x7fc00000) : (m_run + __log2f(l_run)) * kLn2;
             }
             tc_fence_before();
             mbar_arrive(&bars.o_free);
@@ -455,22 +480,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
+// Tq query rows per sequence against Tk key/value rows; lens == nullptr for the plain forward
+// (Tq == Tk), else the per-sequence cache lengths of a prefill.
 template <int D>
-cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H,
-                          int window, float scale, int* err, cudaStream_t st) {
+cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int* lens, void* o, float* lse, int B,
+                          int Tq, int Tk, int H, int window, float scale, int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBN) ||
-        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBN))
+    if (!make_tmap_bthd(&tq, q, B, Tq, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, Tk, H, D, 64, kBN) ||
+        !make_tmap_bthd(&tv, v, B, Tk, H, D, 64, kBN))
         return cudaErrorInvalidValue;
     FwdParams p;
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.B = B;
-    p.T = T;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.lens = lens;
     p.H = H;
-    p.W = (window <= 0 || window >= T) ? T : window;
+    p.W = (window <= 0 || window >= Tk) ? Tk : window;
     p.scale_log2 = scale * kLog2e;
-    p.n_pairs = (T + 2 * kBM - 1) / (2 * kBM);
+    p.n_pairs = (Tq + 2 * kBM - 1) / (2 * kBM);
     p.err = err;
     const int smem = FwdSmem<D>::kBytes + 1024;
     static bool attr_set[64] = {false};
@@ -478,7 +507,9 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(fwd_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
@@ -491,7 +522,10 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
     const long n_items = (long)p.n_pairs * H * B;
     const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
-    fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+    if (lens != nullptr)
+        fwd_tc_kernel<D, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+    else
+        fwd_tc_kernel<D, false><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -500,8 +534,15 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
 
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st) {
-    return D == 128 ? launch_fwd_tc<128>(q, k, v, o, lse, B, T, H, window, scale, err, st)
-                    : launch_fwd_tc<64>(q, k, v, o, lse, B, T, H, window, scale, err, st);
+    return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, o, lse, B, T, T, H, window, scale, err, st)
+                    : launch_fwd_tc<64>(q, k, v, nullptr, o, lse, B, T, T, H, window, scale, err, st);
+}
+
+cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
+                           float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,
+                           cudaStream_t st) {
+    return D == 128 ? launch_fwd_tc<128>(q, kcache, vcache, lens, o, lse, N, Tq, Tmax, H, window, scale, err, st)
+                    : launch_fwd_tc<64>(q, kcache, vcache, lens, o, lse, N, Tq, Tmax, H, window, scale, err, st);
 }
 
 }  // namespace nc

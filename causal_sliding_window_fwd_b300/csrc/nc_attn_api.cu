@@ -85,6 +85,29 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
+nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens, void* o,
+                          float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
+                          cudaStream_t stream) {
+    nc_status st = check_shape(N, Tmax, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (Tq <= 0 || Tq > Tmax) return NC_ERR_INVALID;
+    if (!q || !kcache || !vcache || !cache_lens || !o || !lse) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !aligned16(lse))
+        return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID;
+    const size_t nq = (size_t)N * Tq * H * D * 2, nc_ = (size_t)N * Tmax * H * D * 2, nl = (size_t)N * H * Tq * 4;
+    const void* ins[4] = {q, kcache, vcache, cache_lens};
+    const size_t in_n[4] = {nq, nc_, nc_, (size_t)N * 4};
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_n[i], o, nq) || overlap(ins[i], in_n[i], lse, nl)) return NC_ERR_INVALID;
+    if (overlap(o, nq, lse, nl)) return NC_ERR_INVALID;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const cudaError_t e =
+        nc::launch_prefill(q, kcache, vcache, cache_lens, o, lse, N, Tq, Tmax, H, D, window, scale, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D) {
     if (B <= 0 || T <= 0 || H <= 0 || D <= 0) return 0;
     return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256) + 256;

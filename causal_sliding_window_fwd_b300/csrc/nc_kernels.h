@@ -15,6 +15,11 @@ int* device_error_word();
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);
 
+// Prefill over a KV cache: q/o [N,Tq,H,D] bf16, lse [N,H,Tq] fp32, caches [N,Tmax,H,D], lens device int32 [N].
+cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
+                           float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,
+                           cudaStream_t st);
+
 // Backward: dq_acc fp32 [B,T,H,D], delta fp32 [B,H,T] and the work-item counter are workspace.
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,

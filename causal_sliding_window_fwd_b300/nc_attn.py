@@ -28,7 +28,8 @@ NC_WINDOW_FULL = -1
 
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
-            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_get_device_error", "nc_launch_count",
+            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_get_device_error",
+            "nc_launch_count",
             "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
 
 # Size of the library's fixed decode scratch array (NC_DECODE_NOALLOC_SCRATCH_BYTES).
@@ -59,6 +60,8 @@ def _load():
     lib.nc_attn_decode_workspace_bytes.restype = sz
     lib.nc_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_decode.restype = i
+    lib.nc_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.nc_attn_prefill.restype = i
     lib.nc_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
     lib.nc_get_device_error.restype = i
     lib.nc_launch_count.argtypes = []
@@ -160,6 +163,21 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: fl
                               _stream(q.device, stream)), "nc_attn_decode")
 
 
+def nc_attn_prefill(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, stream=None) -> None:
+    """Prefill into caller-owned o [N,Tq,H,D] bf16 and lse [N,H,Tq] fp32; cache_lens count the new tokens."""
+    N, Tmax, H, D = kcache.shape
+    Tq = q.shape[1]
+    _need(q, "q", torch.bfloat16, (N, Tq, H, D))
+    _need(kcache, "kcache", torch.bfloat16)
+    _need(vcache, "vcache", torch.bfloat16, (N, Tmax, H, D))
+    _need(cache_lens, "cache_lens", torch.int32, (N,))
+    _need(o, "o", torch.bfloat16, (N, Tq, H, D))
+    _need(lse, "lse", torch.float32, (N, H, Tq))
+    _check(lib.nc_attn_prefill(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
+                               N, Tq, Tmax, H, D, int(window), float(scale), _stream(q.device, stream)),
+           "nc_attn_prefill")
+
+
 def nc_attn_decode_noalloc_scratch_bytes(N: int, Tmax: int, H: int, D: int, window: int) -> int:
     return int(lib.nc_attn_decode_noalloc_scratch_bytes(N, Tmax, H, D, int(window)))
 
@@ -226,6 +244,17 @@ def attn_bwd(q, k, v, o, dO, lse, window: int, scale: float | None = None, works
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
     return dq, dk, dv
+
+
+def attn_prefill(q, kcache, vcache, cache_lens, window: int, scale: float | None = None, stream=None):
+    """Returns (o [N,Tq,H,D], lse [N,H,Tq]) for the new tokens q [N,Tq,H,D]."""
+    N, Tmax, H, D = kcache.shape
+    Tq = q.shape[1]
+    scale = default_scale(D) if scale is None else scale
+    o = torch.empty((N, Tq, H, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((N, H, Tq), dtype=torch.float32, device=q.device)
+    nc_attn_prefill(q, kcache, vcache, cache_lens, o, lse, window, scale, stream)
+    return o, lse
 
 
 def attn_decode(q, kcache, vcache, cache_lens, window: int, scale: float | None = None, workspace=None,

@@ -90,6 +90,33 @@ DECODE = DecodeWorkload("decode N64 H10 D128 Tmax8192 len U[256,8192] W{1024,ful
                         64, 8192, 10, 128, 256, 8192, (1024, WINDOW_FULL), _seed(4, 0))
 
 
+@dataclass(frozen=True)
+class PrefillWorkload:
+    """Tq new tokens appended to each sequence of a padded KV cache [N, Tmax, H, D].
+
+    A sequence's length counts its new tokens (their keys and values are in the cache)."""
+    name: str
+    N: int
+    Tq: int
+    Tmax: int
+    H: int
+    D: int
+    len_lo: int
+    len_hi: int          # inclusive
+    windows: tuple
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+# Prompt prefill after earlier turns (the Engine's prefill over a KV cache): 8 sequences, 2048
+# new tokens each, total lengths U[2048, 8192], depth-20 heads.
+PREFILL = PrefillWorkload("prefill N8 Tq2048 H10 D128 Tmax8192 len U[2048,8192] W{1024,full}",
+                          8, 2048, 8192, 10, 128, 2048, 8192, (1024, WINDOW_FULL), _seed(6, 0))
+
+
 def generator(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=torch.device(device))
     g.manual_seed(int(seed))
@@ -133,6 +160,33 @@ def make_decode(wl: DecodeWorkload, device="cpu", poison_tail: bool = False):
         kc.masked_fill_(dead, float("nan"))
         vc.masked_fill_(dead, float("nan"))
     return q, kc, vc, lens.to(device)
+
+
+def prefill_lens(wl: PrefillWorkload) -> torch.Tensor:
+    """Per-sequence cache lengths (new tokens included), uniform in [len_lo, len_hi], int32 on the CPU."""
+    g = generator(wl.seed, "cpu")
+    return torch.randint(wl.len_lo, wl.len_hi + 1, (wl.N,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def make_prefill(wl: PrefillWorkload, device="cpu"):
+    """(q [N,Tq,H,D], kcache, vcache [N,Tmax,H,D], lens int32 [N]) with lens on ``device``."""
+    lens = prefill_lens(wl)
+    g = generator(wl.seed + 1, device)
+    q = randn_bf16((wl.N, wl.Tq, wl.H, wl.D), g, device)
+    kc = randn_bf16((wl.N, wl.Tmax, wl.H, wl.D), g, device)
+    vc = randn_bf16((wl.N, wl.Tmax, wl.H, wl.D), g, device)
+    return q, kc, vc, lens.to(device)
+
+
+def prefill_pairs(lens, Tq: int, window: int) -> int:
+    """Visible (query, key) pairs of a prefill: new token t of a sequence of length L is position
+    L - Tq + t and sees min(W, position + 1) keys."""
+    total = 0
+    for L in (int(x) for x in lens):
+        for t in range(Tq):
+            i = L - Tq + t
+            total += (i + 1) if window <= 0 else min(window, i + 1)
+    return total
 
 
 def pairs_in_window(T: int, window: int) -> int:

@@ -126,6 +126,30 @@ nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, 
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Prefill (append) over a KV cache: Tq new tokens per sequence attend over the
+ * cache ("nanochat" walkthrough, page 4: the Engine's prefill/decode split
+ * over a KV cache).  The keys and values of the new tokens are already in the
+ * cache: cache_lens[n] = L counts them, and new token t is the query at
+ * position L - Tq + t; it sees cache rows max(0, L - Tq + t + 1 - window) ..
+ * L - Tq + t.  With Tq = 1 this is nc_attn_decode's result.
+ *   q          : const bf16 [N, Tq, H, D] device
+ *   kcache     : const bf16 [N, Tmax, H, D] device
+ *   vcache     : const bf16 [N, Tmax, H, D] device
+ *   cache_lens : const int32 [N] device, each in [Tq, Tmax]; a value outside
+ *                that range sets NC_ERR_BAD_CACHE_LEN on the device and makes
+ *                that sequence's o and lse rows NaN
+ *   o          : bf16 [N, Tq, H, D] device, written
+ *   lse        : fp32 [N, H, Tq] device, written
+ * The cache is read in 128-row blocks: rows from L up to the end of the
+ * 128-row block that holds row L - 1 are loaded and masked out, so they must
+ * hold finite values (any finite values, e.g. the zeros of a fresh cache).
+ * Rows beyond that block are never read.  Needs no workspace; Tq <= Tmax.
+ */
+nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
+                          void* o, float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
+                          cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * the kernels set (NC_OK if nothing went wrong since the last call).
  * Returns NC_ERR_CUDA if the synchronisation itself failed.

@@ -26,7 +26,7 @@ def _declared():
 
 
 def test_header_declares_the_abi():
-    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_bwd_workspace_bytes",
+    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_prefill", "nc_attn_bwd_workspace_bytes",
             "nc_attn_decode_workspace_bytes", "nc_get_device_error", "nc_status_string",
             "nc_launch_count"} <= set(_declared())
 
@@ -141,3 +141,30 @@ def test_decode_rejects_bad_arguments(lib):
     assert _dec(lib, p) == lib.NC_ERR_INVALID
     p = list(A[:6]); p[3] = p[3] + 2        # lens misaligned
     assert _dec(lib, p) == lib.NC_ERR_INVALID
+
+
+def _pre(lib, ptrs=None, **kw):
+    a = dict(N=4, Tq=16, Tmax=256, H=2, D=128, window=64, scale=0.1)
+    a.update(kw)
+    p = list(A[:6]) if ptrs is None else ptrs
+    return lib.lib.nc_attn_prefill(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                                   a["N"], a["Tq"], a["Tmax"], a["H"], a["D"], a["window"],
+                                   ctypes.c_float(a["scale"]), None)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _pre(lib, N=0) == lib.NC_ERR_INVALID
+    assert _pre(lib, Tq=0) == lib.NC_ERR_INVALID
+    assert _pre(lib, Tq=257) == lib.NC_ERR_INVALID  # more new tokens than cache rows
+    assert _pre(lib, D=96) == lib.NC_ERR_UNSUPPORTED
+    assert _pre(lib, window=0) == lib.NC_ERR_INVALID
+    assert _pre(lib, scale=float("nan")) == lib.NC_ERR_INVALID
+    for i in range(6):
+        p = list(A[:6]); p[i] = 0
+        assert _pre(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[4] = p[2]            # o aliases the value cache
+    assert _pre(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[0] = p[0] + 8        # q not 16-byte aligned
+    assert _pre(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[3] = p[3] + 2        # lens misaligned
+    assert _pre(lib, p) == lib.NC_ERR_INVALID

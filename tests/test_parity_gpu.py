@@ -245,6 +245,111 @@ def test_decode_bad_length_reports_and_nans(nc):
     assert nc.nc_get_device_error() == 0  # cleared by the read
 
 
+# ---------------------------------------------------------------- prefill over a KV cache
+
+
+def _prefill_inputs(N, Tq, Tmax, H, D, lens, seed):
+    g = workloads.generator(seed, "cuda")
+    q = workloads.randn_bf16((N, Tq, H, D), g, "cuda")
+    kc = workloads.randn_bf16((N, Tmax, H, D), g, "cuda")
+    vc = workloads.randn_bf16((N, Tmax, H, D), g, "cuda")
+    return q, kc, vc, torch.tensor(lens, dtype=torch.int32, device="cuda")
+
+
+def _poison_past_length(kc, vc, lens):
+    """Rows at or beyond a sequence's length: the rest of the 128-row block that holds its last
+    row gets large finite values (loaded and masked out), every later row NaN (never read)."""
+    Tmax = kc.shape[1]
+    for n, L in enumerate(int(x) for x in lens):
+        end = min(Tmax, (L + 127) // 128 * 128)
+        kc[n, L:end] = 3.0e4
+        vc[n, L:end] = -3.0e4
+        kc[n, end:] = float("nan")
+        vc[n, end:] = float("nan")
+
+
+PREFILL_CASES = [
+    # (N, Tq, Tmax, H, D, window, lens)
+    (2, 1, 300, 2, 128, 100, [1, 300]),
+    (2, 37, 400, 2, 64, -1, [37, 251]),
+    (3, 128, 512, 2, 128, 64, [128, 300, 512]),
+    (2, 200, 700, 1, 128, 129, [200, 650]),
+    (2, 257, 1024, 2, 64, 1, [300, 1024]),
+    (4, 90, 1000, 3, 128, 512, [90, 91, 513, 999]),
+    (2, 600, 2048, 2, 128, 256, [600, 1999]),
+]
+
+
+@pytest.mark.parametrize("N,Tq,Tmax,H,D,window,lens", PREFILL_CASES)
+def test_prefill_small(nc, oracle_mod, N, Tq, Tmax, H, D, window, lens):
+    q, kc, vc, lens_t = _prefill_inputs(N, Tq, Tmax, H, D, lens, 5000 + Tq + Tmax)
+    scale = 1.0 / math.sqrt(D)
+    o_ref, lse_ref, ok = oracle_mod.prefill(q.cpu(), kc.cpu(), vc.cpu(), lens_t.cpu(), window, scale)
+    assert ok
+    _poison_past_length(kc, vc, lens)
+    o, lse = nc.attn_prefill(q, kc, vc, lens_t, window, scale)
+    assert nc.nc_get_device_error() == 0
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
+def test_prefill_of_whole_sequence_is_the_forward(nc):
+    """Every cache row new (L = Tq = Tmax): the same products in the same order as the forward."""
+    B, T, H, D, W = 2, 333, 2, 128, 100
+    q, k, v, _ = workloads.make_qkvdo_shape(B, T, H, D, seed=61, device="cuda")
+    o, lse = nc.attn_fwd(q, k, v, W)
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    op, lsep = nc.attn_prefill(q, k, v, lens, W)
+    assert nc.nc_get_device_error() == 0
+    assert torch.equal(op, o) and torch.equal(lsep, lse)
+
+
+def test_prefill_of_one_token_matches_decode(nc):
+    N, Tmax, H, D, W = 5, 900, 2, 128, 300
+    q, kc, vc, lens = _prefill_inputs(N, 1, Tmax, H, D, [1, 2, 129, 640, 900], 71)
+    op, lsep = nc.attn_prefill(q, kc, vc, lens, W)
+    od, lsed = nc.attn_decode(q[:, 0].contiguous(), kc, vc, lens, W)
+    assert nc.nc_get_device_error() == 0
+    torch.testing.assert_close(op[:, 0].float(), od.float(), atol=2e-2, rtol=0)
+    assert (lsep[:, :, 0] - lsed).abs().max().item() < 1e-3
+
+
+def test_prefill_bad_length_reports_and_nans(nc, oracle_mod):
+    N, Tq, Tmax, H, D = 4, 50, 256, 2, 128
+    q, kc, vc, lens = _prefill_inputs(N, Tq, Tmax, H, D, [50, 49, 257, 200], 83)
+    o, lse = nc.attn_prefill(q, kc, vc, lens, -1)
+    assert nc.nc_get_device_error() == nc.NC_ERR_BAD_CACHE_LEN
+    for n in (1, 2):
+        assert torch.isnan(o[n].float()).all() and torch.isnan(lse[n]).all()
+    good = [0, 3]
+    o_ref, lse_ref, ok = oracle_mod.prefill(q[good].cpu(), kc[good].cpu(), vc[good].cpu(), lens[good].cpu(), -1,
+                                            1.0 / math.sqrt(D))
+    assert ok
+    assert rel_err(o[good], o_ref) <= O_TOL
+    assert abs_err(lse[good], lse_ref) <= LSE_TOL
+    assert nc.nc_get_device_error() == 0  # cleared by the read
+
+
+@pytest.mark.parametrize("window", [1024, -1])
+def test_prefill_full_size_sampled(nc, oracle_mod, window):
+    """The benchmark's prefill workload; the oracle checks the last 256 new tokens of a few
+    (sequence, head) slices, which sit at the same cache positions in a Tq = 256 prefill."""
+    wl = workloads.PREFILL
+    q, kc, vc, lens = workloads.make_prefill(wl, "cuda")
+    o, lse = nc.attn_prefill(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    seqs, heads, tail = [0, int(torch.argmax(lens)), int(torch.argmin(lens))], [0, 7], 256
+    for hh in heads:
+        qs = q[seqs, wl.Tq - tail:, hh:hh + 1].contiguous().cpu()
+        ks = kc[seqs, :, hh:hh + 1].contiguous().cpu()
+        vs = vc[seqs, :, hh:hh + 1].contiguous().cpu()
+        o_ref, lse_ref, ok = oracle_mod.prefill(qs, ks, vs, lens[seqs].cpu(), window, wl.scale)
+        assert ok
+        assert rel_err(o[seqs, wl.Tq - tail:, hh:hh + 1], o_ref) <= O_TOL
+        assert abs_err(lse[seqs, hh:hh + 1, wl.Tq - tail:], lse_ref) <= LSE_TOL
+
+
 # ---------------------------------------------------------------- failure detection
 
 
