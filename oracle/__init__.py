@@ -154,6 +154,45 @@ def prefill(q, kcache, vcache, cache_lens, window: int, scale: float):
     return _load().prefill(q, kcache, vcache, cache_lens, window, scale)
 
 
+def _doc_bounds(cu_seqlens):
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+    cu = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+    assert cu[0] == 0 and all(b >= a for a, b in zip(cu, cu[1:])), "cu_seqlens must start at 0 and not decrease"
+    return cu
+
+
+def fwd_varlen(q, k, v, cu_seqlens, window: int, scale: float):
+    """Document-masked (varlen) forward over packed rows.  q, k, v: [1, total, H, D]; document d is rows
+    cu_seqlens[d] .. cu_seqlens[d+1]-1 and attends only within itself (the window counts positions inside
+    the document).  Each document is an independent problem, so this is the forward applied per slice.
+    Returns (o [1, total, H, D], lse [1, H, total])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu = _doc_bounds(cu_seqlens)
+    _, total, H, D = q.shape
+    assert cu[-1] == total
+    o = np.empty_like(q)
+    lse = np.empty((1, H, total), dtype=np.float64)
+    for a, b in zip(cu, cu[1:]):
+        if b > a:
+            od, ld = _load().fwd(q[:, a:b], k[:, a:b], v[:, a:b], window, scale)
+            o[:, a:b] = od
+            lse[:, :, a:b] = ld
+    return o, lse
+
+
+def bwd_varlen(q, k, v, dO, cu_seqlens, window: int, scale: float):
+    """Gradients of the document-masked forward: the backward applied per document slice."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    cu = _doc_bounds(cu_seqlens)
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    for a, b in zip(cu, cu[1:]):
+        if b > a:
+            g = _load().bwd(q[:, a:b], k[:, a:b], v[:, a:b], dO[:, a:b], window, scale)
+            dq[:, a:b], dk[:, a:b], dv[:, a:b] = g
+    return dq, dk, dv
+
+
 def decode(q, kcache, vcache, cache_lens, window: int, scale: float):
     """One-token decode.  q [N,H,D]; caches [N,Tmax,H,D]; cache_lens [N] (int).
 

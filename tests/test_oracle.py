@@ -410,3 +410,69 @@ def test_prefill_bad_length_is_reported(oracle_mod):
     assert not ok
     assert np.isnan(o[0]).all() and np.isnan(lse[0]).all()
     assert np.isfinite(o[1]).all()
+
+
+# ---------------------------------------------------------------- document-masked (varlen) attention
+
+
+def _packed_mask(cu, window):
+    """Explicit (query, key) visibility over packed rows: same document, causal, inside the window."""
+    total = cu[-1]
+    doc = np.zeros(total, dtype=np.int64)
+    start = np.zeros(total, dtype=np.int64)
+    for d, (a, b) in enumerate(zip(cu, cu[1:])):
+        doc[a:b] = d
+        start[a:b] = a
+    i = np.arange(total).reshape(-1, 1)
+    j = np.arange(total).reshape(1, -1)
+    m = (doc.reshape(-1, 1) == doc.reshape(1, -1)) & (j <= i)
+    if window > 0:
+        m &= (i - j) < window
+    return m
+
+
+@pytest.mark.parametrize("cu,window", [([0, 7], 3), ([0, 3, 3, 10, 16], 4), ([0, 1, 2, 9], -1), ([0, 5, 12], 1)])
+def test_varlen_matches_torch_sdpa_with_packed_mask(oracle_mod, cu, window):
+    """torch SDPA in fp64 with an explicit block-diagonal band mask, and its autograd."""
+    total, H, D = cu[-1], 2, 8
+    scale = 1.0 / math.sqrt(D)
+    q, k, v, dO = (torch.from_numpy(_rand((1, total, H, D), 400 + s)) for s in range(4))
+    mask = torch.from_numpy(_packed_mask(cu, window))
+    qt, kt, vt = (x.transpose(1, 2).clone().requires_grad_(True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    out.backward(dO.transpose(1, 2))
+    logits = scale * qt.detach() @ kt.detach().transpose(-1, -2)
+    lse_ref = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1)
+    o, lse = oracle_mod.fwd_varlen(q, k, v, cu, window, scale)
+    np.testing.assert_allclose(o, out.detach().transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref.numpy(), atol=1e-12)
+    dq, dk, dv = oracle_mod.bwd_varlen(q, k, v, dO, cu, window, scale)
+    np.testing.assert_allclose(dq, qt.grad.transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.transpose(1, 2).numpy(), atol=1e-12)
+
+
+def test_varlen_documents_do_not_interact(oracle_mod):
+    cu = [0, 6, 6, 15, 20]
+    total, H, D = cu[-1], 2, 4
+    q, k, v, dO = (_rand((1, total, H, D), 410 + s) for s in range(4))
+    o0, l0 = oracle_mod.fwd_varlen(q, k, v, cu, 5, 0.6)
+    g0 = oracle_mod.bwd_varlen(q, k, v, dO, cu, 5, 0.6)
+    q2, k2, v2, dO2 = (x.copy() for x in (q, k, v, dO))
+    for x in (q2, k2, v2, dO2):
+        x[:, 6:15] = _rand((1, 9, H, D), 420)  # replace the third document only
+    o1, l1 = oracle_mod.fwd_varlen(q2, k2, v2, cu, 5, 0.6)
+    g1 = oracle_mod.bwd_varlen(q2, k2, v2, dO2, cu, 5, 0.6)
+    for sl in (slice(0, 6), slice(15, 20)):
+        np.testing.assert_array_equal(o1[:, sl], o0[:, sl])
+        np.testing.assert_array_equal(l1[:, :, sl], l0[:, :, sl])
+        for a, b in zip(g1, g0):
+            np.testing.assert_array_equal(a[:, sl], b[:, sl])
+
+
+def test_varlen_single_document_is_the_forward(oracle_mod):
+    q, k, v = (_rand((1, 13, 2, 4), 430 + s) for s in range(3))
+    o, lse = oracle_mod.fwd_varlen(q, k, v, [0, 13], 4, 0.5)
+    of, lf = oracle_mod.fwd(q, k, v, 4, 0.5)
+    np.testing.assert_array_equal(o, of)
+    np.testing.assert_array_equal(lse, lf)
