@@ -74,10 +74,17 @@ struct FwdParams {
     // of sequence b is position L_b - Tq + t.  A length outside [Tq, Tk] gives NaN rows and
     // NC_ERR_BAD_CACHE_LEN.
     const int* lens;
+    // Document-masked (varlen) forward: q, k, v, o are packed [1, Tq, H, D] rows (Tq = Tk = total)
+    // and document d is rows cu[d] .. cu[d+1]-1, attending only within itself; nullptr otherwise.
+    const int* cu;
+    int n_docs;
     float scale_log2;
-    int n_pairs;          // query-tile pairs per (b, h)
+    int n_pairs;          // query-tile pairs per (b, h), or per (document, h): the longest document's
     int* err;
 };
+
+// Forward variants: plain, prefill over a KV cache, document-masked packed rows.
+enum FwdMode { kModePlain = 0, kModeCache = 1, kModeVarlen = 2 };
 
 // Key blocks [lo, hi] that intersect the window of some query of the tile whose first query sits at
 // position pos0; the last query of the sequence sits at position last.
@@ -99,8 +106,11 @@ __device__ __forceinline__ void record_timeout(FwdBarriers& bars, int* err) {
 // Geometry of one work item: a pair of 128-row query tiles of one (batch, head).
 struct FwdItem {
     int b, h;
-    int off;            // position of query row 0 (0 for the plain forward)
-    bool bad;           // the sequence's cache length is out of range: its rows become NaN
+    int off;            // position of query row 0 among the keys (prefill); 0 otherwise
+    int base;           // first packed row of the document (varlen); 0 otherwise
+    int len;            // query rows of this sequence or document
+    bool bad;           // the sequence's cache length (or the document's bounds) is out of range
+    bool empty;         // nothing to do (a varlen pair past its document's end, or a bad document)
     int r0[2];
     int lo[2], hi[2];   // key blocks each tile visits (empty range for an inactive tile 1)
     int kb_lo, kb_hi;   // union of the two ranges
@@ -109,26 +119,39 @@ struct FwdItem {
 
 // Items are numbered heaviest first (query-tile pair descending, then (h, b)), so the
 // static zigzag assignment over persistent CTAs (nc_sched.cuh) hands out the long causal tiles first.
-template <bool kCache>
+template <int kMode>
 __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     FwdItem it;
-    const int bh = w % (p.B * p.H);
-    const int pair = p.n_pairs - 1 - w / (p.B * p.H);
+    const int per_pair = kMode == kModeVarlen ? p.H * p.n_docs : p.B * p.H;
+    const int bh = w % per_pair;
+    const int pair = p.n_pairs - 1 - w / per_pair;
     it.h = bh % p.H;
-    it.b = bh / p.H;
+    it.b = kMode == kModeVarlen ? 0 : bh / p.H;
     it.r0[0] = pair * 2 * kBM;
     it.r0[1] = pair * 2 * kBM + kBM;
     it.off = 0;
+    it.base = 0;
+    it.len = p.Tq;
     it.bad = false;
-    if (kCache) {
+    it.empty = false;
+    if (kMode == kModeCache) {
         // a bad length still runs (clamped into range) so every role keeps the same schedule;
         // the epilogue then writes NaN rows instead
         const int L = p.lens[it.b];
         it.bad = L < p.Tq || L > p.Tk;
         it.off = min(max(L, p.Tq), p.Tk) - p.Tq;
     }
-    const int last = it.off + p.Tq - 1;
-    it.active1 = it.r0[1] < p.Tq;
+    if (kMode == kModeVarlen) {
+        const int d = bh / p.H;
+        const int a = p.cu[d], e = p.cu[d + 1];
+        it.bad = a < 0 || e < a || e > p.Tq || e - a > p.n_pairs * 2 * kBM;
+        it.base = it.bad ? 0 : a;
+        it.len = it.bad ? 0 : e - a;
+        it.empty = it.bad || it.r0[0] >= it.len;
+        if (it.empty) it.len = 1;  // keeps the block arithmetic below in range; nothing is done
+    }
+    const int last = it.off + it.len - 1;
+    it.active1 = it.r0[1] < it.len;
     tile_blocks(it.off + it.r0[0], last, p.W, it.lo[0], it.hi[0]);
     tile_blocks(it.off + it.r0[1], last, p.W, it.lo[1], it.hi[1]);
     if (!it.active1) {
@@ -140,8 +163,11 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     return it;
 }
 
-// kCache: prefill over a KV cache (per-sequence query offsets from p.lens); otherwise the plain forward.
-template <int D, bool kCache>
+// kMode: the plain forward, prefill over a KV cache (per-sequence query offsets from p.lens), or
+// document-masked packed rows (per-document row bases from p.cu).  Varlen work items past a
+// document's end are skipped by every role alike; `ip` counts the items a role really ran and
+// gives the phases of the per-item barriers.
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -186,7 +212,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
         regs_decrease<72>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -197,9 +223,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int q_loads = 0;
         bool ok = true;
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem it = fwd_item<kCache>(sched_item_index(ii), p);
+            const FwdItem it = fwd_item<kMode>(sched_item_index(ii), p);
+            if (it.empty) {
+                if (it.bad && lane == 0) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
+                continue;
+            }
             // Q of this item once the previous item's S products have read theirs
-            if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
+            if (!mbar_wait_warp(&bars.q_empty, (q_loads & 1) ^ 1) || aborted(bars)) {
                 ok = false;
                 break;
             }
@@ -207,7 +237,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int t = 0; t < 2; ++t)
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_4d_w(smem + L::kQOff + t * L::kTileBytes + c * kBM * 128, &tm_q, &bars.q_full, c * 64,
-                                  it.h, it.r0[t], it.b);
+                                  it.h, it.base + it.r0[t], it.b);
             ++q_loads;
             const int n_loads = 2 * (it.kb_hi - it.kb_lo + 1);
             for (int x = 0; x < n_loads; ++x, ++seq) {
@@ -221,7 +251,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint8_t* dst = smem + L::kKVOff + slot * L::kTileBytes;
                 mbar_arrive_expect_tx_w(&bars.kv_full[slot], L::kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, it.h, kb * kBN, it.b);
+                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, it.h, it.base + kb * kBN, it.b);
             }
         }
         if (!ok) record_timeout(bars, p.err);
@@ -234,7 +264,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
         regs_decrease<72>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
         {
             constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
@@ -269,10 +299,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             bool ok = true;
             int seq = 0;                 // K/V ring position over all items
             int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
+            int ip = 0;                  // items run
             for (int ii = 0; ok && ii < my_items; ++ii) {
-                const FwdItem it = fwd_item<kCache>(sched_item_index(ii), p);
+                const FwdItem it = fwd_item<kMode>(sched_item_index(ii), p);
+                if (it.empty) continue;
                 auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
-                ok = mbar_wait_warp(&bars.q_full, ii & 1);
+                ok = mbar_wait_warp(&bars.q_full, ip & 1);
                 if (!ok) break;
                 {
                     const int slot_k = seq % kStages;
@@ -296,9 +328,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     bool k_ready = false;
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (act(t, kb)) {
-                            if (first_pv && ii > 0) {
+                            if (first_pv && ip > 0) {
                                 // the epilogue of the previous item has read both O tiles
-                                ok = mbar_wait_warp(&bars.o_free, (ii - 1) & 1) && !aborted(bars);
+                                ok = mbar_wait_warp(&bars.o_free, (ip - 1) & 1) && !aborted(bars);
                                 if (!ok) break;
                             }
                             first_pv = false;
@@ -327,6 +359,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 if (ok) mma_commit_w(&bars.o_final);
+                ++ip;
             }
             if (!ok) record_timeout(bars, p.err);
             // all products must have landed before TMEM is released
@@ -338,7 +371,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         regs_increase<216>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * p.B);
+        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
@@ -349,8 +382,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float sl2 = p.scale_log2;
         bool ok = true;
         int n_s = 0;  // S tiles of this query tile consumed over all items
+        int ip = 0;   // items run
         for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem item = fwd_item<kCache>(sched_item_index(ii), p);
+            const FwdItem item = fwd_item<kMode>(sched_item_index(ii), p);
+            if (item.empty) continue;
             const int tr0 = t ? item.r0[1] : item.r0[0];
             const int t_lo = t ? item.lo[1] : item.lo[0];
             const int t_hi = t ? item.hi[1] : item.hi[0];
@@ -439,14 +474,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2; then hand both O tiles back
-            if (ok) ok = mbar_wait_warp(&bars.o_final, ii & 1) && !aborted(bars);
+            if (ok) ok = mbar_wait_warp(&bars.o_final, ip & 1) && !aborted(bars);
+            ++ip;
             if (!ok) break;
             tc_fence_after();
             if (tile_on) {
                 const float inv_l = item.bad ? __int_as_float(0x7fc00000) : 1.f / l_run;  // NaN rows for a bad length
-                const bool in_range = row < p.Tq;
+                const bool in_range = row < item.len;
                 if (item.bad && row_in_tile == 0 && t == 0) set_device_error(p.err, NC_ERR_BAD_CACHE_LEN);
-                __nv_bfloat16* orow = p.o + ((static_cast<size_t>(item.b) * p.Tq + row) * p.H + item.h) * D;
+                __nv_bfloat16* orow =
+                    p.o + ((static_cast<size_t>(item.b) * p.Tq + item.base + row) * p.H + item.h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -464,7 +501,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
                 if (in_range)
-                    p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.Tq + row] =
+                    p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.Tq + item.base + row] =
                         item.bad ? __int_as_float(0x7fc00000) : (m_run + __log2f(l_run)) * kLn2;
             }
             tc_fence_before();
@@ -482,9 +519,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
 // Tq query rows per sequence against Tk key/value rows; lens == nullptr for the plain forward
 // (Tq == Tk), else the per-sequence cache lengths of a prefill.
+// cu != nullptr: document-masked packed rows (B = 1, Tq = Tk = total), n_docs documents, the longest
+// at most max_len rows.
 template <int D>
-cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int* lens, void* o, float* lse, int B,
-                          int Tq, int Tk, int H, int window, float scale, int* err, cudaStream_t st) {
+cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int* lens, const int* cu, int n_docs,
+                          int max_len, void* o, float* lse, int B, int Tq, int Tk, int H, int window, float scale,
+                          int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv;
     if (!make_tmap_bthd(&tq, q, B, Tq, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, Tk, H, D, 64, kBN) ||
         !make_tmap_bthd(&tv, v, B, Tk, H, D, 64, kBN))
@@ -496,10 +536,12 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.Tq = Tq;
     p.Tk = Tk;
     p.lens = lens;
+    p.cu = cu;
+    p.n_docs = n_docs;
     p.H = H;
     p.W = (window <= 0 || window >= Tk) ? Tk : window;
     p.scale_log2 = scale * kLog2e;
-    p.n_pairs = (Tq + 2 * kBM - 1) / (2 * kBM);
+    p.n_pairs = ((cu != nullptr ? max_len : Tq) + 2 * kBM - 1) / (2 * kBM);
     p.err = err;
     const int smem = FwdSmem<D>::kBytes + 1024;
     static bool attr_set[64] = {false};
@@ -507,9 +549,11 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModePlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModeCache>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModeVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
@@ -519,13 +563,15 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
         e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const long n_items = (long)p.n_pairs * H * B;
+    const long n_items = (long)p.n_pairs * H * (cu != nullptr ? n_docs : B);
     const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
-    if (lens != nullptr)
-        fwd_tc_kernel<D, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+    if (cu != nullptr)
+        fwd_tc_kernel<D, kModeVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+    else if (lens != nullptr)
+        fwd_tc_kernel<D, kModeCache><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
     else
-        fwd_tc_kernel<D, false><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+        fwd_tc_kernel<D, kModePlain><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -534,15 +580,26 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
 
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st) {
-    return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, o, lse, B, T, T, H, window, scale, err, st)
-                    : launch_fwd_tc<64>(q, k, v, nullptr, o, lse, B, T, T, H, window, scale, err, st);
+    return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st)
+                    : launch_fwd_tc<64>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st);
 }
 
 cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
                            float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,
                            cudaStream_t st) {
-    return D == 128 ? launch_fwd_tc<128>(q, kcache, vcache, lens, o, lse, N, Tq, Tmax, H, window, scale, err, st)
-                    : launch_fwd_tc<64>(q, kcache, vcache, lens, o, lse, N, Tq, Tmax, H, window, scale, err, st);
+    return D == 128 ? launch_fwd_tc<128>(q, kcache, vcache, lens, nullptr, 0, 0, o, lse, N, Tq, Tmax, H, window, scale,
+                                         err, st)
+                    : launch_fwd_tc<64>(q, kcache, vcache, lens, nullptr, 0, 0, o, lse, N, Tq, Tmax, H, window, scale,
+                                        err, st);
+}
+
+cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const int* cu, int n_docs, int max_len,
+                              void* o, float* lse, int total, int H, int D, int window, float scale, int* err,
+                              cudaStream_t st) {
+    return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, cu, n_docs, max_len, o, lse, 1, total, total, H, window,
+                                         scale, err, st)
+                    : launch_fwd_tc<64>(q, k, v, nullptr, cu, n_docs, max_len, o, lse, 1, total, total, H, window,
+                                        scale, err, st);
 }
 
 }  // namespace nc

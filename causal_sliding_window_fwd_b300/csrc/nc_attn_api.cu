@@ -64,6 +64,7 @@ const char* nc_status_string(nc_status s) {
         case NC_ERR_CUDA: return "NC_ERR_CUDA";
         case NC_ERR_DEVICE_TIMEOUT: return "NC_ERR_DEVICE_TIMEOUT";
         case NC_ERR_BAD_CACHE_LEN: return "NC_ERR_BAD_CACHE_LEN";
+        case NC_ERR_BAD_SEQLENS: return "NC_ERR_BAD_SEQLENS";
     }
     return "NC_ERR_UNKNOWN";
 }
@@ -82,6 +83,29 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
     int* err = error_word();
     if (err == nullptr) return NC_ERR_CUDA;
     const cudaError_t e = nc::launch_fwd(q, k, v, o, lse, B, T, H, D, window, scale, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens, void* o, float* lse,
+                             int n_docs, int total, int max_seqlen, int H, int D, int window, float scale,
+                             cudaStream_t stream) {
+    nc_status st = check_shape(1, total, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (n_docs <= 0 || max_seqlen <= 0 || max_seqlen > total) return NC_ERR_INVALID;
+    if ((int64_t)n_docs * H >= (int64_t(1) << 31)) return NC_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !cu_seqlens || !o || !lse) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return NC_ERR_INVALID;
+    const size_t nb = (size_t)total * H * D * 2, nl = (size_t)H * total * 4, nc_ = (size_t)(n_docs + 1) * 4;
+    const void* ins[4] = {q, k, v, cu_seqlens};
+    const size_t in_n[4] = {nb, nb, nb, nc_};
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_n[i], o, nb) || overlap(ins[i], in_n[i], lse, nl)) return NC_ERR_INVALID;
+    if (overlap(o, nb, lse, nl)) return NC_ERR_INVALID;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const cudaError_t e = nc::launch_fwd_varlen(q, k, v, cu_seqlens, n_docs, max_seqlen, o, lse, total, H, D, window,
+                                                scale, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

@@ -15,6 +15,11 @@ int* device_error_word();
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);
 
+// Document-masked forward over packed rows: q/k/v/o [total,H,D] bf16, lse [H,total] fp32, cu device int32 [n_docs+1].
+cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const int* cu, int n_docs, int max_len,
+                              void* o, float* lse, int total, int H, int D, int window, float scale, int* err,
+                              cudaStream_t st);
+
 // Prefill over a KV cache: q/o [N,Tq,H,D] bf16, lse [N,H,Tq] fp32, caches [N,Tmax,H,D], lens device int32 [N].
 cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
                            float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,

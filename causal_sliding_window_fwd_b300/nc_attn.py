@@ -24,11 +24,13 @@ NC_ERR_WORKSPACE = 3
 NC_ERR_CUDA = 4
 NC_ERR_DEVICE_TIMEOUT = 5
 NC_ERR_BAD_CACHE_LEN = 6
+NC_ERR_BAD_SEQLENS = 7
 NC_WINDOW_FULL = -1
 
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
-            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_get_device_error",
+            "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
+            "nc_get_device_error",
             "nc_launch_count",
             "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
 
@@ -62,6 +64,8 @@ def _load():
     lib.nc_attn_decode.restype = i
     lib.nc_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.nc_attn_prefill.restype = i
+    lib.nc_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.nc_attn_fwd_varlen.restype = i
     lib.nc_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
     lib.nc_get_device_error.restype = i
     lib.nc_launch_count.argtypes = []
@@ -161,6 +165,31 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: fl
     _check(lib.nc_attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
                               N, Tmax, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
                               _stream(q.device, stream)), "nc_attn_decode")
+
+
+def nc_attn_fwd_varlen(q, k, v, cu_seqlens, o, lse, max_seqlen: int, window: int, scale: float,
+                       stream=None) -> None:
+    """Document-masked forward over packed rows q, k, v, o [total,H,D] bf16; lse [H,total] fp32;
+    cu_seqlens int32 [n_docs+1] on the device."""
+    total, H, D = q.shape
+    n_docs = cu_seqlens.shape[0] - 1
+    for name, x in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(x, name, torch.bfloat16, (total, H, D))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (n_docs + 1,))
+    _need(lse, "lse", torch.float32, (H, total))
+    _check(lib.nc_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(o), _ptr(lse), n_docs, total,
+                                  int(max_seqlen), H, D, int(window), float(scale), _stream(q.device, stream)),
+           "nc_attn_fwd_varlen")
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None, stream=None):
+    """Returns (o [total,H,D], lse [H,total])."""
+    total, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    nc_attn_fwd_varlen(q, k, v, cu_seqlens, o, lse, max_seqlen, window, scale, stream)
+    return o, lse
 
 
 def nc_attn_prefill(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, stream=None) -> None:

@@ -59,7 +59,9 @@ typedef enum {
     NC_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than the *_workspace_bytes() figure */
     NC_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed */
     NC_ERR_DEVICE_TIMEOUT = 5, /* device: a pipeline wait ran out of time; outputs are not valid */
-    NC_ERR_BAD_CACHE_LEN = 6   /* device: a decode cache length was outside [1, Tmax]; its rows are NaN */
+    NC_ERR_BAD_CACHE_LEN = 6,  /* device: a decode/prefill cache length was out of range; its rows are NaN */
+    NC_ERR_BAD_SEQLENS = 7     /* device: document bounds (cu_seqlens) out of order, out of range, or a
+                                  document longer than max_seqlen; its rows are not written */
 } nc_status;
 
 #define NC_WINDOW_FULL (-1)
@@ -124,6 +126,26 @@ size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D);
 nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
                          void* o, float* lse, int N, int Tmax, int H, int D, int window, float scale,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Document-masked (varlen) forward over packed rows: pretraining packs
+ * several documents into a row, and each token attends only to earlier
+ * tokens of its own document, inside the window (positions counted from the
+ * document's start).  Document d is rows cu_seqlens[d] .. cu_seqlens[d+1]-1.
+ *   q, k, v     : const bf16 [total, H, D] device
+ *   cu_seqlens  : const int32 [n_docs + 1] device, 0 = cu_seqlens[0] <= ...
+ *                 <= cu_seqlens[n_docs] = total, each document at most
+ *                 max_seqlen rows; a document whose bounds break this sets
+ *                 NC_ERR_BAD_SEQLENS on the device and its rows are not written
+ *   o           : bf16 [total, H, D] device, written
+ *   lse         : fp32 [H, total] device, written
+ * Rows of o and lse that belong to no document (none, if cu_seqlens covers
+ * [0, total)) are not written.  With one document this is nc_attn_fwd with
+ * B = 1, T = total.
+ */
+nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens, void* o,
+                             float* lse, int n_docs, int total, int max_seqlen, int H, int D, int window,
+                             float scale, cudaStream_t stream);
 
 /*
  * Prefill (append) over a KV cache: Tq new tokens per sequence attend over the

@@ -26,7 +26,8 @@ def _declared():
 
 
 def test_header_declares_the_abi():
-    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_prefill", "nc_attn_bwd_workspace_bytes",
+    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
+            "nc_attn_bwd_workspace_bytes",
             "nc_attn_decode_workspace_bytes", "nc_get_device_error", "nc_status_string",
             "nc_launch_count"} <= set(_declared())
 
@@ -168,3 +169,29 @@ def test_prefill_rejects_bad_arguments(lib):
     assert _pre(lib, p) == lib.NC_ERR_INVALID
     p = list(A[:6]); p[3] = p[3] + 2        # lens misaligned
     assert _pre(lib, p) == lib.NC_ERR_INVALID
+
+
+def _fvl(lib, ptrs=None, **kw):
+    a = dict(n_docs=3, total=512, max_seqlen=300, H=2, D=128, window=64, scale=0.1)
+    a.update(kw)
+    p = list(A[:6]) if ptrs is None else ptrs
+    return lib.lib.nc_attn_fwd_varlen(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                                      a["n_docs"], a["total"], a["max_seqlen"], a["H"], a["D"], a["window"],
+                                      ctypes.c_float(a["scale"]), None)
+
+
+def test_fwd_varlen_rejects_bad_arguments(lib):
+    assert lib.status_string(7) == "NC_ERR_BAD_SEQLENS"
+    assert _fvl(lib, n_docs=0) == lib.NC_ERR_INVALID
+    assert _fvl(lib, total=0) == lib.NC_ERR_INVALID
+    assert _fvl(lib, max_seqlen=0) == lib.NC_ERR_INVALID
+    assert _fvl(lib, max_seqlen=513) == lib.NC_ERR_INVALID  # longer than the packed rows
+    assert _fvl(lib, D=32) == lib.NC_ERR_UNSUPPORTED
+    assert _fvl(lib, window=-2) == lib.NC_ERR_INVALID
+    for i in range(6):
+        p = list(A[:6]); p[i] = 0
+        assert _fvl(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[4] = p[0]            # o aliases q
+    assert _fvl(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[3] = p[3] + 2        # cu_seqlens misaligned
+    assert _fvl(lib, p) == lib.NC_ERR_INVALID

@@ -350,6 +350,65 @@ def test_prefill_full_size_sampled(nc, oracle_mod, window):
         assert abs_err(lse[seqs, hh:hh + 1, wl.Tq - tail:], lse_ref) <= LSE_TOL
 
 
+# ---------------------------------------------------------------- document-masked (varlen) attention
+
+
+VARLEN_CASES = [
+    # (doc lengths, H, D, window)
+    ([7], 2, 128, 3),
+    ([1, 1, 130, 0, 257, 5], 2, 128, -1),
+    ([300, 64, 1, 700], 2, 64, 100),
+    ([128, 128, 256, 511, 1], 3, 128, 128),
+    ([1000, 999, 2], 1, 128, 1),
+]
+
+
+def _varlen_inputs(lens, H, D, seed):
+    total = sum(lens)
+    g = workloads.generator(seed, "cuda")
+    q, k, v, dO = (workloads.randn_bf16((total, H, D), g, "cuda") for _ in range(4))
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+    return q, k, v, dO, cu
+
+
+@pytest.mark.parametrize("lens,H,D,window", VARLEN_CASES)
+def test_fwd_varlen_small(nc, oracle_mod, lens, H, D, window):
+    q, k, v, _, cu = _varlen_inputs(lens, H, D, 6000 + sum(lens))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = nc.attn_fwd_varlen(q, k, v, cu, max(lens), window, scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref = oracle_mod.fwd_varlen(q.unsqueeze(0).cpu(), k.unsqueeze(0).cpu(), v.unsqueeze(0).cpu(),
+                                           cu.cpu(), window, scale)
+    assert rel_err(o, o_ref[0]) <= O_TOL
+    assert abs_err(lse, lse_ref[0]) <= LSE_TOL
+
+
+def test_fwd_varlen_single_document_is_the_forward(nc):
+    T, H, D, W = 333, 2, 128, 100
+    q, k, v, _ = workloads.make_qkvdo_shape(1, T, H, D, seed=91, device="cuda")
+    o, lse = nc.attn_fwd(q, k, v, W)
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    ov, lsev = nc.attn_fwd_varlen(q[0], k[0], v[0], cu, T, W)
+    assert nc.nc_get_device_error() == 0
+    assert torch.equal(ov, o[0]) and torch.equal(lsev, lse[0])
+
+
+def test_fwd_varlen_bad_document_reports(nc, oracle_mod):
+    lens = [100, 400, 50]  # the middle document is longer than max_seqlen below
+    q, k, v, _, cu = _varlen_inputs(lens, 2, 128, 97)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((2, sum(lens)), float("nan"), dtype=torch.float32, device="cuda")
+    nc.nc_attn_fwd_varlen(q, k, v, cu, o, lse, 256, -1, 0.1)
+    assert nc.nc_get_device_error() == nc.NC_ERR_BAD_SEQLENS
+    assert torch.isnan(o[100:500].float()).all()  # not written
+    o_ref, lse_ref = oracle_mod.fwd_varlen(q.unsqueeze(0).cpu(), k.unsqueeze(0).cpu(), v.unsqueeze(0).cpu(),
+                                           cu.cpu(), -1, 0.1)
+    for sl in (slice(0, 100), slice(500, 550)):
+        assert rel_err(o[sl], o_ref[0, sl]) <= O_TOL
+        assert abs_err(lse[:, sl], lse_ref[0][:, sl]) <= LSE_TOL
+    assert nc.nc_get_device_error() == 0
+
+
 # ---------------------------------------------------------------- failure detection
 
 
