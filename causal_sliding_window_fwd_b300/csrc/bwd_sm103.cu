@@ -111,6 +111,10 @@ struct BwdParams {
     int n_kb, n_qb;
     int group;             // (batch, head) pairs per scheduling group
     int* work;             // work-item counter, zero on entry
+    // Document-masked backward over packed rows (B = 1, T = total): document d is rows
+    // cu[d] .. cu[d+1]-1; n_kb then counts the key blocks of the longest document.  nullptr otherwise.
+    const int* cu;
+    int n_docs;
     int* err;
 };
 
@@ -121,22 +125,44 @@ struct BwdParams {
 // into groups of p.group (about one wave of CTAs' worth of items); inside a group the index
 // runs over n outermost, so the longest causal walks (small n) go first, while the CTAs that
 // run at the same time share the Q and dO blocks of a few heads in L2.
+// Varlen: the pairs are (document, head), positions count from the document's start, and items past a
+// document's last key block are empty (the producer skips them).
 struct BwdItem {
     int n, h, b, j0, m_lo, n_it;
+    int base;   // first packed row of the document (varlen), else 0
+    int len;    // rows of the sequence or document
+    bool bad;   // the document's bounds are out of range
+    bool empty;
 };
 
+template <bool kVarlen>
 __device__ __forceinline__ BwdItem bwd_item(int w, const BwdParams& p) {
     BwdItem it;
+    const int n_pairs = kVarlen ? p.n_docs * p.H : p.B * p.H;
     const int per_group = p.n_kb * p.group;
     const int grp = w / per_group, r = w - grp * per_group;
-    const int in_grp = min(p.group, p.B * p.H - grp * p.group);  // the last group may be short
+    const int in_grp = min(p.group, n_pairs - grp * p.group);  // the last group may be short
     const int bh = grp * p.group + r % in_grp;
     it.n = r / in_grp;
     it.h = bh % p.H;
-    it.b = bh / p.H;
+    it.b = kVarlen ? 0 : bh / p.H;
     it.j0 = it.n * kBK;
     it.m_lo = it.n;  // kBQ == kBK: query block n holds the first queries at or after key j0
-    const int m_hi = min(p.n_qb - 1, (it.j0 + kBK - 1 + p.W - 1) / kBQ);
+    it.base = 0;
+    it.len = p.T;
+    it.bad = false;
+    it.empty = false;
+    int n_qb = p.n_qb;
+    if (kVarlen) {
+        const int d = bh / p.H;
+        const int a = p.cu[d], e = p.cu[d + 1];
+        it.bad = a < 0 || e < a || e > p.T || e - a > p.n_kb * kBK;
+        it.base = it.bad ? 0 : a;
+        it.len = it.bad ? 0 : e - a;
+        n_qb = (it.len + kBQ - 1) / kBQ;
+        it.empty = it.bad || it.j0 >= it.len;
+    }
+    const int m_hi = min(n_qb - 1, (it.j0 + kBK - 1 + p.W - 1) / kBQ);
     it.n_it = m_hi - it.m_lo + 1;
     return it;
 }
@@ -147,6 +173,29 @@ __device__ __forceinline__ bool aborted(const BwdBarriers* bars) {
 
 __device__ __forceinline__ int publish_item(BwdBarriers* bars, int k, int n_items, int* work) {
     return ring_publish_item(bars->item_full, bars->item_empty, bars->item, k, n_items, work);
+}
+
+// Like publish_item, but takes further indices while they name empty items.
+template <bool kVarlen>
+__device__ __forceinline__ int publish_item_skipping(BwdBarriers* bars, int k, int n_items, const BwdParams& p) {
+    const int slot = k % kItemSlots;
+    if (!mbar_wait_warp(&bars->item_empty[slot], ((k / kItemSlots) & 1) ^ 1)) return -2;
+    int w = 0;
+    if (lane_id() == 0) {
+        for (;;) {
+            w = atomicAdd(p.work, 1);
+            if (w >= n_items) {
+                w = -1;
+                break;
+            }
+            const BwdItem it = bwd_item<kVarlen>(w, p);
+            if (it.bad) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
+            if (!it.empty) break;
+        }
+        bars->item[slot] = w;
+        mbar_arrive(&bars->item_full[slot]);
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
 }
 
 __device__ __forceinline__ int read_item(BwdBarriers* bars, int k) {
@@ -167,7 +216,7 @@ __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, flo
                  : "memory");
 }
 
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -180,7 +229,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* s_delta = reinterpret_cast<float*>(smem + L::kDelta);
 
     const int warp = warp_id(), lane = lane_id();
-    const int n_items = p.n_kb * p.H * p.B;
+    const int n_items = p.n_kb * p.H * (kVarlen ? p.n_docs : p.B);
 
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
@@ -243,13 +292,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             int kv_loads = 0;
             bool ok = true;
             for (int ii = 0; ok; ++ii) {
-                const int w = publish_item(bars, ii, n_items, p.work);
+                // varlen: pass over items past a document's end (and report bad document bounds)
+                // before publishing, so the other roles only ever see items with work
+                const int w = kVarlen ? publish_item_skipping<kVarlen>(bars, ii, n_items, p)
+                                      : publish_item(bars, ii, n_items, p.work);
                 if (w == -2 || aborted(bars)) {
                     ok = false;
                     break;
                 }
                 if (w < 0) break;
-                const BwdItem item = bwd_item(w, p);
+                const BwdItem item = bwd_item<kVarlen>(w, p);
                 // K and V of this item once every product of the previous item has read theirs
                 if (!mbar_wait_warp(&bars->kv_empty, (ii & 1) ^ 1) || aborted(bars)) {
                     ok = false;
@@ -257,8 +309,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 mbar_arrive_expect_tx_w(&bars->kv_full, 2 * L::kTile);
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, item.h, item.j0, item.b);
-                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, item.h, item.j0, item.b);
+                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, item.h,
+                                  item.base + item.j0, item.b);
+                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, item.h,
+                                  item.base + item.j0, item.b);
                 }
                 ++kv_loads;
                 for (int it = 0; it < item.n_it; ++it) {
@@ -271,7 +325,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx_w(&bars->q_full[st], L::kTile);
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64,
-                                      item.h, i0, item.b);
+                                      item.h, item.base + i0, item.b);
                     ++gq;
                     if (!mbar_wait_warp(&bars->do_empty[so], ((gd / L::kDOStages) & 1) ^ 1) || aborted(bars)) {
                         ok = false;
@@ -280,7 +334,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mbar_arrive_expect_tx_w(&bars->do_full[so], L::kTile);
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_4d_w(smem + L::kDO + so * L::kTile + c * kBQ * 128, &tm_do, &bars->do_full[so],
-                                      c * 64, item.h, i0, item.b);
+                                      c * 64, item.h, item.base + i0, item.b);
                     ++gd;
                 }
             }
@@ -339,7 +393,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     break;
                 }
                 if (w < 0) break;
-                const BwdItem item = bwd_item(w, p);
+                const BwdItem item = bwd_item<kVarlen>(w, p);
                 ok = mbar_wait_warp(&bars->kv_full, ii & 1) && !aborted(bars);
                 if (!ok) break;
                 {
@@ -436,9 +490,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // boundaries too): threads 0-63 fetch lse, threads 64-127 fetch Delta
         const bool fetch_lse = tid < 64;
         const int qoff = 64 * g + (tid & 63);
-        auto stat = [&](const BwdItem& item, int i) {
-            if (i >= p.T) return fetch_lse ? INFINITY : 0.f;
-            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T;
+        auto stat = [&](const BwdItem& item, int i) {  // i: row within the sequence / document
+            if (i >= item.len) return fetch_lse ? INFINITY : 0.f;  // past the end: P = 0
+            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T + item.base;
             return fetch_lse ? p.lse[rowvec + i] * kLog2e : p.delta[rowvec + i];
         };
         bool ok = true;
@@ -452,7 +506,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             }
             if (w < 0) break;
-            const BwdItem item = bwd_item(w, p);
+            const BwdItem item = bwd_item<kVarlen>(w, p);
             const int n = item.n, h = item.h, b = item.b, j0 = item.j0;
             const int j = j0 + tid;
             float nx = stat(item, item.m_lo * kBQ + qoff);
@@ -601,6 +655,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
                 const float mul = g ? 1.f : p.scale;
                 uint8_t* tile = g == 0 ? smem + L::kDS : (L::kTmaReduce ? smem + L::kStage : smem + L::kDS + kBK * 128);
+                // a varlen key block that runs past its document's end is written row by row, so the
+                // next document's rows are left alone
+                const bool partial = kVarlen && j0 + kBK > item.len;
+                __nv_bfloat16* grow = (g ? p.dv : p.dk) +
+                                      ((static_cast<size_t>(b) * p.T + item.base + j) * p.H + h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -614,16 +673,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
                         // columns 32c + 8 v4 .. +7: 16-byte unit 4 (c % 2) + v4 of the row's 64-column chunk c / 2
                         const int unit = 4 * (c % 2) + v4;
-                        *reinterpret_cast<uint4*>(tile + (c / 2) * (kBK * 128) + tid * 128 + ((unit ^ (tid & 7)) << 4)) = pkt;
+                        if (partial) {
+                            if (j < item.len) reinterpret_cast<uint4*>(grow + c * 32)[v4] = pkt;
+                        } else {
+                            *reinterpret_cast<uint4*>(tile + (c / 2) * (kBK * 128) + tid * 128 + ((unit ^ (tid & 7)) << 4)) =
+                                pkt;
+                        }
                     }
                 }
                 fence_async_smem();
                 named_bar_sync(1 + g, 128);
                 if (tid == 0) {
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_store_4d(g ? &tm_dv : &tm_dk, tile + c * (kBK * 128), c * 64, h, j0, b);
-                    bulk_commit();
-                    bulk_wait_read();
+                    if (!partial) {
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_store_4d(g ? &tm_dv : &tm_dk, tile + c * (kBK * 128), c * 64, h, item.base + j0, b);
+                        bulk_commit();
+                        bulk_wait_read();
+                    }
                     // the dS tile may be written again (the next item's first dS) once this is set
                     if (g == 0 || !L::kTmaReduce) mbar_arrive(&bars->epi_done);
                 }
@@ -646,8 +712,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             }
             if (w < 0) break;
-            const BwdItem item = bwd_item(w, p);
-            const int h = item.h, b = item.b;
+            const BwdItem item = bwd_item<kVarlen>(w, p);
+            const int h = item.h, b = item.b, base = item.base;
             for (int it = 0; it < item.n_it; ++it, ++gi) {
                 const int i0 = (item.m_lo + it) * kBQ;
                 const bool got = mbar_wait_warp(&bars->dq_full, gi & 1) && !aborted(bars);
@@ -679,7 +745,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         fence_async_smem();
                         named_bar_sync(3, 128);
                         if (tid == 0) {
-                            tma_reduce_add_4d(&tm_dq, stage, 0, h, i0 + 64 * half, b);
+                            // rows past a varlen document's end carry exact zeros (P = 0 there)
+                            tma_reduce_add_4d(&tm_dq, stage, 0, h, base + i0 + 64 * half, b);
                             bulk_commit();
                         }
                     }
@@ -691,7 +758,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 } else {
                     // thread = query row, TMEM columns = the D dQ columns
                     const int i = i0 + tid;
-                    float* dst = p.dq_acc + (static_cast<size_t>(b) * p.T + i) * row_stride + static_cast<size_t>(h) * D;
+                    float* dst =
+                        p.dq_acc + (static_cast<size_t>(b) * p.T + base + i) * row_stride + static_cast<size_t>(h) * D;
                     uint32_t r[64];
                     {
                         uint32_t a[32], c2[32];
@@ -704,7 +772,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     tc_fence_before();
                     mbar_arrive(&bars->dq_empty);
-                    if (i < p.T) {
+                    if (i < item.len) {
 #pragma unroll
                         for (int v4 = 0; v4 < 16; ++v4)
                             red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
@@ -780,10 +848,12 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
     reinterpret_cast<uint4*>(dq)[t] = pkt;
 }
 
+// cu != nullptr: document-masked packed rows (B = 1, T = total), n_docs documents of at most max_len rows.
 template <int D>
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
-                          float scale, float* dq_acc, float* delta, int* work, int* err, cudaStream_t st) {
+                          float scale, float* dq_acc, float* delta, int* work, const int* cu, int n_docs,
+                          int max_len, int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
@@ -806,9 +876,11 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     p.W = (window <= 0 || window >= T) ? T : window;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
-    p.n_kb = (T + kBK - 1) / kBK;
+    p.n_kb = ((cu != nullptr ? max_len : T) + kBK - 1) / kBK;
     p.n_qb = (T + kBQ - 1) / kBQ;
     p.work = work;
+    p.cu = cu;
+    p.n_docs = n_docs;
     p.err = err;
     const int smem = BwdSmem<D>::kBytes;
     static bool attr_set[64] = {false};
@@ -816,7 +888,9 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(bwd_main_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_main_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
@@ -826,13 +900,17 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const long n_items = (long)p.n_kb * H * B;
+    const int n_pairs = (cu != nullptr ? n_docs : B) * H;
+    const long n_items = (long)p.n_kb * n_pairs;
     const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_kb - 1) / p.n_kb;
-    if (p.group > B * H) p.group = B * H;
-    bwd_main_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+    if (p.group > n_pairs) p.group = n_pairs;
+    if (cu != nullptr)
+        bwd_main_kernel<D, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+    else
+        bwd_main_kernel<D, false><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     const size_t n8 = (size_t)rows * D / 8;
     bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
                                                                  scale);
@@ -846,9 +924,19 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
                        float* dq_acc, float* delta, int* work, int* err, cudaStream_t st) {
     return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
-                                         err, st)
+                                         nullptr, 0, 0, err, st)
                     : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
-                                        err, st);
+                                        nullptr, 0, 0, err, st);
+}
+
+cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const int* cu, int n_docs, int max_len, void* dq, void* dk, void* dv,
+                              int total, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
+                              int* err, cudaStream_t st) {
+    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, 1, total, H, window, scale, dq_acc, delta,
+                                         work, cu, n_docs, max_len, err, st)
+                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, 1, total, H, window, scale, dq_acc, delta,
+                                        work, cu, n_docs, max_len, err, st);
 }
 
 }  // namespace nc

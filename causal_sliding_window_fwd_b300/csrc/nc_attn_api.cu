@@ -109,6 +109,46 @@ nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const 
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
+nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv, int n_docs,
+                             int total, int max_seqlen, int H, int D, int window, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    nc_status st = check_shape(1, total, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (n_docs <= 0 || max_seqlen <= 0 || max_seqlen > total) return NC_ERR_INVALID;
+    if ((int64_t)n_docs * H >= (int64_t(1) << 31)) return NC_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o || !dO || !lse || !cu_seqlens || !dq || !dk || !dv) return NC_ERR_INVALID;
+    const void* all[9] = {q, k, v, o, dO, lse, dq, dk, dv};
+    for (const void* p : all)
+        if (!aligned16(p)) return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return NC_ERR_INVALID;
+    const size_t need = nc_attn_bwd_workspace_bytes(1, total, H, D);
+    if (workspace == nullptr || workspace_bytes < need) return NC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return NC_ERR_INVALID;
+    const size_t nb = (size_t)total * H * D * 2, nl = (size_t)H * total * 4, nc_ = (size_t)(n_docs + 1) * 4;
+    const void* ins[7] = {q, k, v, o, dO, lse, cu_seqlens};
+    const size_t in_n[7] = {nb, nb, nb, nb, nb, nl, nc_};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_n[4] = {nb, nb, nb, need};
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 7; ++i)
+            if (overlap(ins[i], in_n[i], outs[a], out_n[a])) return NC_ERR_INVALID;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], out_n[a], outs[b], out_n[b])) return NC_ERR_INVALID;
+    }
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)total * H * D * 4, 256);
+    float* delta = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)H * total * 4, 256);
+    int* work = reinterpret_cast<int*>(ws);
+    const cudaError_t e = nc::launch_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, n_docs, max_seqlen, dq, dk, dv,
+                                                total, H, D, window, scale, dq_acc, delta, work, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens, void* o,
                           float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
                           cudaStream_t stream) {

@@ -20,6 +20,12 @@ cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const
                               void* o, float* lse, int total, int H, int D, int window, float scale, int* err,
                               cudaStream_t st);
 
+// Document-masked backward over packed rows; workspace as for launch_bwd with B = 1, T = total.
+cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const int* cu, int n_docs, int max_len, void* dq, void* dk, void* dv,
+                              int total, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
+                              int* err, cudaStream_t st);
+
 // Prefill over a KV cache: q/o [N,Tq,H,D] bf16, lse [N,H,Tq] fp32, caches [N,Tmax,H,D], lens device int32 [N].
 cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
                            float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,

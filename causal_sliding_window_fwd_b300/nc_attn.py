@@ -30,6 +30,7 @@ NC_WINDOW_FULL = -1
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
             "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
+            "nc_attn_bwd_varlen",
             "nc_get_device_error",
             "nc_launch_count",
             "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
@@ -66,6 +67,8 @@ def _load():
     lib.nc_attn_prefill.restype = i
     lib.nc_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.nc_attn_fwd_varlen.restype = i
+    lib.nc_attn_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_bwd_varlen.restype = i
     lib.nc_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
     lib.nc_get_device_error.restype = i
     lib.nc_launch_count.argtypes = []
@@ -180,6 +183,34 @@ def nc_attn_fwd_varlen(q, k, v, cu_seqlens, o, lse, max_seqlen: int, window: int
     _check(lib.nc_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(o), _ptr(lse), n_docs, total,
                                   int(max_seqlen), H, D, int(window), float(scale), _stream(q.device, stream)),
            "nc_attn_fwd_varlen")
+
+
+def nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen: int, window: int, scale: float,
+                       workspace, stream=None) -> None:
+    """Backward of the document-masked forward into caller-owned dq, dk, dv [total,H,D]."""
+    total, H, D = q.shape
+    n_docs = cu_seqlens.shape[0] - 1
+    for name, x in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(x, name, torch.bfloat16, (total, H, D))
+    _need(lse, "lse", torch.float32, (H, total))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (n_docs + 1,))
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib.nc_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(cu_seqlens),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), n_docs, total, int(max_seqlen), H, D, int(window),
+                                  float(scale), _ptr(workspace), workspace.numel(), _stream(q.device, stream)),
+           "nc_attn_bwd_varlen")
+
+
+def attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None,
+                    workspace=None, stream=None):
+    """Returns (dq, dk, dv), each [total,H,D] bf16."""
+    total, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nc_attn_bwd_workspace_bytes(1, total, H, D), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen, window, scale, workspace, stream)
+    return dq, dk, dv
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None, stream=None):

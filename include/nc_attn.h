@@ -148,6 +148,18 @@ nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const 
                              float scale, cudaStream_t stream);
 
 /*
+ * Backward of nc_attn_fwd_varlen, for the o and lse it produced with the same
+ * arguments.  Shapes as there (dO, dq, dk, dv [total, H, D] bf16, lse
+ * [H, total] fp32); workspace >= nc_attn_bwd_workspace_bytes(1, total, H, D).
+ * Rows that belong to no document get dq = 0 and are not written in dk, dv.
+ * Bad document bounds set NC_ERR_BAD_SEQLENS as in the forward.
+ */
+nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv, int n_docs,
+                             int total, int max_seqlen, int H, int D, int window, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Prefill (append) over a KV cache: Tq new tokens per sequence attend over the
  * cache ("nanochat" walkthrough, page 4: the Engine's prefill/decode split
  * over a KV cache).  The keys and values of the new tokens are already in the

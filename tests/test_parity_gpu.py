@@ -383,6 +383,30 @@ def test_fwd_varlen_small(nc, oracle_mod, lens, H, D, window):
     assert abs_err(lse, lse_ref[0]) <= LSE_TOL
 
 
+@pytest.mark.parametrize("lens,H,D,window", VARLEN_CASES)
+def test_bwd_varlen_small(nc, oracle_mod, lens, H, D, window):
+    q, k, v, dO, cu = _varlen_inputs(lens, H, D, 7000 + sum(lens))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = nc.attn_fwd_varlen(q, k, v, cu, max(lens), window, scale)
+    dq, dk, dv = nc.attn_bwd_varlen(q, k, v, o, dO, lse, cu, max(lens), window, scale)
+    assert nc.nc_get_device_error() == 0
+    refs = oracle_mod.bwd_varlen(q.unsqueeze(0).cpu(), k.unsqueeze(0).cpu(), v.unsqueeze(0).cpu(),
+                                 dO.unsqueeze(0).cpu(), cu.cpu(), window, scale)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        assert rel_err(got, ref[0]) <= G_TOL, name
+
+
+def test_bwd_varlen_single_document_is_the_backward(nc):
+    T, H, D, W = 333, 2, 128, 100
+    q, k, v, dO = workloads.make_qkvdo_shape(1, T, H, D, seed=93, device="cuda")
+    o, lse, dq, dk, dv = run_fwd_bwd(nc, q, k, v, dO, W, 1.0 / math.sqrt(D))
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    dqv, dkv, dvv = nc.attn_bwd_varlen(q[0], k[0], v[0], o[0], dO[0], lse[0], cu, T, W, 1.0 / math.sqrt(D))
+    assert nc.nc_get_device_error() == 0
+    assert torch.equal(dkv, dk[0]) and torch.equal(dvv, dv[0])  # one key block per CTA: a fixed order
+    torch.testing.assert_close(dqv.float(), dq[0].float(), atol=2e-2, rtol=0)  # dQ sums in any order
+
+
 def test_fwd_varlen_single_document_is_the_forward(nc):
     T, H, D, W = 333, 2, 128, 100
     q, k, v, _ = workloads.make_qkvdo_shape(1, T, H, D, seed=91, device="cuda")
