@@ -314,6 +314,7 @@ def run_ours(args, dist: Dist):
     if not args.no_decode:
         out["decode"] = run_decode(dev, stream, nc_attn, peaks, peak_kind)
         out["prefill"] = run_prefill(dev, stream, nc_attn, peaks, peak_kind)
+        out["varlen"] = run_varlen(dev, stream, nc_attn, peaks, peak_kind)
     return out
 
 
@@ -359,6 +360,54 @@ def decode_bytes(lens, wl, window):
     W = wl.Tmax if window <= 0 else window
     rows = sum(min(int(L), W) for L in lens.tolist())
     return rows * wl.H * wl.D * 2 * 2 + wl.N * wl.H * wl.D * 2 * 2 + wl.N * wl.H * 4 + wl.N * 4
+
+
+def run_varlen(dev, stream, nc_attn, peaks, peak_kind):
+    """Document-masked fwd and bwd over packed rows; TFLOP/s of 4*D (fwd), 10*D (bwd) flops per visible pair,
+    L2 flushed before each timed call."""
+    wl = workloads.VARLEN
+    q, k, v, dO, cu, max_len = workloads.make_varlen(wl, dev)
+    total = q.shape[0]
+    lens = (cu[1:] - cu[:-1]).tolist()
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.H, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(1, total, wl.H, wl.D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {"workload": wl.name, "documents": len(lens), "l2": "flushed (256 MB write) before every timed call"}
+
+    def timed(fn, n=15):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            evs = []
+            for _ in range(n):
+                flush.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                fn()
+                e.record(stream)
+                evs.append((s, e))
+            torch.cuda.synchronize()
+        return statistics.median([s.elapsed_time(e) for s, e in evs])
+
+    for window in wl.windows:
+        fwd_ms = timed(lambda: nc_attn.nc_attn_fwd_varlen(q, k, v, cu, o, lse, max_len, window, wl.scale, stream))
+        bwd_ms = timed(lambda: nc_attn.nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu, dq, dk, dv, max_len, window,
+                                                          wl.scale, ws, stream))
+        pairs = wl.H * sum(workloads.pairs_in_window(L, window) for L in lens)
+        fwd_tf = 4.0 * wl.D * pairs / (fwd_ms * 1e-3) / 1e12
+        bwd_tf = 10.0 * wl.D * pairs / (bwd_ms * 1e-3) / 1e12
+        step_tf = 14.0 * wl.D * pairs / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+        key = "w1024" if window > 0 else "full"
+        res[key] = {"window": window, "fwd_us": round(fwd_ms * 1e3, 2), "bwd_us": round(bwd_ms * 1e3, 2),
+                    "fwd_TFLOP_s": round(fwd_tf, 1), "bwd_TFLOP_s": round(bwd_tf, 1),
+                    "TFLOP_s": round(step_tf, 1),
+                    "roofline": {"bound": "tensor", "achieved": round(step_tf, 1), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(step_tf / peaks["bf16_tflops"], 4),
+                                 "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
+    assert nc_attn.nc_get_device_error(stream) == 0
+    return res
 
 
 def run_prefill(dev, stream, nc_attn, peaks, peak_kind):

@@ -117,6 +117,33 @@ PREFILL = PrefillWorkload("prefill N8 Tq2048 H10 D128 Tmax8192 len U[2048,8192] 
                           8, 2048, 8192, 10, 128, 2048, 8192, (1024, WINDOW_FULL), _seed(6, 0))
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """Documents packed into fixed-length rows (document-masked attention over packed rows).
+
+    Document lengths are drawn log-normal (median exp(mu) tokens), clipped to [16, T], and laid
+    one after another; a document that does not fit in what is left of a row is cut there and
+    continues as a new document at the start of the next row."""
+    name: str
+    rows: int
+    T: int
+    H: int
+    D: int
+    mu: float
+    sigma: float
+    windows: tuple
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+# The depth-20 training rows, packed with documents of median ~490 tokens.
+VARLEN = VarlenWorkload("packed documents 16 rows x 2048 H10 D128 lengths lognormal(6.2, 0.9) W{1024,full}",
+                        16, 2048, 10, 128, 6.2, 0.9, (1024, WINDOW_FULL), _seed(7, 0))
+
+
 def generator(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=torch.device(device))
     g.manual_seed(int(seed))
@@ -187,6 +214,31 @@ def prefill_pairs(lens, Tq: int, window: int) -> int:
             i = L - Tq + t
             total += (i + 1) if window <= 0 else min(window, i + 1)
     return total
+
+
+def varlen_doc_lengths(wl: VarlenWorkload) -> list:
+    """Document lengths of the packed rows, in order (they sum to rows * T)."""
+    rng = torch.Generator().manual_seed(wl.seed)
+    out = []
+    for _ in range(wl.rows):
+        left = wl.T
+        while left > 0:
+            x = torch.randn((), generator=rng).item() * wl.sigma + wl.mu
+            L = min(max(int(round(math.exp(x))), 16), wl.T)
+            L = min(L, left)
+            out.append(L)
+            left -= L
+    return out
+
+
+def make_varlen(wl: VarlenWorkload, device="cpu"):
+    """(q, k, v, dO [total,H,D] bf16, cu_seqlens int32 [n_docs+1] on ``device``, max_seqlen)."""
+    lens = varlen_doc_lengths(wl)
+    total = wl.rows * wl.T
+    g = generator(wl.seed + 1, device)
+    q, k, v, dO = (randn_bf16((total, wl.H, wl.D), g, device) for _ in range(4))
+    cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(lens), 0).tolist()), dtype=torch.int32, device=device)
+    return q, k, v, dO, cu, max(lens)
 
 
 def pairs_in_window(T: int, window: int) -> int:

@@ -407,6 +407,27 @@ def test_bwd_varlen_single_document_is_the_backward(nc):
     torch.testing.assert_close(dqv.float(), dq[0].float(), atol=2e-2, rtol=0)  # dQ sums in any order
 
 
+@pytest.mark.parametrize("window", [1024, -1])
+def test_varlen_full_size_sampled(nc, oracle_mod, window):
+    """The packed-documents workload; the oracle checks a few documents on two heads."""
+    wl = workloads.VARLEN
+    q, k, v, dO, cu, max_len = workloads.make_varlen(wl, "cuda")
+    o, lse = nc.attn_fwd_varlen(q, k, v, cu, max_len, window, wl.scale)
+    dq, dk, dv = nc.attn_bwd_varlen(q, k, v, o, dO, lse, cu, max_len, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    lens = (cu[1:] - cu[:-1]).tolist()
+    for d in (0, int(np.argmax(lens)), int(np.argmin(lens)), len(lens) - 1):
+        a, b = int(cu[d]), int(cu[d + 1])
+        for hh in (0, 9):
+            sl = lambda x: x[a:b, hh:hh + 1].unsqueeze(0).cpu()
+            o_ref, lse_ref = oracle_mod.fwd(sl(q), sl(k), sl(v), window, wl.scale)
+            assert rel_err(o[a:b, hh:hh + 1], o_ref[0]) <= O_TOL
+            assert abs_err(lse[hh:hh + 1, a:b], lse_ref[0]) <= LSE_TOL
+            refs = oracle_mod.bwd(sl(q), sl(k), sl(v), sl(dO), window, wl.scale)
+            for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+                assert rel_err(got[a:b, hh:hh + 1], ref[0]) <= G_TOL, name
+
+
 def test_fwd_varlen_single_document_is_the_forward(nc):
     T, H, D, W = 333, 2, 128, 100
     q, k, v, _ = workloads.make_qkvdo_shape(1, T, H, D, seed=91, device="cuda")
