@@ -21,6 +21,7 @@
 // lets one tile's softmax overlap the other tile's products.  The running
 // maximum is only raised (and O rescaled in TMEM) when it grows by more
 // than 2^8, which keeps every exponent bounded and the sum exact.
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -37,6 +38,14 @@ constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per block
 constexpr int kStages = 4;        // K/V ring slots
 constexpr int kThreads = 384;     // 12 warps
+constexpr int kItemReaders = 9;   // warps that read each work-item slot: the MMA warp and 8 softmax warps
+
+// Varlen work-item counters: one {next item, CTAs finished} pair per call, taken round-robin
+// from this ring.  They are zero at load, and the last CTA of each launch zeroes its pair
+// again, so a pair is zero whenever a launch starts with it; calls in flight at the same time
+// (on different streams) use different pairs as long as fewer than kWorkSlots overlap.
+constexpr int kWorkSlots = 4096;
+__device__ int g_fwd_work[kWorkSlots][2];
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -59,6 +68,9 @@ struct FwdBarriers {
     uint64_t o_final;
     uint64_t o_free;
     uint64_t drain;
+    uint64_t item_full[kItemSlots];   // varlen: work-item ring (see nc_sched.cuh)
+    uint64_t item_empty[kItemSlots];
+    int item[kItemSlots];
     uint32_t tmem_base;
     int abort;
 };
@@ -78,6 +90,7 @@ struct FwdParams {
     // and document d is rows cu[d] .. cu[d+1]-1, attending only within itself; nullptr otherwise.
     const int* cu;
     int n_docs;
+    int* work;            // varlen: {next item, CTAs finished}, zero on entry and left zero on exit
     float scale_log2;
     int n_pairs;          // query-tile pairs per (b, h), or per (document, h): the longest document's
     int* err;
@@ -163,6 +176,30 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     return it;
 }
 
+// Varlen producer warp (converged): take item indices from the counter until one has work (reporting
+// bad document bounds on the way) and publish it in slot k % kItemSlots; -1 once all are taken,
+// -2 if the wait for the slot ran out.
+__device__ __forceinline__ int publish_fwd_item(FwdBarriers& bars, int k, int n_items, const FwdParams& p) {
+    const int slot = k % kItemSlots;
+    if (!mbar_wait_warp(&bars.item_empty[slot], ((k / kItemSlots) & 1) ^ 1)) return -2;
+    int w = 0;
+    if (lane_id() == 0) {
+        for (;;) {
+            w = atomicAdd(&p.work[0], 1);
+            if (w >= n_items) {
+                w = -1;
+                break;
+            }
+            const FwdItem it = fwd_item<kModeVarlen>(w, p);
+            if (it.bad) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
+            if (!it.empty) break;
+        }
+        bars.item[slot] = w;
+        mbar_arrive(&bars.item_full[slot]);
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+}
+
 // kMode: the plain forward, prefill over a KV cache (per-sequence query offsets from p.lens), or
 // document-masked packed rows (per-document row bases from p.cu).  Varlen work items past a
 // document's end are skipped by every role alike; `ip` counts the items a role really ran and
@@ -192,6 +229,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&bars.o_final, 1);
         mbar_init(&bars.o_free, 2 * kBM);
         mbar_init(&bars.drain, 1);
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(&bars.item_full[s], 1);
+            mbar_init(&bars.item_empty[s], kItemReaders);
+        }
         bars.abort = 0;
         fence_barrier_init();
     }
@@ -222,8 +263,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int seq = 0;          // K/V loads issued over all items (ring position)
         int q_loads = 0;
         bool ok = true;
-        for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem it = fwd_item<kMode>(sched_item_index(ii), p);
+        const int n_items = p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B);
+        for (int ii = 0; ok; ++ii) {
+            // plain / prefill: the static zigzag schedule; varlen: items with work, from the counter
+            int w;
+            if (kMode == kModeVarlen) {
+                w = publish_fwd_item(bars, ii, n_items, p);
+                if (w == -2 || aborted(bars)) {
+                    ok = false;
+                    break;
+                }
+                if (w < 0) break;
+            } else {
+                if (ii >= my_items) break;
+                w = sched_item_index(ii);
+            }
+            const FwdItem it = fwd_item<kMode>(w, p);
             if (it.empty) {
                 if (it.bad && lane == 0) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
                 continue;
@@ -255,6 +310,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
         }
         if (!ok) record_timeout(bars, p.err);
+        if (kMode == kModeVarlen && lane == 0) {
+            // this CTA takes no more items: the last CTA to get here zeroes the counter pair
+            __threadfence();
+            if (atomicAdd(&p.work[1], 1) == static_cast<int>(gridDim.x) - 1) {
+                p.work[0] = 0;
+                p.work[1] = 0;
+                __threadfence();
+            }
+        }
+        __syncwarp();
         // never leave while a copy into this CTA's shared memory may still land: only the
         // last use of each slot (and of Q) can still be outstanding
         for (int x = seq - kStages < 0 ? 0 : seq - kStages; x < seq; ++x)
@@ -300,8 +365,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int seq = 0;                 // K/V ring position over all items
             int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
             int ip = 0;                  // items run
-            for (int ii = 0; ok && ii < my_items; ++ii) {
-                const FwdItem it = fwd_item<kMode>(sched_item_index(ii), p);
+            for (int ii = 0; ok; ++ii) {
+                int w;
+                if (kMode == kModeVarlen) {
+                    w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
+                    if (w == -2) {
+                        ok = false;
+                        break;
+                    }
+                    if (w < 0) break;
+                } else {
+                    if (ii >= my_items) break;
+                    w = sched_item_index(ii);
+                }
+                const FwdItem it = fwd_item<kMode>(w, p);
                 if (it.empty) continue;
                 auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
                 ok = mbar_wait_warp(&bars.q_full, ip & 1);
@@ -383,8 +460,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         int n_s = 0;  // S tiles of this query tile consumed over all items
         int ip = 0;   // items run
-        for (int ii = 0; ok && ii < my_items; ++ii) {
-            const FwdItem item = fwd_item<kMode>(sched_item_index(ii), p);
+        for (int ii = 0; ok; ++ii) {
+            int w;
+            if (kMode == kModeVarlen) {
+                w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
+                if (w == -2) {
+                    ok = false;
+                    break;
+                }
+                if (w < 0) break;
+            } else {
+                if (ii >= my_items) break;
+                w = sched_item_index(ii);
+            }
+            const FwdItem item = fwd_item<kMode>(w, p);
             if (item.empty) continue;
             const int tr0 = t ? item.r0[1] : item.r0[0];
             const int t_lo = t ? item.lo[1] : item.lo[0];
@@ -538,6 +627,7 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.lens = lens;
     p.cu = cu;
     p.n_docs = n_docs;
+    p.work = nullptr;
     p.H = H;
     p.W = (window <= 0 || window >= Tk) ? Tk : window;
     p.scale_log2 = scale * kLog2e;
@@ -566,6 +656,19 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     const long n_items = (long)p.n_pairs * H * (cu != nullptr ? n_docs : B);
     const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
+    if (cu != nullptr) {
+        static int* work_base[64] = {nullptr};
+        static std::atomic<unsigned> work_seq{0};
+        int* wb = dev < 64 ? work_base[dev] : nullptr;
+        if (wb == nullptr) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_fwd_work);
+            if (e != cudaSuccess) return e;
+            wb = static_cast<int*>(ptr);
+            if (dev < 64) work_base[dev] = wb;
+        }
+        p.work = wb + 2 * (work_seq.fetch_add(1u) % kWorkSlots);
+    }
     if (cu != nullptr)
         fwd_tc_kernel<D, kModeVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
     else if (lens != nullptr)
