@@ -1,0 +1,461 @@
+// Deterministic dQ pass of the backward on 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Operation (see include/nc_attn.h, nc_attn_bwd_deterministic): the same gradient as the main
+// backward, dQ_i = scale * sum_j dS_ij k_j with dS = P * (dP - Delta), but every 128-row query
+// block is owned by one CTA that walks its key blocks in a fixed order and accumulates dQ in TMEM.
+// The result therefore does not depend on which CTA runs when (the main backward adds the
+// partials of different key blocks with reduce-adds in whatever order they arrive).  The pass
+// recomputes S = Q K^T and dP = dO V^T for every visible (query block, key block) pair: two
+// products more per pair than the main pass, which in this mode computes only dK and dV.
+//
+// Persistent CTAs (one per SM, 384 threads).  A work item is one query block m of one
+// (batch, head); the producer warp takes item indices from a global counter and publishes them
+// in a shared-memory ring.  Indices run over groups of about one wave of items; inside a group
+// m runs outermost from the last block down (the longest causal walks first), so the CTAs that
+// run at the same time read the K and V of a few heads and share them in L2.  Warp roles:
+//   warp 0      TMA producer: Q and dO of the item once, then K and V blocks through a 2-slot ring
+//   warp 1      MMA issuer (one lane) and TMEM owner
+//   warps 4-7   one thread per query row, key columns [0, 64): P, dS; then dQ columns [0, D/2)
+//   warps 8-11  the same for key columns [64, 128); then dQ columns [D/2, D)
+// TMEM: ST [0,128) holds S; DP0 [128,256) and DP1 [384,512) hold dP of alternate key blocks,
+// then dS packed as bf16 over the columns each warpgroup has already read (the A operand of
+// dQ += dS K); DQ [256,256+D) accumulates dQ.
+// Products for key block j, once dS(j) is in TMEM: S(j+1) into ST and dP(j+1) into the other DP
+// region (so the P/dS warps can start on block j+1 at once), then dQ += dS(j) K(j).
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "nc_attn.h"
+#include "nc_kernels.h"
+#include "nc_ptx.cuh"
+#include "nc_sched.cuh"
+#include "nc_tma.h"
+
+namespace nc {
+namespace {
+
+constexpr int kBQ = 128;        // query rows per block
+constexpr int kBK = 128;        // keys per block
+constexpr int kKVStages = 2;    // K/V ring slots (a slot holds one K and one V block)
+constexpr int kThreads = 384;
+constexpr int kItemReaders = 9; // warps that read each work-item slot: the MMA warp and 8 P/dS warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DqSmem {
+    static constexpr int kTile = kBQ * D * 2;  // one 128-row bf16 tile
+    static constexpr int kQ = 0;
+    static constexpr int kDO = kQ + kTile;
+    static constexpr int kKV = kDO + kTile;    // slot s: K at kKV + 2 s kTile, V right after
+    static constexpr int kBytes = kKV + kKVStages * 2 * kTile;
+};
+
+struct DqBarriers {
+    uint64_t kv_full[kKVStages];
+    uint64_t kv_empty[kKVStages];
+    uint64_t q_full;
+    uint64_t q_empty;
+    uint64_t s_full;
+    uint64_t dp_full;
+    uint64_t ds_full;
+    uint64_t dq_final;
+    uint64_t drain;
+    uint64_t item_full[kItemSlots];
+    uint64_t item_empty[kItemSlots];
+    int item[kItemSlots];
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct DqParams {
+    const float* lse;    // [B, H, T]
+    const float* delta;  // [B, H, T]
+    __nv_bfloat16* dq;   // [B, T, H, D]
+    int B, T, H, W;      // W effective, 1 <= W <= T
+    float scale, scale_log2;
+    int n_qb;
+    int group;           // (batch, head) pairs per scheduling group
+    int* work;           // work-item counter, zero on entry
+    int* err;
+};
+
+// One item: query block m of one (batch, head) and the key blocks n_lo .. m that its window reaches.
+struct DqItem {
+    int m, h, b, n_lo;
+};
+
+__device__ __forceinline__ DqItem dq_item(int w, const DqParams& p) {
+    DqItem it;
+    const int n_pairs = p.B * p.H;
+    const int per_group = p.n_qb * p.group;
+    const int grp = w / per_group, r = w - grp * per_group;
+    const int in_grp = min(p.group, n_pairs - grp * p.group);  // the last group may be short
+    const int bh = grp * p.group + r % in_grp;
+    it.m = p.n_qb - 1 - r / in_grp;
+    it.h = bh % p.H;
+    it.b = bh / p.H;
+    // the earliest key any row of the block sees is m*128 - W + 1; key block n holds one of
+    // those keys iff n*128 + 127 >= m*128 - W + 1
+    const int x = it.m * kBQ - p.W - (kBK - 2);
+    it.n_lo = x <= 0 ? 0 : (x + kBK - 1) / kBK;
+    return it;
+}
+
+__device__ __forceinline__ bool aborted(const DqBarriers& bars) {
+    return *reinterpret_cast<const volatile int*>(&bars.abort) != 0;
+}
+
+__device__ __forceinline__ void record_timeout(DqBarriers& bars, int* err) {
+    set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
+    atomicExch(&bars.abort, 1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const DqParams p) {
+    using L = DqSmem<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ DqBarriers bars;
+    const int warp = warp_id(), lane = lane_id();
+    const int n_items = p.n_qb * p.H * p.B;
+
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kKVStages; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.ds_full, 2 * kBQ);
+        mbar_init(&bars.dq_final, 1);
+        mbar_init(&bars.drain, 1);
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(&bars.item_full[s], 1);
+            mbar_init(&bars.item_empty[s], kItemReaders);
+        }
+        bars.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    constexpr uint32_t kColST = 0, kColDQ = 256;
+    auto col_dp = [](int gj) -> uint32_t { return (gj & 1) ? 384u : 128u; };
+
+    // registers: 384 threads x 168 at launch = 128 x 72 (producer / MMA warpgroup) + 256 x 216 (P/dS)
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        // the whole warp runs this loop converged; lane 0 issues each copy
+        regs_decrease<72>();
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+        }
+        __syncwarp();
+        int seq = 0, q_loads = 0;
+        bool ok = true;
+        for (int ii = 0; ok; ++ii) {
+            const int w = ring_publish_item(bars.item_full, bars.item_empty, bars.item, ii, n_items, p.work);
+            if (w == -2 || aborted(bars)) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;
+            const DqItem it = dq_item(w, p);
+            // Q and dO of this item once the previous item's S and dP products have read theirs
+            if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx_w(&bars.q_full, 2 * L::kTile);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_4d_w(smem + L::kQ + c * kBQ * 128, &tm_q, &bars.q_full, c * 64, it.h, it.m * kBQ, it.b);
+                tma_load_4d_w(smem + L::kDO + c * kBQ * 128, &tm_do, &bars.q_full, c * 64, it.h, it.m * kBQ, it.b);
+            }
+            ++q_loads;
+            for (int n = it.n_lo; n <= it.m; ++n, ++seq) {
+                const int slot = seq % kKVStages;
+                if (!mbar_wait_warp(&bars.kv_empty[slot], ((seq / kKVStages) & 1) ^ 1) || aborted(bars)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* kdst = smem + L::kKV + slot * 2 * L::kTile;
+                mbar_arrive_expect_tx_w(&bars.kv_full[slot], 2 * L::kTile);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_4d_w(kdst + c * kBK * 128, &tm_k, &bars.kv_full[slot], c * 64, it.h, n * kBK, it.b);
+                    tma_load_4d_w(kdst + L::kTile + c * kBK * 128, &tm_v, &bars.kv_full[slot], c * 64, it.h,
+                                  n * kBK, it.b);
+                }
+            }
+        }
+        if (!ok) record_timeout(bars, p.err);
+        // never leave while a copy into this CTA's shared memory may still land: the last use of
+        // each slot is the only one whose completion can still be outstanding
+        for (int x = seq - kKVStages < 0 ? 0 : seq - kKVStages; x < seq; ++x)
+            mbar_wait_warp(&bars.kv_full[x % kKVStages], (x / kKVStages) & 1);
+        if (q_loads > 0) mbar_wait_warp(&bars.q_full, (q_loads - 1) & 1);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // the whole warp runs this loop converged; lane 0 issues each product
+        regs_decrease<72>();
+        constexpr uint32_t id_qk = idesc_bf16(kBQ, kBK, false, false);  // S, dP (both operands K-major)
+        constexpr uint32_t id_dq = idesc_bf16(kBQ, D, false, true);     // dQ (A from TMEM, B MN-major)
+        const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO), sKV = smem_u32(smem + L::kKV);
+        // descriptors are built once; each product adds a constant (bytes / 16) to the start field
+        const uint64_t q_kmaj = sdesc(sQ, 16, 1024), do_kmaj = sdesc(sDO, 16, 1024);
+        const uint64_t kv_kmaj = sdesc(sKV, 16, 1024), k_mn = sdesc(sKV, kBK * 128, 1024);
+        constexpr uint64_t kTileStep = L::kTile >> 4;
+        constexpr uint64_t kChunk = (kBQ * 128) >> 4;
+        auto issue_s_dp = [&](int slot, uint32_t dp_col) {
+            const uint64_t kd = kv_kmaj + 2 * slot * kTileStep, vd = kd + kTileStep;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T into ST
+                const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                mma_ss_w(tmem + kColST, q_kmaj + off, kd + off, id_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bars.s_full);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T into a DP region
+                const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                mma_ss_w(tmem + dp_col, do_kmaj + off, vd + off, id_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bars.dp_full);
+        };
+        bool ok = true;
+        int seq = 0, gj = 0;  // K/V ring position; key blocks processed over all items (barrier phases)
+        for (int ii = 0; ok; ++ii) {
+            const int w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
+            if (w == -2) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;
+            const DqItem it = dq_item(w, p);
+            ok = mbar_wait_warp(&bars.q_full, ii & 1) &&
+                 mbar_wait_warp(&bars.kv_full[seq % kKVStages], (seq / kKVStages) & 1) && !aborted(bars);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s_dp(seq % kKVStages, col_dp(gj));
+            if (it.n_lo == it.m) mma_commit_w(&bars.q_empty);  // every S and dP of this item is issued
+            for (int n = it.n_lo; n <= it.m; ++n, ++seq, ++gj) {
+                const int slot = seq % kKVStages;
+                // dS(j) is in TMEM, and S(j) and dP(j) have been read
+                ok = mbar_wait_warp(&bars.ds_full, gj & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                if (n < it.m) {
+                    const int slot1 = (seq + 1) % kKVStages;
+                    ok = mbar_wait_warp(&bars.kv_full[slot1], ((seq + 1) / kKVStages) & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s_dp(slot1, col_dp(gj + 1));
+                    if (n + 1 == it.m) mma_commit_w(&bars.q_empty);
+                }
+                // dQ += dS K(j)  (A = dS packed in DP: keys 0-63 in columns [0,32), 64-127 in [64,96)).
+                // The first product of an item overwrites DQ; the P/dS warps read the previous
+                // item's DQ out before their dS arrivals for this item.
+                const uint64_t kmn = k_mn + 2 * slot * kTileStep;
+                const uint32_t a = tmem + col_dp(gj);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_ts_w(tmem + kColDQ, a + pc, kmn + kk * (2048 >> 4), id_dq, (n > it.n_lo || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_w(&bars.kv_empty[slot]);  // K(j) and V(j): S, dP and dQ were their readers
+            }
+            if (!ok) break;
+            mma_commit_w(&bars.dq_final);
+        }
+        if (!ok) record_timeout(bars, p.err);
+        mma_commit_w(&bars.drain);
+        mbar_wait_warp(&bars.drain, 0);
+    } else if (warp < 4) {
+        regs_decrease<72>();
+    } else {
+        // ------------------------------------------------------------ P and dS (thread = query row)
+        regs_increase<216>();
+        const int g = (warp - 4) / 4;  // key columns [64 g, 64 g + 64)
+        const int tid = threadIdx.x - 128 * (g + 1);
+        const uint32_t lanes = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        int gj = 0;
+        for (int ii = 0; ok; ++ii) {
+            const int w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
+            if (w == -2) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;
+            const DqItem item = dq_item(w, p);
+            const int i = item.m * kBQ + tid;  // this thread's query row
+            const bool row_ok = i < p.T;
+            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T;
+            // past the last row: lse = inf, so P = 0 and dS = 0
+            const float lse_l2 = row_ok ? p.lse[rowvec + i] * kLog2e : INFINITY;
+            const float dlt = row_ok ? p.delta[rowvec + i] : 0.f;
+            for (int n = item.n_lo; n <= item.m; ++n, ++gj) {
+                ok = mbar_wait_warp(&bars.s_full, gj & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                // P in bf16, two per word: dS uses the same rounding of P as the main pass's dK
+                uint32_t pp[32];
+                {
+                    uint32_t a[32], b2[32];
+                    tmem_ld32x2(tmem + lanes + kColST + 64 * g, tmem + lanes + kColST + 64 * g + 32, a, b2);
+                    const int j0 = n * kBK + 64 * g;
+                    const bool full = (n < item.m) && (item.m * kBQ + kBQ - 1 - n * kBK < p.W);
+#pragma unroll
+                    for (int x = 0; x < 64; x += 2) {
+                        const float s0 = __uint_as_float(x < 32 ? a[x] : b2[x - 32]);
+                        const float s1 = __uint_as_float(x < 32 ? a[x + 1] : b2[x - 31]);
+                        float e0, e1;
+                        fma_f32x2(e0, e1, s0, s1, sl2, sl2, -lse_l2, -lse_l2);
+                        float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                        if (!full) {
+                            const int j = j0 + x;
+                            if (j > i || i - j >= p.W) p0 = 0.f;
+                            if (j + 1 > i || i - (j + 1) >= p.W) p1 = 0.f;
+                        }
+                        pp[x / 2] = pack_bf16x2(p0, p1);
+                    }
+                }
+                ok = mbar_wait_warp(&bars.dp_full, gj & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dp_addr = tmem + lanes + col_dp(gj) + 64 * g;
+                {
+                    uint32_t a[32], b2[32];
+                    tmem_ld32x2(dp_addr, dp_addr + 32, a, b2);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int x = 0; x < 32; x += 2) {
+                            const uint32_t wp = pp[16 * c + x / 2];
+                            float t0, t1, d0, d1;
+                            add_f32x2(t0, t1, __uint_as_float(c ? b2[x] : a[x]),
+                                      __uint_as_float(c ? b2[x + 1] : a[x + 1]), -dlt, -dlt);
+                            mul_f32x2(d0, d1, __uint_as_float(wp << 16), __uint_as_float(wp & 0xffff0000u), t0, t1);
+                            pk[x / 2] = pack_bf16x2(d0, d1);
+                        }
+                        // dS (bf16) over this warpgroup's already-read DP columns
+                        tmem_st16(dp_addr + 16 * c, pk);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars.ds_full);
+            }
+            if (!ok) break;
+            // epilogue: dq = bf16(scale * DQ); warpgroup g writes dQ columns [g D/2, (g+1) D/2) of
+            // its row (a whole 128-byte line for D = 128)
+            ok = mbar_wait_warp(&bars.dq_final, ii & 1) && !aborted(bars);
+            if (!ok) break;
+            tc_fence_after();
+            __nv_bfloat16* drow =
+                p.dq + ((static_cast<size_t>(item.b) * p.T + (row_ok ? i : 0)) * p.H + item.h) * D + g * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lanes + kColDQ + g * (D / 2) + c * 32, r);
+                if (row_ok) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 pkt;
+                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * p.scale,
+                                            __uint_as_float(r[8 * v4 + 1]) * p.scale);
+                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * p.scale,
+                                            __uint_as_float(r[8 * v4 + 3]) * p.scale);
+                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * p.scale,
+                                            __uint_as_float(r[8 * v4 + 5]) * p.scale);
+                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * p.scale,
+                                            __uint_as_float(r[8 * v4 + 7]) * p.scale);
+                        reinterpret_cast<uint4*>(drow + c * 32)[v4] = pkt;
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+        if (!ok) record_timeout(bars, p.err);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                         const float* delta, void* dq, int B, int T, int H, int window, float scale, int* work,
+                         int* err, cudaStream_t st) {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
+        !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ))
+        return cudaErrorInvalidValue;
+    DqParams p;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.W = (window <= 0 || window >= T) ? T : window;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.n_qb = (T + kBQ - 1) / kBQ;
+    p.work = work;
+    p.err = err;
+    const int smem = DqSmem<D>::kBytes;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set[dev] = true;
+    }
+    static int sms[64] = {0};
+    if (dev < 64 && sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int n_pairs = B * H;
+    const long n_items = (long)p.n_qb * n_pairs;
+    const int n_sm = dev < 64 ? sms[dev] : 148;
+    const int grid = (int)(n_items < n_sm ? n_items : n_sm);
+    // a scheduling group holds about one wave of items
+    p.group = (n_sm + p.n_qb - 1) / p.n_qb;
+    if (p.group > n_pairs) p.group = n_pairs;
+    bwd_dq_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                          const float* delta, void* dq, int B, int T, int H, int D, int window, float scale, int* work,
+                          int* err, cudaStream_t st) {
+    return D == 128 ? launch_dq_tc<128>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, err, st)
+                    : launch_dq_tc<64>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, err, st);
+}
+
+}  // namespace nc

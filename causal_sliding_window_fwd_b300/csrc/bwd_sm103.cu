@@ -216,7 +216,8 @@ __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, flo
                  : "memory");
 }
 
-template <int D, bool kVarlen>
+// kNoDq: dK and dV only (the deterministic backward computes dQ in a separate pass).
+template <int D, bool kVarlen, bool kNoDq = false>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -403,7 +404,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(st);
-                    ok = (gi == 0 || mbar_wait_warp(&bars->dq_empty, (gi - 1) & 1)) &&
+                    ok = (kNoDq || gi == 0 || mbar_wait_warp(&bars->dq_empty, (gi - 1) & 1)) &&
                          mbar_wait_warp(&bars->do_full[so], (gi / L::kDOStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
@@ -437,7 +438,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     mma_commit_w(&bars->q_empty[st]);  // Q of this block: S^T and dK were its readers
                     // dQ of this block into DPT (issued after dK, which read dS^T from DPT)
-                    if constexpr (D == 128) {
+                    if constexpr (kNoDq) {
+                    } else if constexpr (D == 128) {
                         // dQ_m^T = K^T dS^T  (M = D lanes, N = queries, K = keys)
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -450,7 +452,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             mma_ss_w(tmem + kColDPT, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), id_qd,
                                      kk > 0 ? 1u : 0u);
                     }
-                    mma_commit_w(&bars->dq_full);
+                    if (!kNoDq) mma_commit_w(&bars->dq_full);
                     if (it + 1 < item.n_it) {
                         // next block: S^T into ST right away (dV above was the last reader of P^T);
                         // dP^T into DPT once this block's dQ has been read out
@@ -459,7 +461,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(st1);
-                        ok = mbar_wait_warp(&bars->dq_empty, gi & 1) &&
+                        ok = (kNoDq || mbar_wait_warp(&bars->dq_empty, gi & 1)) &&
                              mbar_wait_warp(&bars->do_full[so1], ((gi + 1) / L::kDOStages) & 1) && !aborted(bars);
                         if (!ok) break;
                         tc_fence_after();
@@ -584,7 +586,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok = mbar_wait_warp(&bars->dp_full, gi & 1) && !aborted(bars);
                 // the first dS of an item goes where the previous item's dK (and for D = 64 dV)
                 // tile was staged: wait until those TMA stores have read it
-                if (ok && it == 0 && ii > 0) ok = mbar_wait_warp(&bars->epi_done, (ii - 1) & 1) && !aborted(bars);
+                // (without the dQ product the dS tile is not written, and the epilogues alone use it)
+                if (!kNoDq && ok && it == 0 && ii > 0)
+                    ok = mbar_wait_warp(&bars->epi_done, (ii - 1) & 1) && !aborted(bars);
                 if (!ok) continue;
                 tc_fence_after();
                 uint32_t drr[64];
@@ -620,7 +624,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tmem_st16(dpt_addr + 64 * g + 16 * c, dk);
                     // dS row into the [key][query] tile: query chunk g, 16-byte units 4c .. 4c+3
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < (kNoDq ? 0 : 4); ++u) {
                         const int unit = 4 * c + u;
                         uint4 v;
                         v.x = dk[4 * u + 0];
@@ -644,7 +648,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // warpgroup 0 uses the dS tile (free once final_ has landed: dQ and dK were its last
             // readers); for D = 128 warpgroup 1 uses the dQ staging tile once the last reduce-add
             // of this item has read it, for D = 64 the second half of the dS tile
-            if (g == 1 && L::kTmaReduce && ok) ok = mbar_wait_warp(&bars->stage_free, ii & 1) && !aborted(bars);
+            if (g == 1 && L::kTmaReduce && !kNoDq && ok)
+                ok = mbar_wait_warp(&bars->stage_free, ii & 1) && !aborted(bars);
             if (!named_bar_and(1 + g, 128, ok)) {  // leave together
                 ok = false;
                 record_timeout(bars, p.err);
@@ -698,6 +703,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else {
         // ------------------------------------------------------------ dQ partials into the fp32 accumulator
         regs_increase<152>();
+        if constexpr (kNoDq) {
+            // no dQ product: these warps only keep reading the item ring so that its slots are released
+            for (int ii = 0;; ++ii) {
+                const int w = read_item(bars, ii);
+                if (w == -2) record_timeout(bars, p.err);
+                if (w < 0) break;
+            }
+        } else {
         const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
@@ -784,6 +797,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if constexpr (L::kTmaReduce) {
             if (tid == 0) bulk_wait_all();  // every reduce-add has landed before the CTA exits
         }
+        }
     }
     if (warp >= 4 && warp < 12 && (threadIdx.x & 127) == 0) bulk_wait_all();  // epilogue stores have landed
     tc_fence_before();
@@ -794,7 +808,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-// Delta = rowsum(dO * O) per (b, h, i) and a zeroed dQ accumulator.
+// Delta = rowsum(dO * O) per (b, h, i), a zeroed dQ accumulator (unless dq_acc is null) and zeroed
+// work-item counters (work[0] for the main kernel, work[1] for the deterministic dQ pass).
 // D / 8 lanes per row, each with one 16-byte load of O and of dO.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
@@ -807,7 +822,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const long row = (tid_g >> 5) * RPW + ((threadIdx.x & 31) / G);
     const int c = threadIdx.x % G;
     const long rows = (long)B * T * H;
-    if (tid_g == 0) *work = 0;  // the main kernel's work-item counter
+    if (tid_g == 0) {
+        work[0] = 0;
+        work[1] = 0;
+    }
     float acc = 0.f;
     if (row < rows) {
         const uint4 a = reinterpret_cast<const uint4*>(o + (size_t)row * D)[c];
@@ -819,9 +837,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
             const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(g2[e]);
             acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
         }
-        float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D + c * 8);
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (dq_acc != nullptr) {
+            float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D + c * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -849,11 +869,12 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
 }
 
 // cu != nullptr: document-masked packed rows (B = 1, T = total), n_docs documents of at most max_len rows.
+// deterministic: dK and dV from the main kernel, dQ from the query-stationary pass (no dQ accumulator).
 template <int D>
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int window,
                           float scale, float* dq_acc, float* delta, int* work, const int* cu, int n_docs,
-                          int max_len, int* err, cudaStream_t st) {
+                          int max_len, int* err, cudaStream_t st, bool deterministic = false) {
     CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
@@ -863,7 +884,8 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     const long rows = (long)B * T * H;
     const long pre_threads = ((rows * (D / 8) + 31) / 32) * 32;
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta, dq_acc, work, B, T, H);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta,
+        deterministic ? nullptr : dq_acc, work, B, T, H);
     BwdParams p;
     p.lse = lse;
     p.delta = delta;
@@ -891,6 +913,9 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         e = cudaFuncSetAttribute(bwd_main_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_main_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_main_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
@@ -907,6 +932,13 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_kb - 1) / p.n_kb;
     if (p.group > n_pairs) p.group = n_pairs;
+    if (deterministic) {
+        bwd_main_kernel<D, false, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
+        count_launches(2);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_bwd_dq(q, k, v, dO, lse, delta, dq, B, T, H, D, window, scale, work + 1, err, st);
+    }
     if (cu != nullptr)
         bwd_main_kernel<D, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     else
@@ -937,6 +969,16 @@ cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const
                                          work, cu, n_docs, max_len, err, st)
                     : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, 1, total, H, window, scale, dq_acc, delta,
                                         work, cu, n_docs, max_len, err, st);
+}
+
+cudaError_t launch_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                     const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int D,
+                                     int window, float scale, float* dq_acc, float* delta, int* work, int* err,
+                                     cudaStream_t st) {
+    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
+                                         nullptr, 0, 0, err, st, true)
+                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
+                                        nullptr, 0, 0, err, st, true);
 }
 
 }  // namespace nc

@@ -177,9 +177,10 @@ size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D) {
     return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256) + 256;
 }
 
-nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                      void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
-                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+static nc_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int D, int window,
+                          float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                          bool deterministic) {
     nc_status st = check_shape(B, T, H, D, window, scale);
     if (st != NC_OK) return st;
     if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return NC_ERR_INVALID;
@@ -208,9 +209,27 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
     float* delta = reinterpret_cast<float*>(ws);
     ws += round_up((size_t)B * H * T * 4, 256);
     int* work = reinterpret_cast<int*>(ws);
-    const cudaError_t e = nc::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc, delta,
-                                         work, err, stream);
+    const cudaError_t e =
+        deterministic ? nc::launch_bwd_deterministic(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc,
+                                                     delta, work, err, stream)
+                      : nc::launch_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, dq_acc, delta,
+                                       work, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, workspace, workspace_bytes, stream,
+                    false);
+}
+
+nc_status nc_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                    const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int D,
+                                    int window, float scale, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    return attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, D, window, scale, workspace, workspace_bytes, stream,
+                    true);
 }
 
 size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D) {

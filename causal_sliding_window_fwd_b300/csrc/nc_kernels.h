@@ -36,4 +36,17 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
                        float* dq_acc, float* delta, int* work, int* err, cudaStream_t st);
 
+// Deterministic backward: dK and dV from the main kernel without its dQ product, then dq from the
+// query-stationary pass (launch_bwd_dq).  Workspace as for launch_bwd (dq_acc is not touched).
+cudaError_t launch_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                     const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int D,
+                                     int window, float scale, float* dq_acc, float* delta, int* work, int* err,
+                                     cudaStream_t st);
+
+// Query-stationary dQ pass: dq [B,T,H,D] bf16 from q, k, v, dO, lse and delta [B,H,T] fp32.
+// `work` is a work-item counter that must be zero when the kernel starts.
+cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                          const float* delta, void* dq, int B, int T, int H, int D, int window, float scale, int* work,
+                          int* err, cudaStream_t st);
+
 }  // namespace nc

@@ -29,6 +29,7 @@ NC_WINDOW_FULL = -1
 
 # Entry points declared in include/nc_attn.h.
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
+            "nc_attn_bwd_deterministic",
             "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
             "nc_attn_bwd_varlen",
             "nc_get_device_error",
@@ -59,6 +60,8 @@ def _load():
     lib.nc_attn_bwd_workspace_bytes.restype = sz
     lib.nc_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_bwd.restype = i
+    lib.nc_attn_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_bwd_deterministic.restype = i
     lib.nc_attn_decode_workspace_bytes.argtypes = [i, i, i, i]
     lib.nc_attn_decode_workspace_bytes.restype = sz
     lib.nc_attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
@@ -144,14 +147,24 @@ def nc_attn_fwd(q, k, v, o, lse, window: int, scale: float, stream=None) -> None
 
 def nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace, stream=None) -> None:
     """Backward into caller-owned dq, dk, dv; ``workspace`` is a uint8 device tensor."""
+    _bwd_call("nc_attn_bwd", q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+
+
+def nc_attn_bwd_deterministic(q, k, v, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace,
+                              stream=None) -> None:
+    """Bitwise-reproducible backward into caller-owned dq, dk, dv (same arguments as nc_attn_bwd)."""
+    _bwd_call("nc_attn_bwd_deterministic", q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+
+
+def _bwd_call(name, q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream):
     B, T, H, D = q.shape
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
         _need(t, n, torch.bfloat16, (B, T, H, D))
     _need(lse, "lse", torch.float32, (B, H, T))
     _need(workspace, "workspace", torch.uint8)
-    _check(lib.nc_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                           B, T, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
-                           _stream(q.device, stream)), "nc_attn_bwd")
+    _check(getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, T, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
+                              _stream(q.device, stream)), name)
 
 
 def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, workspace, stream=None) -> None:
@@ -295,14 +308,16 @@ def attn_fwd(q, k, v, window: int, scale: float | None = None, stream=None):
     return o, lse
 
 
-def attn_bwd(q, k, v, o, dO, lse, window: int, scale: float | None = None, workspace=None, stream=None):
-    """Returns (dq, dk, dv)."""
+def attn_bwd(q, k, v, o, dO, lse, window: int, scale: float | None = None, workspace=None, stream=None,
+             deterministic: bool = False):
+    """Returns (dq, dk, dv); ``deterministic`` selects the bitwise-reproducible backward."""
     B, T, H, D = q.shape
     scale = default_scale(D) if scale is None else scale
     if workspace is None:
         workspace = torch.empty(nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+    (nc_attn_bwd_deterministic if deterministic else nc_attn_bwd)(q, k, v, o, dO, lse, dq, dk, dv, window, scale,
+                                                                  workspace, stream)
     return dq, dk, dv
 
 

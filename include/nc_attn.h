@@ -103,6 +103,22 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int B, int T, int H, int D, int window, float scale,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Deterministic backward.  The same gradients, arguments, layout, workspace
+ * (nc_attn_bwd_workspace_bytes) and errors as nc_attn_bwd, but dq, dk and dv
+ * are bitwise identical from run to run on the same device for the same
+ * inputs: dK and dV accumulate in a fixed order in the main kernel, and dq
+ * comes from a second pass in which one CTA owns each 128-row query block and
+ * sums its key blocks in a fixed order, instead of adding partials with fp32
+ * atomics.  The second pass recomputes S = scale q k^T and dP = dO v^T for
+ * every visible block pair, so this call does about 7/5 of nc_attn_bwd's
+ * tensor-core work.  The fp32 dQ accumulator part of the workspace is unused.
+ */
+nc_status nc_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                    const float* lse, void* dq, void* dk, void* dv,
+                                    int B, int T, int H, int D, int window, float scale,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of device workspace nc_attn_decode needs for its split-K partial
  * results (fp32 running max, sum and output per split). */
 size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D);

@@ -26,7 +26,7 @@ def _declared():
 
 
 def test_header_declares_the_abi():
-    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
+    assert {"nc_attn_fwd", "nc_attn_bwd", "nc_attn_bwd_deterministic", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
             "nc_attn_bwd_workspace_bytes",
             "nc_attn_decode_workspace_bytes", "nc_get_device_error", "nc_status_string",
             "nc_launch_count"} <= set(_declared())
@@ -90,31 +90,32 @@ def test_fwd_rejects_null_misaligned_and_aliased(lib):
     assert _fwd(lib, p) == lib.NC_ERR_INVALID
 
 
-def _bwd(lib, ptrs=None, ws=None, ws_bytes=None, **kw):
+def _bwd(lib, ptrs=None, ws=None, ws_bytes=None, fn="nc_attn_bwd", **kw):
     a = dict(GOOD, **kw)
     p = list(A[:9]) if ptrs is None else ptrs
     need = lib.nc_attn_bwd_workspace_bytes(a["B"], a["T"], a["H"], a["D"])
     ws = A[9] if ws is None else ws
     ws_bytes = need if ws_bytes is None else ws_bytes
-    return lib.lib.nc_attn_bwd(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"], a["window"],
-                               ctypes.c_float(a["scale"]), ctypes.c_void_p(ws), ws_bytes, None)
+    return getattr(lib.lib, fn)(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"], a["window"],
+                                ctypes.c_float(a["scale"]), ctypes.c_void_p(ws), ws_bytes, None)
 
 
-def test_bwd_rejects_bad_arguments(lib):
-    assert _bwd(lib, D=80) == lib.NC_ERR_UNSUPPORTED
-    assert _bwd(lib, window=0) == lib.NC_ERR_INVALID
+@pytest.mark.parametrize("fn", ["nc_attn_bwd", "nc_attn_bwd_deterministic"])
+def test_bwd_rejects_bad_arguments(lib, fn):
+    assert _bwd(lib, D=80, fn=fn) == lib.NC_ERR_UNSUPPORTED
+    assert _bwd(lib, window=0, fn=fn) == lib.NC_ERR_INVALID
     need = lib.nc_attn_bwd_workspace_bytes(2, 64, 2, 64)
-    assert _bwd(lib, ws_bytes=need - 1) == lib.NC_ERR_WORKSPACE
-    assert _bwd(lib, ws=0) == lib.NC_ERR_WORKSPACE
-    assert _bwd(lib, ws=A[9] + 4) == lib.NC_ERR_INVALID
+    assert _bwd(lib, ws_bytes=need - 1, fn=fn) == lib.NC_ERR_WORKSPACE
+    assert _bwd(lib, ws=0, fn=fn) == lib.NC_ERR_WORKSPACE
+    assert _bwd(lib, ws=A[9] + 4, fn=fn) == lib.NC_ERR_INVALID
     for i in range(9):
         p = list(A[:9]); p[i] = 0
-        assert _bwd(lib, p) == lib.NC_ERR_INVALID
+        assert _bwd(lib, p, fn=fn) == lib.NC_ERR_INVALID
     p = list(A[:9]); p[6] = p[0]            # dq aliases q
-    assert _bwd(lib, p) == lib.NC_ERR_INVALID
+    assert _bwd(lib, p, fn=fn) == lib.NC_ERR_INVALID
     p = list(A[:9]); p[7] = p[6]            # dk aliases dq
-    assert _bwd(lib, p) == lib.NC_ERR_INVALID
-    assert _bwd(lib, ws=A[1]) == lib.NC_ERR_INVALID  # workspace over k
+    assert _bwd(lib, p, fn=fn) == lib.NC_ERR_INVALID
+    assert _bwd(lib, ws=A[1], fn=fn) == lib.NC_ERR_INVALID  # workspace over k
 
 
 def _dec(lib, ptrs=None, ws_bytes=None, **kw):

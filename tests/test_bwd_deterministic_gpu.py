@@ -1,0 +1,122 @@
+"""GPU: the deterministic backward (nc_attn_bwd_deterministic) through the C ABI.
+
+Three things are checked:
+  * parity with the fp64 oracle, at the tolerances of the plain backward
+    (|dX - dX_ref| <= 3e-2 * max|dX_ref|, the scale floored at 1e-4);
+  * bitwise reproducibility of dq, dk and dv over repeated calls whose
+    workspaces start with different garbage;
+  * dk and dv bitwise equal to those of nc_attn_bwd (the same products in the
+    same order in both modes), dq equal to its dq up to summation order.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from causal_sliding_window_fwd_b300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+G_TOL = 3e-2
+
+
+@pytest.fixture(scope="module")
+def nc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_sliding_window_fwd_b300 import nc_attn
+    return nc_attn
+
+
+def rel_err(got, ref):
+    got = got.detach().float().cpu().numpy()
+    ref = np.asarray(ref)
+    assert np.isfinite(got).all(), "non-finite values in GPU output"
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
+
+
+def forward(nc, q, k, v, window, scale):
+    B, T, H, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    nc.nc_attn_fwd(q, k, v, o, lse, window, scale)
+    return o, lse
+
+
+def backward(nc, q, k, v, o, dO, lse, window, scale, deterministic, fill=0xFF):
+    B, T, H, D = q.shape
+    ws = torch.full((nc.nc_attn_bwd_workspace_bytes(B, T, H, D),), fill, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    fn = nc.nc_attn_bwd_deterministic if deterministic else nc.nc_attn_bwd
+    fn(q, k, v, o, dO, lse, dq, dk, dv, window, scale, ws)
+    assert nc.nc_get_device_error() == 0
+    return dq, dk, dv
+
+
+CASES = [
+    # (B, T, H, D, window): single blocks, ragged tails, windows of 1, below, at and above a block,
+    # full causal, and more (query block, head, batch) items than SMs
+    (1, 1, 1, 64, 1), (1, 7, 1, 128, 3), (2, 128, 1, 64, 1), (1, 200, 2, 128, 127), (1, 257, 1, 128, 129),
+    (1, 333, 2, 64, 332), (2, 384, 3, 128, -1), (1, 513, 2, 64, 100), (1, 700, 1, 128, 512),
+    (2, 800, 48, 64, 300), (1, 1100, 40, 128, 200),
+]
+
+
+@pytest.mark.parametrize("B,T,H,D,window", CASES)
+def test_deterministic_matches_oracle(nc, oracle_mod, B, T, H, D, window):
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=3000 + T + window, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    o, lse = forward(nc, q, k, v, window, scale)
+    dq, dk, dv = backward(nc, q, k, v, o, dO, lse, window, scale, True)
+    dq_r, dk_r, dv_r = oracle_mod.bwd(q.cpu(), k.cpu(), v.cpu(), dO.cpu(), window, scale)
+    assert rel_err(dq, dq_r) <= G_TOL, "dq"
+    assert rel_err(dk, dk_r) <= G_TOL, "dk"
+    assert rel_err(dv, dv_r) <= G_TOL, "dv"
+    # dK and dV come from the same products in the same order as in the plain backward
+    dq2, dk2, dv2 = backward(nc, q, k, v, o, dO, lse, window, scale, False)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    torch.testing.assert_close(dq.float(), dq2.float(), atol=2e-2, rtol=0)
+
+
+def test_deterministic_is_bitwise_repeatable(nc):
+    B, T, H, D, W = 2, 1000, 20, 128, 300
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=31, device="cuda")
+    o, lse = forward(nc, q, k, v, W, 0.088)
+    first = backward(nc, q, k, v, o, dO, lse, W, 0.088, True, fill=0x00)
+    for fill in (0xFF, 0x7F):
+        again = backward(nc, q, k, v, o, dO, lse, W, 0.088, True, fill=fill)
+        for x, y in zip(first, again):
+            assert torch.equal(x, y)
+
+
+def test_deterministic_window_one(nc):
+    """Window 1: o = v, dv = dO exactly, and dq = dk = 0 up to the rounding of dP - Delta."""
+    q, k, v, dO = workloads.make_qkvdo_shape(2, 300, 3, 128, seed=77, device="cuda")
+    o, lse = forward(nc, q, k, v, 1, 0.088)
+    dq, dk, dv = backward(nc, q, k, v, o, dO, lse, 1, 0.088, True)
+    assert torch.equal(dv, dO)
+    assert dq.float().abs().max().item() < 1e-5 and dk.float().abs().max().item() < 1e-5
+
+
+@pytest.mark.parametrize("call_idx", [0, 1])
+def test_deterministic_full_size(nc, oracle_mod, call_idx):
+    """The depth-20-like layer pair at full size: sampled (b, h) slices against the oracle,
+    repeatability, and agreement with the plain backward."""
+    call = workloads.D20_PAIR.calls[call_idx]
+    q, k, v, dO = workloads.make_qkvdo(call, "cuda")
+    o, lse = forward(nc, q, k, v, call.window, call.scale)
+    dq, dk, dv = backward(nc, q, k, v, o, dO, lse, call.window, call.scale, True)
+    dq1, dk1, dv1 = backward(nc, q, k, v, o, dO, lse, call.window, call.scale, True, fill=0x00)
+    assert torch.equal(dq, dq1) and torch.equal(dk, dk1) and torch.equal(dv, dv1)
+    dq2, dk2, dv2 = backward(nc, q, k, v, o, dO, lse, call.window, call.scale, False)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert (dq.float() - dq2.float()).abs().max().item() <= 2e-2 * dq2.float().abs().max().item()
+    rng = np.random.default_rng(call.seed + 1)
+    picks = {(call.B - 1, call.H - 1), (int(rng.integers(call.B)), int(rng.integers(call.H)))}
+    for b, h in sorted(picks):
+        sl = [x[b:b + 1, :, h:h + 1, :].contiguous().cpu() for x in (q, k, v, dO)]
+        dq_r, dk_r, dv_r = oracle_mod.bwd(*sl, call.window, call.scale)
+        assert rel_err(dq[b:b + 1, :, h:h + 1, :], dq_r) <= G_TOL, "dq"
+        assert rel_err(dk[b:b + 1, :, h:h + 1, :], dk_r) <= G_TOL, "dk"
+        assert rel_err(dv[b:b + 1, :, h:h + 1, :], dv_r) <= G_TOL, "dv"
