@@ -315,6 +315,7 @@ def run_ours(args, dist: Dist):
         out["decode"] = run_decode(dev, stream, nc_attn, peaks, peak_kind)
         out["prefill"] = run_prefill(dev, stream, nc_attn, peaks, peak_kind)
         out["varlen"] = run_varlen(dev, stream, nc_attn, peaks, peak_kind)
+        out["deterministic_bwd"] = run_deterministic(bufs, calls, dev, stream, nc_attn, peaks, peak_kind)
     return out
 
 
@@ -405,6 +406,46 @@ def run_varlen(dev, stream, nc_attn, peaks, peak_kind):
                     "TFLOP_s": round(step_tf, 1),
                     "roofline": {"bound": "tensor", "achieved": round(step_tf, 1), "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": round(step_tf / peaks["bf16_tflops"], 4),
+                                 "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
+    assert nc_attn.nc_get_device_error(stream) == 0
+    return res
+
+
+def run_deterministic(bufs, calls, dev, stream, nc_attn, peaks, peak_kind):
+    """Bitwise-reproducible backward on the layer pair beside the plain one, L2 flushed before each call.
+    useful TFLOP/s counts 10*D flops per visible pair (as for the plain backward); executed counts the
+    14*D the deterministic path runs (two more products per pair in its dQ pass)."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {"l2": "flushed (256 MB write) before every timed call"}
+
+    def timed(fn, n=15):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            evs = []
+            for _ in range(n):
+                flush.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                fn()
+                e.record(stream)
+                evs.append((s, e))
+            torch.cuda.synchronize()
+        return statistics.median([s.elapsed_time(e) for s, e in evs])
+
+    for call, b in zip(calls, bufs):
+        args = (b["q"], b["k"], b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"], call.window,
+                call.scale, b["ws"], stream)
+        det_ms = timed(lambda: nc_attn.nc_attn_bwd_deterministic(*args))
+        plain_ms = timed(lambda: nc_attn.nc_attn_bwd(*args))
+        pairs = call.B * call.H * workloads.pairs_in_window(call.T, call.window)
+        useful = 10.0 * call.D * pairs / (det_ms * 1e-3) / 1e12
+        executed = 14.0 * call.D * pairs / (det_ms * 1e-3) / 1e12
+        key = "w1024" if call.window < call.T else "full"
+        res[key] = {"window": call.window, "us": round(det_ms * 1e3, 2), "plain_us": round(plain_ms * 1e3, 2),
+                    "useful_TFLOP_s": round(useful, 1), "executed_TFLOP_s": round(executed, 1),
+                    "roofline": {"bound": "tensor", "achieved": round(executed, 1), "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": round(executed / peaks["bf16_tflops"], 4),
                                  "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
     assert nc_attn.nc_get_device_error(stream) == 0
     return res

@@ -13,15 +13,17 @@
 // in a shared-memory ring.  Indices run over groups of about one wave of items; inside a group
 // m runs outermost from the last block down (the longest causal walks first), so the CTAs that
 // run at the same time read the K and V of a few heads and share them in L2.  Warp roles:
-//   warp 0      TMA producer: Q and dO of the item once, then K and V blocks through a 2-slot ring
+//   warp 0      TMA producer: Q and dO of the item once, then K blocks through a 3-slot ring and V
+//               blocks through a 2-slot ring (V is free once dP has read it, K only after dQ)
 //   warp 1      MMA issuer (one lane) and TMEM owner
 //   warps 4-7   one thread per query row, key columns [0, 64): P, dS; then dQ columns [0, D/2)
 //   warps 8-11  the same for key columns [64, 128); then dQ columns [D/2, D)
 // TMEM: ST [0,128) holds S; DP0 [128,256) and DP1 [384,512) hold dP of alternate key blocks,
 // then dS packed as bf16 over the columns each warpgroup has already read (the A operand of
 // dQ += dS K); DQ [256,256+D) accumulates dQ.
-// Products for key block j, once dS(j) is in TMEM: S(j+1) into ST and dP(j+1) into the other DP
-// region (so the P/dS warps can start on block j+1 at once), then dQ += dS(j) K(j).
+// Products for key block j: once the P/dS warps have read S(j) out of TMEM, S(j+1) into ST and
+// dP(j+1) into the other DP region (they run while the warps compute P(j) and dS(j)); once dS(j)
+// is in TMEM, dQ += dS(j) K(j).
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -36,7 +38,8 @@ namespace {
 
 constexpr int kBQ = 128;        // query rows per block
 constexpr int kBK = 128;        // keys per block
-constexpr int kKVStages = 2;    // K/V ring slots (a slot holds one K and one V block)
+constexpr int kKStages = 3;     // K ring slots
+constexpr int kVStages = 2;     // V ring slots
 constexpr int kThreads = 384;
 constexpr int kItemReaders = 9; // warps that read each work-item slot: the MMA warp and 8 P/dS warps
 constexpr float kLog2e = 1.4426950408889634f;
@@ -46,18 +49,24 @@ struct DqSmem {
     static constexpr int kTile = kBQ * D * 2;  // one 128-row bf16 tile
     static constexpr int kQ = 0;
     static constexpr int kDO = kQ + kTile;
-    static constexpr int kKV = kDO + kTile;    // slot s: K at kKV + 2 s kTile, V right after
-    static constexpr int kBytes = kKV + kKVStages * 2 * kTile;
+    static constexpr int kK = kDO + kTile;     // kKStages tiles
+    static constexpr int kV = kK + kKStages * kTile;  // kVStages tiles
+    static constexpr int kBytes = kV + kVStages * kTile;
 };
 
 struct DqBarriers {
-    uint64_t kv_full[kKVStages];
-    uint64_t kv_empty[kKVStages];
+    uint64_t k_full[kKStages];
+    uint64_t k_empty[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t v_empty[kVStages];
     uint64_t q_full;
     uint64_t q_empty;
     uint64_t s_full;
-    uint64_t dp_full;
-    uint64_t ds_full;
+    uint64_t s_free;
+    // one per DP region (block parity): dP(j+1) lands before the P/dS warps wait for dP(j), so a
+    // single barrier could complete two phases ahead of its waiter
+    uint64_t dp_full[2];
+    uint64_t ds_full[2];
     uint64_t dq_final;
     uint64_t drain;
     uint64_t item_full[kItemSlots];
@@ -125,15 +134,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         return;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kKVStages; ++s) {
-            mbar_init(&bars.kv_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.q_empty, 1);
         mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.ds_full, 2 * kBQ);
+        mbar_init(&bars.s_free, 2 * kBQ);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.dp_full[s], 1);
+            mbar_init(&bars.ds_full[s], 2 * kBQ);
+        }
         mbar_init(&bars.dq_final, 1);
         mbar_init(&bars.drain, 1);
         for (int s = 0; s < kItemSlots; ++s) {
@@ -166,7 +182,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tma_prefetch_desc(&tm_do);
         }
         __syncwarp();
-        int seq = 0, q_loads = 0;
+        int seq = 0, q_loads = 0, k_loads = 0, v_loads = 0;
         bool ok = true;
         for (int ii = 0; ok; ++ii) {
             const int w = ring_publish_item(bars.item_full, bars.item_empty, bars.item, ii, n_items, p.work);
@@ -188,25 +204,34 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             ++q_loads;
             for (int n = it.n_lo; n <= it.m; ++n, ++seq) {
-                const int slot = seq % kKVStages;
-                if (!mbar_wait_warp(&bars.kv_empty[slot], ((seq / kKVStages) & 1) ^ 1) || aborted(bars)) {
+                const int ks = seq % kKStages, vs = seq % kVStages;
+                if (!mbar_wait_warp(&bars.k_empty[ks], ((seq / kKStages) & 1) ^ 1) || aborted(bars)) {
                     ok = false;
                     break;
                 }
-                uint8_t* kdst = smem + L::kKV + slot * 2 * L::kTile;
-                mbar_arrive_expect_tx_w(&bars.kv_full[slot], 2 * L::kTile);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d_w(kdst + c * kBK * 128, &tm_k, &bars.kv_full[slot], c * 64, it.h, n * kBK, it.b);
-                    tma_load_4d_w(kdst + L::kTile + c * kBK * 128, &tm_v, &bars.kv_full[slot], c * 64, it.h,
+                mbar_arrive_expect_tx_w(&bars.k_full[ks], L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kK + ks * L::kTile + c * kBK * 128, &tm_k, &bars.k_full[ks], c * 64, it.h,
                                   n * kBK, it.b);
+                ++k_loads;
+                if (!mbar_wait_warp(&bars.v_empty[vs], ((seq / kVStages) & 1) ^ 1) || aborted(bars)) {
+                    ok = false;
+                    break;
                 }
+                mbar_arrive_expect_tx_w(&bars.v_full[vs], L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kV + vs * L::kTile + c * kBK * 128, &tm_v, &bars.v_full[vs], c * 64, it.h,
+                                  n * kBK, it.b);
+                ++v_loads;
             }
         }
         if (!ok) record_timeout(bars, p.err);
         // never leave while a copy into this CTA's shared memory may still land: the last use of
         // each slot is the only one whose completion can still be outstanding
-        for (int x = seq - kKVStages < 0 ? 0 : seq - kKVStages; x < seq; ++x)
-            mbar_wait_warp(&bars.kv_full[x % kKVStages], (x / kKVStages) & 1);
+        for (int x = k_loads - kKStages < 0 ? 0 : k_loads - kKStages; x < k_loads; ++x)
+            mbar_wait_warp(&bars.k_full[x % kKStages], (x / kKStages) & 1);
+        for (int x = v_loads - kVStages < 0 ? 0 : v_loads - kVStages; x < v_loads; ++x)
+            mbar_wait_warp(&bars.v_full[x % kVStages], (x / kVStages) & 1);
         if (q_loads > 0) mbar_wait_warp(&bars.q_full, (q_loads - 1) & 1);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -214,26 +239,38 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         regs_decrease<72>();
         constexpr uint32_t id_qk = idesc_bf16(kBQ, kBK, false, false);  // S, dP (both operands K-major)
         constexpr uint32_t id_dq = idesc_bf16(kBQ, D, false, true);     // dQ (A from TMEM, B MN-major)
-        const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO), sKV = smem_u32(smem + L::kKV);
+        const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+        const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
         // descriptors are built once; each product adds a constant (bytes / 16) to the start field
         const uint64_t q_kmaj = sdesc(sQ, 16, 1024), do_kmaj = sdesc(sDO, 16, 1024);
-        const uint64_t kv_kmaj = sdesc(sKV, 16, 1024), k_mn = sdesc(sKV, kBK * 128, 1024);
+        const uint64_t k_kmaj = sdesc(sK, 16, 1024), v_kmaj = sdesc(sV, 16, 1024);
+        const uint64_t k_mn = sdesc(sK, kBK * 128, 1024);
         constexpr uint64_t kTileStep = L::kTile >> 4;
         constexpr uint64_t kChunk = (kBQ * 128) >> 4;
-        auto issue_s_dp = [&](int slot, uint32_t dp_col) {
-            const uint64_t kd = kv_kmaj + 2 * slot * kTileStep, vd = kd + kTileStep;
+        // S = Q K^T into ST, then dP = dO V^T into the DP region of block gb (ring position sq)
+        auto issue_s_dp = [&](int sq, int gb) -> bool {
+            const uint32_t dp_col = col_dp(gb);
+            const int ks = sq % kKStages, vs = sq % kVStages;
+            if (!mbar_wait_warp(&bars.k_full[ks], (sq / kKStages) & 1) || aborted(bars)) return false;
+            tc_fence_after();
+            const uint64_t kd = k_kmaj + ks * kTileStep;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T into ST
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
                 mma_ss_w(tmem + kColST, q_kmaj + off, kd + off, id_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit_w(&bars.s_full);
+            if (!mbar_wait_warp(&bars.v_full[vs], (sq / kVStages) & 1) || aborted(bars)) return false;
+            tc_fence_after();
+            const uint64_t vd = v_kmaj + vs * kTileStep;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T into a DP region
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
                 mma_ss_w(tmem + dp_col, do_kmaj + off, vd + off, id_qk, kk > 0 ? 1u : 0u);
             }
-            mma_commit_w(&bars.dp_full);
+            mma_commit_w(&bars.dp_full[gb & 1]);
+            mma_commit_w(&bars.v_empty[vs]);  // dP was the only reader of this V block
+            return true;
         };
         bool ok = true;
         int seq = 0, gj = 0;  // K/V ring position; key blocks processed over all items (barrier phases)
@@ -245,37 +282,37 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             if (w < 0) break;
             const DqItem it = dq_item(w, p);
-            ok = mbar_wait_warp(&bars.q_full, ii & 1) &&
-                 mbar_wait_warp(&bars.kv_full[seq % kKVStages], (seq / kKVStages) & 1) && !aborted(bars);
+            ok = mbar_wait_warp(&bars.q_full, ii & 1) && issue_s_dp(seq, gj);
             if (!ok) break;
-            tc_fence_after();
-            issue_s_dp(seq % kKVStages, col_dp(gj));
             if (it.n_lo == it.m) mma_commit_w(&bars.q_empty);  // every S and dP of this item is issued
             for (int n = it.n_lo; n <= it.m; ++n, ++seq, ++gj) {
-                const int slot = seq % kKVStages;
-                // dS(j) is in TMEM, and S(j) and dP(j) have been read
-                ok = mbar_wait_warp(&bars.ds_full, gj & 1) && !aborted(bars);
-                if (!ok) break;
-                tc_fence_after();
+                const int ks = seq % kKStages;
                 if (n < it.m) {
-                    const int slot1 = (seq + 1) % kKVStages;
-                    ok = mbar_wait_warp(&bars.kv_full[slot1], ((seq + 1) / kKVStages) & 1) && !aborted(bars);
+                    // S(j) has been read out of ST.  (The wait is skipped for an item's last block;
+                    // its phase is then passed over, never overtaken: the next arrival needs the
+                    // next item's first S, issued after this block's dS.)
+                    ok = mbar_wait_warp(&bars.s_free, gj & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s_dp(slot1, col_dp(gj + 1));
+                    ok = issue_s_dp(seq + 1, gj + 1);
+                    if (!ok) break;
                     if (n + 1 == it.m) mma_commit_w(&bars.q_empty);
                 }
+                // dS(j) is in TMEM, and dP(j) has been read
+                ok = mbar_wait_warp(&bars.ds_full[gj & 1], (gj >> 1) & 1) && !aborted(bars);
+                if (!ok) break;
+                tc_fence_after();
                 // dQ += dS K(j)  (A = dS packed in DP: keys 0-63 in columns [0,32), 64-127 in [64,96)).
                 // The first product of an item overwrites DQ; the P/dS warps read the previous
                 // item's DQ out before their dS arrivals for this item.
-                const uint64_t kmn = k_mn + 2 * slot * kTileStep;
+                const uint64_t kmn = k_mn + ks * kTileStep;
                 const uint32_t a = tmem + col_dp(gj);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint32_t pc = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
                     mma_ts_w(tmem + kColDQ, a + pc, kmn + kk * (2048 >> 4), id_dq, (n > it.n_lo || kk > 0) ? 1u : 0u);
                 }
-                mma_commit_w(&bars.kv_empty[slot]);  // K(j) and V(j): S, dP and dQ were their readers
+                mma_commit_w(&bars.k_empty[ks]);  // K(j): S and dQ were its readers
             }
             if (!ok) break;
             mma_commit_w(&bars.dq_final);
@@ -312,11 +349,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ok = mbar_wait_warp(&bars.s_full, gj & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
-                // P in bf16, two per word: dS uses the same rounding of P as the main pass's dK
-                uint32_t pp[32];
+                float pf[64];  // P of this thread's row over the warpgroup's 64 keys
                 {
                     uint32_t a[32], b2[32];
                     tmem_ld32x2(tmem + lanes + kColST + 64 * g, tmem + lanes + kColST + 64 * g + 32, a, b2);
+                    // S is in registers: the MMA warp may write the next S into ST
+                    tc_fence_before();
+                    mbar_arrive(&bars.s_free);
                     const int j0 = n * kBK + 64 * g;
                     const bool full = (n < item.m) && (item.m * kBQ + kBQ - 1 - n * kBK < p.W);
 #pragma unroll
@@ -331,10 +370,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             if (j > i || i - j >= p.W) p0 = 0.f;
                             if (j + 1 > i || i - (j + 1) >= p.W) p1 = 0.f;
                         }
-                        pp[x / 2] = pack_bf16x2(p0, p1);
+                        pf[x] = p0;
+                        pf[x + 1] = p1;
                     }
                 }
-                ok = mbar_wait_warp(&bars.dp_full, gj & 1) && !aborted(bars);
+                ok = mbar_wait_warp(&bars.dp_full[gj & 1], (gj >> 1) & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t dp_addr = tmem + lanes + col_dp(gj) + 64 * g;
@@ -346,11 +386,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 32; x += 2) {
-                            const uint32_t wp = pp[16 * c + x / 2];
                             float t0, t1, d0, d1;
                             add_f32x2(t0, t1, __uint_as_float(c ? b2[x] : a[x]),
                                       __uint_as_float(c ? b2[x + 1] : a[x + 1]), -dlt, -dlt);
-                            mul_f32x2(d0, d1, __uint_as_float(wp << 16), __uint_as_float(wp & 0xffff0000u), t0, t1);
+                            mul_f32x2(d0, d1, pf[32 * c + x], pf[32 * c + x + 1], t0, t1);
                             pk[x / 2] = pack_bf16x2(d0, d1);
                         }
                         // dS (bf16) over this warpgroup's already-read DP columns
@@ -359,7 +398,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars.ds_full);
+                mbar_arrive(&bars.ds_full[gj & 1]);
             }
             if (!ok) break;
             // epilogue: dq = bf16(scale * DQ); warpgroup g writes dQ columns [g D/2, (g+1) D/2) of

@@ -6,7 +6,8 @@ Three things are checked:
   * bitwise reproducibility of dq, dk and dv over repeated calls whose
     workspaces start with different garbage;
   * dk and dv bitwise equal to those of nc_attn_bwd (the same products in the
-    same order in both modes), dq equal to its dq up to summation order.
+    same order in both modes), dq equal to its dq up to summation order and
+    the rounding of P (kept in fp32 by the dQ pass, bf16 in the main pass).
 """
 import math
 
@@ -76,7 +77,9 @@ def test_deterministic_matches_oracle(nc, oracle_mod, B, T, H, D, window):
     # dK and dV come from the same products in the same order as in the plain backward
     dq2, dk2, dv2 = backward(nc, q, k, v, o, dO, lse, window, scale, False)
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
-    torch.testing.assert_close(dq.float(), dq2.float(), atol=2e-2, rtol=0)
+    # the two paths round dS differently (the dQ pass keeps P in fp32), so they agree to about one
+    # bf16 unit of the largest entries
+    assert (dq.float() - dq2.float()).abs().max().item() <= 1e-2 * dq2.float().abs().max().item()
 
 
 def test_deterministic_is_bitwise_repeatable(nc):
