@@ -207,10 +207,6 @@ __device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
     atomicExch(&bars->abort, 1);
 }
 
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -424,6 +420,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                  (it > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
+                    if (kNoDq && it + 1 < item.n_it) {
+                        // without the dQ product nothing else waits on this block's DPT, so the next
+                        // block's S^T goes into ST right away (dV above was the last reader of P^T) and
+                        // the P/dS warps find it ready when they finish this block's dS.  (With dQ, the
+                        // next dP^T waits for dQ to leave DPT, and issuing S^T early only moves the wait.)
+                        const int st1 = (gi + 1) % kQStages;
+                        ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(st1);
+                    }
                     // dK += dS^T Q  (A = dS^T packed in DPT: reading A from TMEM halves this
                     // product's shared-memory traffic, and shared-memory bandwidth is what the
                     // products of this kernel compete for)
@@ -457,10 +464,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // next block: S^T into ST right away (dV above was the last reader of P^T);
                         // dP^T into DPT once this block's dQ has been read out
                         const int st1 = (gi + 1) % kQStages, so1 = (gi + 1) % L::kDOStages;
-                        ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_s(st1);
+                        if (!kNoDq) {
+                            ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(st1);
+                        }
                         ok = (kNoDq || mbar_wait_warp(&bars->dq_empty, gi & 1)) &&
                              mbar_wait_warp(&bars->do_full[so1], ((gi + 1) / L::kDOStages) & 1) && !aborted(bars);
                         if (!ok) break;

@@ -55,7 +55,9 @@ struct FwdSmem {
     static constexpr int kTileBytes = kBM * D * 2;     // one Q tile or one K/V block
     static constexpr int kQOff = 0;                    // Q0, Q1
     static constexpr int kKVOff = 2 * kTileBytes;      // ring
-    static constexpr int kBytes = kKVOff + kStages * kTileBytes;
+    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;  // O epilogue: 64 columns x 128 rows per tile
+    static constexpr int kStageBytes = 2 * kBM * 128;
+    static constexpr int kBytes = kStageOff + kStageBytes;
 };
 
 struct FwdBarriers {
@@ -207,7 +209,7 @@ __device__ __forceinline__ int publish_fwd_item(FwdBarriers& bars, int k, int n_
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
     using L = FwdSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -464,7 +466,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int w;
             if (kMode == kModeVarlen) {
                 w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
-                if (w == -2) {
+                // the warps of this warpgroup read the same slot; they leave together if any wait ran out
+                // (the epilogue below synchronises them with named barriers)
+                if (!named_bar_and(1 + t, 128, w != -2)) {
                     ok = false;
                     break;
                 }
@@ -565,27 +569,63 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2; then hand both O tiles back
             if (ok) ok = mbar_wait_warp(&bars.o_final, ip & 1) && !aborted(bars);
             ++ip;
+            ok = named_bar_and(1 + t, 128, ok);  // leave together: the epilogue synchronises the warpgroup
             if (!ok) break;
             tc_fence_after();
             if (tile_on) {
                 const float inv_l = item.bad ? __int_as_float(0x7fc00000) : 1.f / l_run;  // NaN rows for a bad length
                 const bool in_range = row < item.len;
                 if (item.bad && row_in_tile == 0 && t == 0) set_device_error(p.err, NC_ERR_BAD_CACHE_LEN);
-                __nv_bfloat16* orow =
-                    p.o + ((static_cast<size_t>(item.b) * p.Tq + item.base + row) * p.H + item.h) * D;
+                // O leaves through TMA stores of 64-column slices staged in shared memory (128-byte
+                // swizzle, the layout of the TMA map), so the global writes go out as whole lines; rows
+                // past the end of the tensor are clipped by the store.  A varlen tile that runs past its
+                // document is written row by row instead, so the next document's rows are left alone.
+                const bool whole = (kMode != kModeVarlen) || (tr0 + kBM <= item.len);
+                if (whole) {
+                    uint8_t* stage = smem + L::kStageOff + t * (kBM * 128);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
-                    if (in_range) {
+                    for (int c = 0; c < D / 64; ++c) {
+                        if (row_in_tile == 0) bulk_wait_read();  // the previous store has read the slice
+                        named_bar_sync(1 + t, 128);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 pkt;
-                            pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                            pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                            pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                            pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                            reinterpret_cast<uint4*>(orow + c * 32)[v] = pkt;
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + c * 64 + h2 * 32, r);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint4 pkt;
+                                pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+                                pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+                                pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+                                pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+                                const int unit = 4 * h2 + v;  // 16-byte unit of the row's 128-byte slice
+                                *reinterpret_cast<uint4*>(stage + row_in_tile * 128 + ((unit ^ (row_in_tile & 7)) << 4)) = pkt;
+                            }
+                        }
+                        fence_async_smem();
+                        named_bar_sync(1 + t, 128);
+                        if (row_in_tile == 0) {
+                            tma_store_4d(&tm_o, stage, c * 64, item.h, item.base + tr0, item.b);
+                            bulk_commit();
+                        }
+                    }
+                } else {
+                    __nv_bfloat16* orow =
+                        p.o + ((static_cast<size_t>(item.b) * p.Tq + item.base + row) * p.H + item.h) * D;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + c * 32, r);
+                        if (in_range) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint4 pkt;
+                                pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+                                pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+                                pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+                                pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+                                reinterpret_cast<uint4*>(orow + c * 32)[v] = pkt;
+                            }
                         }
                     }
                 }
@@ -598,6 +638,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         if (!ok) record_timeout(bars, p.err);
     }
+    if (warp >= 4 && (threadIdx.x & 127) == 0) bulk_wait_all();  // the O stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -614,9 +655,9 @@ template <int D>
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int* lens, const int* cu, int n_docs,
                           int max_len, void* o, float* lse, int B, int Tq, int Tk, int H, int window, float scale,
                           int* err, cudaStream_t st) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_tmap_bthd(&tq, q, B, Tq, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, Tk, H, D, 64, kBN) ||
-        !make_tmap_bthd(&tv, v, B, Tk, H, D, 64, kBN))
+        !make_tmap_bthd(&tv, v, B, Tk, H, D, 64, kBN) || !make_tmap_bthd(&to, o, B, Tq, H, D, 64, kBM))
         return cudaErrorInvalidValue;
     FwdParams p;
     p.o = static_cast<__nv_bfloat16*>(o);
@@ -670,11 +711,11 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
         p.work = wb + 2 * (work_seq.fetch_add(1u) % kWorkSlots);
     }
     if (cu != nullptr)
-        fwd_tc_kernel<D, kModeVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+        fwd_tc_kernel<D, kModeVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
     else if (lens != nullptr)
-        fwd_tc_kernel<D, kModeCache><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+        fwd_tc_kernel<D, kModeCache><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
     else
-        fwd_tc_kernel<D, kModePlain><<<grid, kThreads, smem, st>>>(tq, tk, tv, p);
+        fwd_tc_kernel<D, kModePlain><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
     count_launches(1);
     return cudaGetLastError();
 }

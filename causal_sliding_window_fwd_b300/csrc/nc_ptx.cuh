@@ -122,6 +122,10 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Wait until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Order this thread's generic-proxy writes to shared memory before later async-proxy reads
+// (a TMA store or a tensor-core operand fetch of the same bytes).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
