@@ -23,7 +23,7 @@
 // dQ += dS K); DQ [256,256+D) accumulates dQ.
 // Products for key block j: once the P/dS warps have read S(j) out of TMEM, S(j+1) into ST and
 // dP(j+1) into the other DP region (they run while the warps compute P(j) and dS(j)); once dS(j)
-// is in TMEM, dQ += dS(j) K(j).
+// is in TMEM, dQ += dS(j) K(j).  An item's dQ is written out after the next item's first dS.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -68,6 +68,7 @@ struct DqBarriers {
     uint64_t dp_full[2];
     uint64_t ds_full[2];
     uint64_t dq_final;
+    uint64_t dq_free;   // the P/dS warps have read DQ out (the next item's first dQ product may overwrite it)
     uint64_t drain;
     uint64_t item_full[kItemSlots];
     uint64_t item_empty[kItemSlots];
@@ -84,6 +85,7 @@ struct DqParams {
     float scale, scale_log2;
     int n_qb;
     int group;           // (batch, head) pairs per scheduling group
+    bool dq32;           // dq is 32-byte aligned: the epilogue writes whole 32-byte sectors
     int* work;           // work-item counter, zero on entry
     int* err;
 };
@@ -151,6 +153,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars.ds_full[s], 2 * kBQ);
         }
         mbar_init(&bars.dq_final, 1);
+        mbar_init(&bars.dq_free, 2 * kBQ);
         mbar_init(&bars.drain, 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&bars.item_full[s], 1);
@@ -302,9 +305,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 ok = mbar_wait_warp(&bars.ds_full[gj & 1], (gj >> 1) & 1) && !aborted(bars);
                 if (!ok) break;
                 tc_fence_after();
-                // dQ += dS K(j)  (A = dS packed in DP: keys 0-63 in columns [0,32), 64-127 in [64,96)).
-                // The first product of an item overwrites DQ; the P/dS warps read the previous
-                // item's DQ out before their dS arrivals for this item.
+                if (n == it.n_lo && ii > 0) {
+                    // the first product of an item overwrites DQ: the P/dS warps have read the previous
+                    // item's dQ out (they do so after this item's first dS)
+                    ok = mbar_wait_warp(&bars.dq_free, (ii - 1) & 1) && !aborted(bars);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // dQ += dS K(j)  (A = dS packed in DP: keys 0-63 in columns [0,32), 64-127 in [64,96))
                 const uint64_t kmn = k_mn + ks * kTileStep;
                 const uint32_t a = tmem + col_dp(gj);
 #pragma unroll
@@ -329,8 +337,45 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int tid = threadIdx.x - 128 * (g + 1);
         const uint32_t lanes = static_cast<uint32_t>(32 * (warp % 4)) << 16;
         const float sl2 = p.scale_log2;
+        // epilogue of an item: dq = bf16(scale * DQ); warpgroup g writes dQ columns [g D/2, (g+1) D/2) of its
+        // row.  It runs after the next item's first dS, so the MMA warp has that block's S and dP products to
+        // run meanwhile; dq_free then lets the next item's first dQ product overwrite DQ.
+        auto epilogue = [&](const DqItem& item, int ie) -> bool {
+            const int i = item.m * kBQ + tid;
+            const bool row_ok = i < p.T;
+            if (!(mbar_wait_warp(&bars.dq_final, ie & 1) && !aborted(bars))) return false;
+            tc_fence_after();
+            __nv_bfloat16* drow =
+                p.dq + ((static_cast<size_t>(item.b) * p.T + (row_ok ? i : 0)) * p.H + item.h) * D + g * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lanes + kColDQ + g * (D / 2) + c * 32, r);
+                uint32_t w[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    w[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * p.scale, __uint_as_float(r[2 * x + 1]) * p.scale);
+                if (row_ok) {
+                    if (p.dq32) {
+                        st_global_v8(drow + c * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                        st_global_v8(drow + c * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+                    } else {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            reinterpret_cast<uint4*>(drow + c * 32)[v4] =
+                                make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.dq_free);
+            return true;
+        };
         bool ok = true;
         int gj = 0;
+        bool have_prev = false;  // an item whose dQ still waits in TMEM
+        DqItem prev{};
+        int prev_ii = 0;
         for (int ii = 0; ok; ++ii) {
             const int w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
             if (w == -2) {
@@ -399,37 +444,18 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars.ds_full[gj & 1]);
-            }
-            if (!ok) break;
-            // epilogue: dq = bf16(scale * DQ); warpgroup g writes dQ columns [g D/2, (g+1) D/2) of
-            // its row (a whole 128-byte line for D = 128)
-            ok = mbar_wait_warp(&bars.dq_final, ii & 1) && !aborted(bars);
-            if (!ok) break;
-            tc_fence_after();
-            __nv_bfloat16* drow =
-                p.dq + ((static_cast<size_t>(item.b) * p.T + (row_ok ? i : 0)) * p.H + item.h) * D + g * (D / 2);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lanes + kColDQ + g * (D / 2) + c * 32, r);
-                if (row_ok) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 pkt;
-                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * p.scale,
-                                            __uint_as_float(r[8 * v4 + 1]) * p.scale);
-                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * p.scale,
-                                            __uint_as_float(r[8 * v4 + 3]) * p.scale);
-                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * p.scale,
-                                            __uint_as_float(r[8 * v4 + 5]) * p.scale);
-                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * p.scale,
-                                            __uint_as_float(r[8 * v4 + 7]) * p.scale);
-                        reinterpret_cast<uint4*>(drow + c * 32)[v4] = pkt;
-                    }
+                if (have_prev) {
+                    have_prev = false;
+                    ok = epilogue(prev, prev_ii);
+                    if (!ok) break;
                 }
             }
-            tc_fence_before();
+            if (!ok) break;
+            have_prev = true;
+            prev = item;
+            prev_ii = ii;
         }
+        if (ok && have_prev) ok = epilogue(prev, prev_ii);
         if (!ok) record_timeout(bars, p.err);
     }
     tc_fence_before();
@@ -461,6 +487,7 @@ cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void
     p.n_qb = (T + kBQ - 1) / kBQ;
     p.work = work;
     p.err = err;
+    p.dq32 = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     const int smem = DqSmem<D>::kBytes;
     static bool attr_set[64] = {false};
     int dev = 0;
