@@ -2,6 +2,7 @@
 
     python -m causal_sliding_window_fwd_b300.profile_case --op fwd --B 16 --T 2048 --H 10 --D 128 --window 2048
     python -m causal_sliding_window_fwd_b300.profile_case --op bwd ...
+    python -m causal_sliding_window_fwd_b300.profile_case --op bwd_det ...   (nc_attn_bwd_deterministic)
     python -m causal_sliding_window_fwd_b300.profile_case --op decode --window 1024
 
 The inputs are made and the forward (needed by the backward) is run before
@@ -19,7 +20,7 @@ from causal_sliding_window_fwd_b300 import nc_attn, workloads
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["fwd", "bwd", "decode"], default="fwd")
+    ap.add_argument("--op", choices=["fwd", "bwd", "bwd_det", "decode"], default="fwd")
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--H", type=int, default=10)
@@ -48,8 +49,9 @@ def main():
         else:
             ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(a.B, a.T, a.H, a.D), dtype=torch.uint8, device=dev)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            fn = nc_attn.nc_attn_bwd_deterministic if a.op == "bwd_det" else nc_attn.nc_attn_bwd
             for _ in range(a.iters):
-                nc_attn.nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, a.window, scale, ws)
+                fn(q, k, v, o, dO, lse, dq, dk, dv, a.window, scale, ws)
     torch.cuda.synchronize()
     assert nc_attn.nc_get_device_error() == 0
     print("done", a.op)
