@@ -91,7 +91,8 @@ struct BwdBarriers {
     uint64_t final_;
     uint64_t drain;
     uint64_t epi_done;    // dK / dV epilogue tiles in the dS region have been read by their TMA stores
-    uint64_t stage_free;  // the last dQ reduce-add of an item has read the staging tile (D = 128)
+    uint64_t dv_final;    // the item's last dV product has landed (D = 128 with dQ: dV leaves through the dO stage)
+    uint64_t do_epi_free; // the dV epilogue's TMA stores have read the dO stage (the next item's first dO may load)
     uint64_t item_full[kItemSlots];
     uint64_t item_empty[kItemSlots];
     int item[kItemSlots];
@@ -252,7 +253,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bars->final_, 1);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->epi_done, L::kTmaReduce ? 1 : 2);
-        mbar_init(&bars->stage_free, 1);
+        mbar_init(&bars->dv_final, 1);
+        mbar_init(&bars->do_epi_free, 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&bars->item_full[s], 1);
             mbar_init(&bars->item_empty[s], kItemReaders);
@@ -324,6 +326,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64,
                                       item.h, item.base + i0, item.b);
                     ++gq;
+                    // D = 128 with dQ: the previous item's dV epilogue stages its tile in the dO stage
+                    if (L::kTmaReduce && !kNoDq && it == 0 && ii > 0 &&
+                        (!mbar_wait_warp(&bars->do_epi_free, (ii - 1) & 1) || aborted(bars))) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait_warp(&bars->do_empty[so], ((gd / L::kDOStages) & 1) ^ 1) || aborted(bars)) {
                         ok = false;
                         break;
@@ -420,6 +428,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                  (it > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit_w(&bars->do_empty[so]);  // dO of this block: dP^T and dV were its readers
+                    if (L::kTmaReduce && !kNoDq && it + 1 == item.n_it) mma_commit_w(&bars->dv_final);
                     if (kNoDq && it + 1 < item.n_it) {
                         // without the dQ product nothing else waits on this block's DPT, so the next
                         // block's S^T goes into ST right away (dV above was the last reader of P^T) and
@@ -507,6 +516,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return fetch_lse ? p.lse[rowvec + i] * kLog2e : p.delta[rowvec + i];
         };
         bool ok = true;
+        bool epi_owed = false;  // thread 0: an epilogue whose store wait and epi_done arrival are still due
         int gi = 0;  // query blocks processed over all items: the phase of every per-block barrier
         for (int ii = 0;; ++ii) {
             const int w = read_item(bars, ii);
@@ -596,6 +606,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // the first dS of an item goes where the previous item's dK (and for D = 64 dV)
                 // tile was staged: wait until those TMA stores have read it
                 // (without the dQ product the dS tile is not written, and the epilogues alone use it)
+                if (!kNoDq && it == 0 && tid == 0 && epi_owed) {
+                    // the previous item's dK (and for D = 64 dV) stores have read the dS tile: waited for
+                    // only now, so the warpgroup went on to this item's P^T meanwhile
+                    bulk_wait_read();
+                    mbar_arrive(&bars->epi_done);
+                    epi_owed = false;
+                }
                 if (!kNoDq && ok && it == 0 && ii > 0)
                     ok = mbar_wait_warp(&bars->epi_done, (ii - 1) & 1) && !aborted(bars);
                 if (!ok) continue;
@@ -653,12 +670,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // sent out by TMA stores, so the global writes leave as whole lines.  The next
             // item's first dV / dK products overwrite the accumulators only after this
             // warpgroup's next P^T / dS^T arrivals, which come after the reads below.
-            if (ok) ok = mbar_wait_warp(&bars->final_, ii & 1) && !aborted(bars);
-            // warpgroup 0 uses the dS tile (free once final_ has landed: dQ and dK were its last
-            // readers); for D = 128 warpgroup 1 uses the dQ staging tile once the last reduce-add
-            // of this item has read it, for D = 64 the second half of the dS tile
-            if (g == 1 && L::kTmaReduce && !kNoDq && ok)
-                ok = mbar_wait_warp(&bars->stage_free, ii & 1) && !aborted(bars);
+            // Warpgroup 0 stages dK in the dS tile, free once final_ has landed (dQ and dK were its last
+            // readers).  Warpgroup 1 stages dV: for D = 128 with dQ in the dO stage, free once the
+            // item's last dV has landed (dv_final, well before final_; the producer loads the next dO
+            // after these stores have read it); without dQ in the dQ staging tile; for D = 64 in the
+            // second half of the dS tile.
+            const bool dv_via_do = L::kTmaReduce && !kNoDq && g == 1;
+            if (ok) ok = mbar_wait_warp(dv_via_do ? &bars->dv_final : &bars->final_, ii & 1) && !aborted(bars);
             if (!named_bar_and(1 + g, 128, ok)) {  // leave together
                 ok = false;
                 record_timeout(bars, p.err);
@@ -668,7 +686,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after();
                 const uint32_t a = tmem + (static_cast<uint32_t>(lane_base) << 16) + (g ? kColDV : kColDK);
                 const float mul = g ? 1.f : p.scale;
-                uint8_t* tile = g == 0 ? smem + L::kDS : (L::kTmaReduce ? smem + L::kStage : smem + L::kDS + kBK * 128);
+                uint8_t* tile = g == 0 ? smem + L::kDS
+                                       : (dv_via_do ? smem + L::kDO
+                                                    : (L::kTmaReduce ? smem + L::kStage : smem + L::kDS + kBK * 128));
                 // a varlen key block that runs past its document's end is written row by row, so the
                 // next document's rows are left alone
                 const bool partial = kVarlen && j0 + kBK > item.len;
@@ -702,10 +722,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int c = 0; c < D / 64; ++c)
                             tma_store_4d(g ? &tm_dv : &tm_dk, tile + c * (kBK * 128), c * 64, h, item.base + j0, b);
                         bulk_commit();
-                        bulk_wait_read();
                     }
-                    // the dS tile may be written again (the next item's first dS) once this is set
-                    if (g == 0 || !L::kTmaReduce) mbar_arrive(&bars->epi_done);
+                    if (dv_via_do) {
+                        bulk_wait_read();
+                        mbar_arrive(&bars->do_epi_free);
+                    } else if (kNoDq) {
+                        bulk_wait_read();
+                        // the tile may be written again (the next epilogue) once this is set
+                        if (g == 0 || !L::kTmaReduce) mbar_arrive(&bars->epi_done);
+                    } else {
+                        // the wait for these stores and the epi_done arrival come just before this
+                        // warpgroup's next dS, the next write of the dS tile
+                        epi_owed = true;
+                    }
                 }
             }
         }
@@ -771,11 +800,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             tma_reduce_add_4d(&tm_dq, stage, 0, h, base + i0 + 64 * half, b);
                             bulk_commit();
                         }
-                    }
-                    if (it + 1 == item.n_it && tid == 0) {
-                        // the dV epilogue of this item reuses the staging tile
-                        bulk_wait_read();
-                        mbar_arrive(&bars->stage_free);
                     }
                 } else {
                     // thread = query row, TMEM columns = the D dQ columns
