@@ -19,7 +19,7 @@
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
 //   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T
 //               from S^T and dP^T; then the dK epilogue
-//   warps 8-11  the same for query columns [64, 128); then the dV epilogue
+//   warps 8-11  the same for query columns [64, 128); then the dV epilogue (staged in the dO stage for D = 128)
 //   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator with
 //               atomics; for D = 128 the product is dQ^T (one thread per dQ
 //               column, so a warp's atomic covers 32 consecutive floats of a row)
