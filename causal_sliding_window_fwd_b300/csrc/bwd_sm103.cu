@@ -76,8 +76,10 @@ struct BwdSmem {
 };
 
 struct BwdBarriers {
-    uint64_t kv_full;
-    uint64_t kv_empty;
+    uint64_t k_full;
+    uint64_t k_empty;     // every product of the item that reads K (S^T, dQ) is done
+    uint64_t v_full;
+    uint64_t v_empty;     // the item's last dP^T (the only reader of V) is done
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
     uint64_t do_full[2];
@@ -234,8 +236,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return;
     }
     if (threadIdx.x == 0) {
-        mbar_init(&bars->kv_full, 1);
-        mbar_init(&bars->kv_empty, 1);
+        mbar_init(&bars->k_full, 1);
+        mbar_init(&bars->k_empty, 1);
+        mbar_init(&bars->v_full, 1);
+        mbar_init(&bars->v_empty, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars->q_full[s], 1);
             mbar_init(&bars->q_empty[s], 1);
@@ -288,7 +292,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             __syncwarp();
             int gq = 0, gd = 0;  // Q and dO blocks loaded over all items (ring positions)
-            int kv_loads = 0;
+            int kv_loads = 0, k_loads = 0;  // V and K loads issued
             bool ok = true;
             for (int ii = 0; ok; ++ii) {
                 // varlen: pass over items past a document's end (and report bad document bounds)
@@ -301,19 +305,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (w < 0) break;
                 const BwdItem item = bwd_item<kVarlen>(w, p);
-                // K and V of this item once every product of the previous item has read theirs
-                if (!mbar_wait_warp(&bars->kv_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                // V of this item once the previous item's last dP^T has read its V (a block before that
+                // item ends), then K once its last dQ has read its K
+                if (!mbar_wait_warp(&bars->v_empty, (ii & 1) ^ 1) || aborted(bars)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_w(&bars->kv_full, 2 * L::kTile);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->kv_full, c * 64, item.h,
+                mbar_arrive_expect_tx_w(&bars->v_full, L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->v_full, c * 64, item.h,
                                   item.base + item.j0, item.b);
-                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->kv_full, c * 64, item.h,
-                                  item.base + item.j0, item.b);
-                }
                 ++kv_loads;
+                if (!mbar_wait_warp(&bars->k_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx_w(&bars->k_full, L::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->k_full, c * 64, item.h,
+                                  item.base + item.j0, item.b);
+                ++k_loads;
                 for (int it = 0; it < item.n_it; ++it) {
                     const int st = gq % kQStages, so = gd % L::kDOStages;
                     const int i0 = (item.m_lo + it) * kBQ;
@@ -350,7 +361,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_wait_warp(&bars->q_full[x % kQStages], (x / kQStages) & 1);
             for (int x = gd - L::kDOStages < 0 ? 0 : gd - L::kDOStages; x < gd; ++x)
                 mbar_wait_warp(&bars->do_full[x % L::kDOStages], (x / L::kDOStages) & 1);
-            if (kv_loads > 0) mbar_wait_warp(&bars->kv_full, (kv_loads - 1) & 1);
+            if (kv_loads > 0) mbar_wait_warp(&bars->v_full, (kv_loads - 1) & 1);
+            if (k_loads > 0) mbar_wait_warp(&bars->k_full, (k_loads - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -399,7 +411,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (w < 0) break;
                 const BwdItem item = bwd_item<kVarlen>(w, p);
-                ok = mbar_wait_warp(&bars->kv_full, ii & 1) && !aborted(bars);
+                ok = mbar_wait_warp(&bars->k_full, ii & 1) && !aborted(bars);
                 if (!ok) break;
                 {
                     // first block of the item: S^T, then dP^T once the previous block's dQ has left DPT
@@ -409,10 +421,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     issue_s(st);
                     ok = (kNoDq || gi == 0 || mbar_wait_warp(&bars->dq_empty, (gi - 1) & 1)) &&
+                         mbar_wait_warp(&bars->v_full, ii & 1) &&
                          mbar_wait_warp(&bars->do_full[so], (gi / L::kDOStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
                     issue_dp(so);
+                    if (item.n_it == 1) mma_commit_w(&bars->v_empty);  // the item's last dP^T is issued
                 }
                 for (int it = 0; it < item.n_it; ++it, ++gi) {
                     const int st = gi % kQStages, so = gi % L::kDOStages;
@@ -484,10 +498,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (!ok) break;
                         tc_fence_after();
                         issue_dp(so1);
+                        if (it + 2 == item.n_it) mma_commit_w(&bars->v_empty);  // the item's last dP^T is issued
                     }
                 }
                 if (!ok) break;
-                mma_commit_w(&bars->kv_empty);  // every product that reads this item's K and V is issued
+                mma_commit_w(&bars->k_empty);  // every product that reads this item's K is issued
                 mma_commit_w(&bars->final_);    // DK and DV of this item are complete once these land
             }
             if (!ok) record_timeout(bars, p.err);
