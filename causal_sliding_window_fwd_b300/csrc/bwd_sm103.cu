@@ -8,21 +8,25 @@
 //
 // Three launches on the caller's stream:
 //   bwd_pre   Delta = rowsum(dO * O) (fp32) and zeroing of the fp32 dQ accumulator
-//   bwd_main  one CTA per (128-key block, head, batch) walks the query blocks
-//             whose window reaches its keys; dK and dV accumulate in TMEM and
-//             the block's dQ contribution is added to the fp32 accumulator
+//   bwd_main  persistent CTAs (one per SM) take work items, each a 128-key block of one
+//             (batch, head), from a counter; an item walks the query blocks whose window
+//             reaches its keys; dK and dV accumulate in TMEM and each block's dQ
+//             contribution is added to the fp32 accumulator
 //   bwd_post  dq = bf16(scale * dQ accumulator)
+// (The deterministic backward runs bwd_main without its dQ product and a separate dQ pass,
+// bwd_dq_sm103.cu, instead of the accumulator.)
 //
 // bwd_main warp roles:
-//   warp 0      TMA producer: K and V once, then Q and dO blocks through a
-//               2-stage ring (128-byte swizzle)
+//   warp 0      TMA producer: each item's V and K (V as soon as the previous item's last dP^T
+//               has read it, K after its last dQ), then Q and dO blocks (128-byte swizzle)
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
-//   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T
-//               from S^T and dP^T; then the dK epilogue
-//   warps 8-11  the same for query columns [64, 128); then the dV epilogue (staged in the dO stage for D = 128)
-//   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator with
-//               atomics; for D = 128 the product is dQ^T (one thread per dQ
-//               column, so a warp's atomic covers 32 consecutive floats of a row)
+//   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T from S^T and
+//               dP^T; then the dK epilogue (staged in the dS tile)
+//   warps 8-11  the same for query columns [64, 128); then the dV epilogue (staged in the
+//               dO stage for D = 128, in the second half of the dS tile for D = 64)
+//   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator: for D = 128
+//               the product is dQ^T (one thread per dQ column), staged in shared memory and
+//               added by TMA reduce-adds; for D = 64 one thread per row, vector atomics
 // TMEM: ST [0,128) holds S^T, then P^T (bf16, two per column) in columns
 //       [0,32) for queries 0-63 and [64,96) for queries 64-127, so each
 //       warpgroup overwrites only columns it has already read.  DPT [128,256)

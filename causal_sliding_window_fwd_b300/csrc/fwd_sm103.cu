@@ -6,13 +6,15 @@
 // uses through FlashAttention-3's window_size argument.  The computation is
 // the textbook definition evaluated block by block with an online softmax.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and walks the
-// 128-key blocks that the causal window makes visible to either tile; blocks
-// wholly outside the window are never loaded (tile skipping).  Warp roles:
+// Persistent CTAs (one per SM) loop over work items.  An item is two 128-row query
+// tiles of one (batch, head); the CTA walks the 128-key blocks that the causal window
+// makes visible to either tile, and blocks wholly outside the window are never loaded
+// (tile skipping).  Warp roles:
 //   warp 0      TMA producer: Q tiles once, then K and V blocks through a
 //               4-slot shared-memory ring (128-byte swizzle)
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
-//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
+//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row); the epilogue
+//               stages O in shared memory and sends it with TMA stores
 //   warps 8-11  softmax + epilogue of query tile 1
 // TMEM: S0 cols [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // P (bf16, two per column) overwrites the first 64 columns of its S tile and
