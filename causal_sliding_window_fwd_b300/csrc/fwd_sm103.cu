@@ -10,12 +10,14 @@
 // tiles of one (batch, head); the CTA walks the 128-key blocks that the causal window
 // makes visible to either tile, and blocks wholly outside the window are never loaded
 // (tile skipping).  Warp roles:
-//   warp 0      TMA producer: Q tiles once, then K and V blocks through a
-//               4-slot shared-memory ring (128-byte swizzle)
-//   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
-//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row); the epilogue
-//               stages O in shared memory and sends it with TMA stores
-//   warps 8-11  softmax + epilogue of query tile 1
+//   warp 0       TMA producer: Q tiles once, then K and V blocks through a
+//                4-slot shared-memory ring (128-byte swizzle)
+//   warp 1       MMA issuer (one lane) and TMEM owner (512 columns)
+//   warps 4-7    softmax of query tile 0 (one thread per row)
+//   warps 8-11   softmax of query tile 1
+//   warps 12-15  epilogue of both tiles: O / l out of TMEM (handed back at once), then
+//                staged in shared memory and sent with TMA stores, and the log-sum-exp;
+//                it runs while the softmax warpgroups already work on the next item
 // TMEM: S0 cols [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // P (bf16, two per column) overwrites the first 64 columns of its S tile and
 // feeds the P*V product straight from TMEM.  The MMA issue order
@@ -39,8 +41,8 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per block
 constexpr int kStages = 4;        // K/V ring slots
-constexpr int kThreads = 384;     // 12 warps
-constexpr int kItemReaders = 9;   // warps that read each work-item slot: the MMA warp and 8 softmax warps
+constexpr int kThreads = 512;     // 16 warps
+constexpr int kItemReaders = 13;  // warps that read each work-item slot: the MMA warp, 8 softmax warps, 4 epilogue warps
 
 // Varlen work-item counters: one {next item, CTAs finished} pair per call, taken round-robin
 // from this ring.  They are zero at load, and the last CTA of each launch zeroes its pair
@@ -57,9 +59,11 @@ struct FwdSmem {
     static constexpr int kTileBytes = kBM * D * 2;     // one Q tile or one K/V block
     static constexpr int kQOff = 0;                    // Q0, Q1
     static constexpr int kKVOff = 2 * kTileBytes;      // ring
-    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;  // O epilogue: 64 columns x 128 rows per tile
-    static constexpr int kStageBytes = 2 * kBM * 128;
-    static constexpr int kBytes = kStageOff + kStageBytes;
+    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;  // O epilogue: one 64-column x 128-row slice
+    static constexpr int kStageBytes = kBM * 128;
+    static constexpr int kStatsOff = kStageOff + kStageBytes;        // row statistics, see FwdStats
+    static constexpr int kBarsOff = kStatsOff + 2 * 2 * kBM * 8;
+    static constexpr int kBytes = kBarsOff + 512;
 };
 
 struct FwdBarriers {
@@ -69,8 +73,13 @@ struct FwdBarriers {
     uint64_t q_empty;
     uint64_t s_full[2];
     uint64_t p_full[2];
+    // row statistics (m, l) handed from a tile's softmax warpgroup to the epilogue, in two slots
+    // (item parity) per tile, each with a full and an empty barrier, so neither side can run a
+    // whole phase ahead of the other on one barrier
+    uint64_t stats_full[2][2];   // [slot][tile]
+    uint64_t stats_empty[2][2];
     uint64_t o_final;
-    uint64_t o_free;
+    uint64_t o_free[2];       // the epilogue has read a tile's O out of TMEM
     uint64_t drain;
     uint64_t item_full[kItemSlots];   // varlen: work-item ring (see nc_sched.cuh)
     uint64_t item_empty[kItemSlots];
@@ -78,6 +87,7 @@ struct FwdBarriers {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(FwdBarriers) <= 512, "barrier block outgrew its shared-memory slot");
 
 struct FwdParams {
     __nv_bfloat16* o;     // [B, Tq, H, D]
@@ -204,6 +214,14 @@ __device__ __forceinline__ int publish_fwd_item(FwdBarriers& bars, int k, int n_
     return __shfl_sync(0xffffffffu, w, 0);
 }
 
+// Next work item of a role: from the static schedule (plain / prefill), or from the item ring that
+// the producer fills (varlen).  -1: no more items; -2: a wait ran out.
+template <int kMode>
+__device__ __forceinline__ int next_item(FwdBarriers& bars, int ii, int my_items) {
+    if (kMode == kModeVarlen) return ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
+    return ii < my_items ? sched_item_index(ii) : -1;
+}
+
 // kMode: the plain forward, prefill over a KV cache (per-sequence query offsets from p.lens), or
 // document-masked packed rows (per-document row bases from p.cu).  Varlen work items past a
 // document's end are skipped by every role alike; `ip` counts the items a role really ran and
@@ -213,12 +231,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
     using L = FwdSmem<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ FwdBarriers bars;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    FwdBarriers& bars = *reinterpret_cast<FwdBarriers*>(smem + L::kBarsOff);
+    // row statistics handed from the softmax warpgroups to the epilogue: [item parity][tile][row] (m, l)
+    float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
 
     const int warp = warp_id(), lane = lane_id();
+    const int n_items = p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B);
 
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars.kv_full[i], 1);
@@ -229,9 +253,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars.s_full[t], 1);
             mbar_init(&bars.p_full[t], kBM);
+            for (int sl = 0; sl < 2; ++sl) {
+                mbar_init(&bars.stats_full[sl][t], kBM);
+                mbar_init(&bars.stats_empty[sl][t], kBM);
+            }
         }
         mbar_init(&bars.o_final, 1);
-        mbar_init(&bars.o_free, 2 * kBM);
+        mbar_init(&bars.o_free[0], kBM);
+        mbar_init(&bars.o_free[1], kBM);
         mbar_init(&bars.drain, 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&bars.item_full[s], 1);
@@ -248,16 +277,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    // 384 threads x 168 registers at launch = 128 x 72 (producer/MMA warpgroup) + 256 x 216 (softmax);
-    // each role sets its budget at the top of its own branch
+    // 512 threads x 128 registers at launch; the producer/MMA warpgroup drops to 56, the softmax
+    // warpgroups rise to 176 and the epilogue drops to 96 (128 x 56 + 256 x 176 + 128 x 96 <= 65536)
     const uint32_t col_s[2] = {0u, 128u};
     const uint32_t col_o[2] = {256u, 256u + D};
+    const int my_items = kMode == kModeVarlen ? 0 : sched_items_of_cta(n_items);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
-        regs_decrease<72>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
+        regs_decrease<56>();
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -267,7 +296,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int seq = 0;          // K/V loads issued over all items (ring position)
         int q_loads = 0;
         bool ok = true;
-        const int n_items = p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B);
         for (int ii = 0; ok; ++ii) {
             // plain / prefill: the static zigzag schedule; varlen: items with work, from the counter
             int w;
@@ -332,217 +360,219 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
-        regs_decrease<72>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
-        {
-            constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
-            const uint32_t q_base = smem_u32(smem + L::kQOff);
-            const uint32_t kv_base = smem_u32(smem + L::kKVOff);
-            // Descriptors are built once; every product then only adds a constant
-            // (byte offset / 16) to the start-address field, which keeps the issue loop short.
-            const uint64_t q_desc = sdesc(q_base, 16, 1024);                // K-major, SW128
-            const uint64_t k_desc = sdesc(kv_base, 16, 1024);               // K-major, SW128
-            const uint64_t v_desc = sdesc(kv_base, kBN * 128, 1024);        // MN-major, SW128
-            constexpr uint64_t kTileStep = L::kTileBytes >> 4;
-            auto issue_s = [&](int t, int slot) {
-                const uint64_t qd = q_desc + t * kTileStep;
-                const uint64_t kd = k_desc + slot * kTileStep;
-                const uint32_t d = tmem + (t ? col_s[1] : col_s[0]);
+        regs_decrease<56>();
+        constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
+        const uint32_t q_base = smem_u32(smem + L::kQOff);
+        const uint32_t kv_base = smem_u32(smem + L::kKVOff);
+        // Descriptors are built once; every product then only adds a constant
+        // (byte offset / 16) to the start-address field, which keeps the issue loop short.
+        const uint64_t q_desc = sdesc(q_base, 16, 1024);                // K-major, SW128
+        const uint64_t k_desc = sdesc(kv_base, 16, 1024);               // K-major, SW128
+        const uint64_t v_desc = sdesc(kv_base, kBN * 128, 1024);        // MN-major, SW128
+        constexpr uint64_t kTileStep = L::kTileBytes >> 4;
+        auto issue_s = [&](int t, int slot) {
+            const uint64_t qd = q_desc + t * kTileStep;
+            const uint64_t kd = k_desc + slot * kTileStep;
+            const uint32_t d = tmem + (t ? col_s[1] : col_s[0]);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    constexpr int kChunk = (kBM * 128) >> 4;
-                    const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
-                    mma_ss_w(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                mma_commit_w(&bars.s_full[t]);
-            };
-            auto issue_pv = [&](int t, int slot, bool accumulate) {
-                const uint64_t vd = v_desc + slot * kTileStep;
-                const uint32_t d = tmem + (t ? col_o[1] : col_o[0]);
-                const uint32_t a = tmem + (t ? col_s[1] : col_s[0]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                constexpr int kChunk = (kBM * 128) >> 4;
+                const uint64_t off = (kk / 4) * kChunk + (kk % 4) * 2;
+                mma_ss_w(d, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bars.s_full[t]);
+        };
+        auto issue_pv = [&](int t, int slot, bool accumulate) {
+            const uint64_t vd = v_desc + slot * kTileStep;
+            const uint32_t d = tmem + (t ? col_o[1] : col_o[0]);
+            const uint32_t a = tmem + (t ? col_s[1] : col_s[0]);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts_w(d, a + kk * 8, vd + kk * (2048 >> 4), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts_w(d, a + kk * 8, vd + kk * (2048 >> 4), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = true;
+        int seq = 0;                 // K/V ring position over all items
+        int n_pv0 = 0, n_pv1 = 0;    // P tiles consumed per query tile over all items
+        int ip = 0;                  // items run
+        for (int ii = 0; ok; ++ii) {
+            const int w = next_item<kMode>(bars, ii, my_items);
+            if (w == -2) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;
+            const FwdItem it = fwd_item<kMode>(w, p);
+            if (it.empty) continue;
+            auto act = [&](int t, int kb) {
+                return t ? (kb >= it.lo[1] && kb <= it.hi[1]) : (kb >= it.lo[0] && kb <= it.hi[0]);
             };
-            bool ok = true;
-            int seq = 0;                 // K/V ring position over all items
-            int n_pv[2] = {0, 0};        // P tiles consumed per query tile over all items
-            int ip = 0;                  // items run
-            for (int ii = 0; ok; ++ii) {
-                int w;
-                if (kMode == kModeVarlen) {
-                    w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
-                    if (w == -2) {
-                        ok = false;
-                        break;
-                    }
-                    if (w < 0) break;
-                } else {
-                    if (ii >= my_items) break;
-                    w = sched_item_index(ii);
-                }
-                const FwdItem it = fwd_item<kMode>(w, p);
-                if (it.empty) continue;
-                auto act = [&](int t, int kb) { return kb >= it.lo[t] && kb <= it.hi[t]; };
-                ok = mbar_wait_warp(&bars.q_full, ip & 1);
+            ok = mbar_wait_warp(&bars.q_full, ip & 1);
+            if (!ok) break;
+            {
+                const int slot_k = seq % kStages;
+                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                 if (!ok) break;
-                {
-                    const int slot_k = seq % kStages;
-                    ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t)
-                        if (act(t, it.kb_lo)) issue_s(t, slot_k);
-                    mma_commit_w(&bars.kv_empty[slot_k]);
-                    ++seq;
-                    if (it.kb_lo == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (act(t, it.kb_lo)) issue_s(t, slot_k);
+                mma_commit_w(&bars.kv_empty[slot_k]);
+                ++seq;
+                if (it.kb_lo == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
+            }
+            bool first_pv0 = true, first_pv1 = true;
+            for (int kb = it.kb_lo; ok && kb <= it.kb_hi; ++kb) {
+                const int slot_v = seq % kStages;
+                ok = mbar_wait_warp(&bars.kv_full[slot_v], (seq / kStages) & 1);
+                if (!ok) break;
+                ++seq;
+                if (kMode == kModeCache && kb == it.kb_hi) {
+                    // the last block of a prefill item may hold cache rows at or past the sequence's
+                    // length; their weights are 0, but 0 x NaN is NaN inside the product, so those
+                    // value rows are zeroed in shared memory first (whatever the cache holds there)
+                    const int r0 = it.off + it.len - kb * kBN;  // first row past the last query position
+                    if (r0 < kBN) {
+                        uint8_t* vt = smem + L::kKVOff + slot_v * L::kTileBytes;
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        for (int u = r0 * 8 + lane; u < kBN * 8; u += 32)  // 16-byte units of 128-byte rows
+                            for (int c = 0; c < D / 64; ++c)
+                                *reinterpret_cast<uint4*>(vt + c * kBN * 128 + u * 16) = z;
+                        fence_async_smem();
+                        __syncwarp();
+                    }
                 }
-                bool first_pv = true;
-                for (int kb = it.kb_lo; ok && kb <= it.kb_hi; ++kb) {
-                    const int slot_v = seq % kStages;
-                    ok = mbar_wait_warp(&bars.kv_full[slot_v], (seq / kStages) & 1);
-                    if (!ok) break;
-                    ++seq;
-                    const bool next = kb + 1 <= it.kb_hi;
-                    const int slot_k = seq % kStages;
-                    bool k_ready = false;
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (act(t, kb)) {
-                            if (first_pv && ip > 0) {
-                                // the epilogue of the previous item has read both O tiles
-                                ok = mbar_wait_warp(&bars.o_free, (ip - 1) & 1) && !aborted(bars);
-                                if (!ok) break;
-                            }
-                            first_pv = false;
-                            ok = mbar_wait_warp(&bars.p_full[t], n_pv[t] & 1) && !aborted(bars);
+                const bool next = kb + 1 <= it.kb_hi;
+                const int slot_k = seq % kStages;
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (act(t, kb)) {
+                        if ((t ? first_pv1 : first_pv0) && ip > 0) {
+                            // the epilogue has read this tile's O of the previous item
+                            ok = mbar_wait_warp(&bars.o_free[t], (ip - 1) & 1) && !aborted(bars);
+                            if (!ok) break;
+                        }
+                        if (t) first_pv1 = false; else first_pv0 = false;
+                        ok = mbar_wait_warp(&bars.p_full[t], (t ? n_pv1 : n_pv0) & 1) && !aborted(bars);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, slot_v, kb > (t ? it.lo[1] : it.lo[0]));
+                        if (t) ++n_pv1; else ++n_pv0;
+                    }
+                    if (next && act(t, kb + 1)) {
+                        if (!k_ready) {
+                            ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                             if (!ok) break;
                             tc_fence_after();
-                            issue_pv(t, slot_v, kb > it.lo[t]);
-                            ++n_pv[t];
+                            k_ready = true;
                         }
-                        if (next && act(t, kb + 1)) {
-                            if (!k_ready) {
-                                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
-                                if (!ok) break;
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            issue_s(t, slot_k);
-                        }
-                    }
-                    if (!ok) break;
-                    mma_commit_w(&bars.kv_empty[slot_v]);
-                    if (next) {
-                        mma_commit_w(&bars.kv_empty[slot_k]);
-                        ++seq;
-                        if (kb + 1 == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
+                        issue_s(t, slot_k);
                     }
                 }
-                if (ok) mma_commit_w(&bars.o_final);
-                ++ip;
+                if (!ok) break;
+                mma_commit_w(&bars.kv_empty[slot_v]);
+                if (next) {
+                    mma_commit_w(&bars.kv_empty[slot_k]);
+                    ++seq;
+                    if (kb + 1 == it.kb_hi) mma_commit_w(&bars.q_empty);  // every S of this item is issued
+                }
             }
-            if (!ok) record_timeout(bars, p.err);
-            // all products must have landed before TMEM is released
-            mma_commit_w(&bars.drain);
-            mbar_wait_warp(&bars.drain, 0);
+            if (ok) mma_commit_w(&bars.o_final);
+            ++ip;
         }
+        if (!ok) record_timeout(bars, p.err);
+        // all products must have landed before TMEM is released
+        mma_commit_w(&bars.drain);
+        mbar_wait_warp(&bars.drain, 0);
     } else if (warp < 4) {
-        regs_decrease<72>();
-    } else {
-        // ------------------------------------------------------------ softmax + epilogue
-        regs_increase<216>();
-        const int my_items = sched_items_of_cta(p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B));
+        regs_decrease<56>();
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ softmax of one query tile
+        // one thread per query row: the whole 128-key row of S is read from TMEM with one wait,
+        // masked on straddling blocks, its maximum taken, and P written back at the end (reading the
+        // row in separately waited chunks between the P stores measured 1.4-2x slower).
+        regs_increase<176>();
         const int t = (warp - 4) / 4;
         const int row_in_tile = threadIdx.x - 128 * (t + 1);  // 0..127 == TMEM lane
         const int lane_base = 32 * (warp % 4);
-        const uint32_t t_col_s = t ? col_s[1] : col_s[0];
-        const uint32_t t_col_o = t ? col_o[1] : col_o[0];
-        const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_s;
-        const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + t_col_o;
+        const uint32_t s_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + (t ? col_s[1] : col_s[0]);
+        const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + (t ? col_o[1] : col_o[0]);
         const float sl2 = p.scale_log2;
         bool ok = true;
         int n_s = 0;  // S tiles of this query tile consumed over all items
         int ip = 0;   // items run
         for (int ii = 0; ok; ++ii) {
-            int w;
-            if (kMode == kModeVarlen) {
-                w = ring_read_item(bars.item_full, bars.item_empty, bars.item, ii);
-                // the warps of this warpgroup read the same slot; they leave together if any wait ran out
-                // (the epilogue below synchronises them with named barriers)
-                if (!named_bar_and(1 + t, 128, w != -2)) {
-                    ok = false;
-                    break;
-                }
-                if (w < 0) break;
-            } else {
-                if (ii >= my_items) break;
-                w = sched_item_index(ii);
+            const int w = next_item<kMode>(bars, ii, my_items);
+            // the warps of this warpgroup leave together if any wait ran out
+            if (!named_bar_and(1 + t, 128, w != -2)) {
+                ok = false;
+                break;
             }
+            if (w < 0) break;
             const FwdItem item = fwd_item<kMode>(w, p);
             if (item.empty) continue;
             const int tr0 = t ? item.r0[1] : item.r0[0];
             const int t_lo = t ? item.lo[1] : item.lo[0];
             const int t_hi = t ? item.hi[1] : item.hi[0];
-            const int row = tr0 + row_in_tile;      // query row (q, o, lse coordinates)
-            const int pos = item.off + row;         // its position among the keys
+            const int pos = item.off + tr0 + row_in_tile;  // this row's position among the keys
             const int tpos0 = item.off + tr0;
             const bool tile_on = (t == 0) || item.active1;
             float m_run = -INFINITY, l_run = 0.f;
             if (tile_on) {
-                int it = 0;
-                for (int kb = t_lo; kb <= t_hi; ++kb, ++it, ++n_s) {
+                for (int kb = t_lo; kb <= t_hi; ++kb, ++n_s) {
                     ok = mbar_wait_warp(&bars.s_full[t], n_s & 1) && !aborted(bars);  // warp-uniform
                     if (!ok) break;
                     tc_fence_after();
-                    float s[kBN];
-                    {
-                        uint32_t r[kBN];
-                        tmem_ld128(s_addr, r);
-#pragma unroll
-                        for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
-                    }
                     // elementwise mask only on blocks that straddle the causal diagonal or the window edge
                     const int k0 = kb * kBN;
-                    const bool full_block = (k0 + kBN - 1 <= tpos0) && (k0 >= tpos0 + kBM - p.W);
-                    if (!full_block) {
+                    const bool masked = !((k0 + kBN - 1 <= tpos0) && (k0 >= tpos0 + kBM - p.W));
+                    const bool first = kb == t_lo;
+                    float sv[kBN];
+                    {
+                        uint32_t r0[64], r1[64];
+                        tmem_ld64_nowait(s_addr, r0);
+                        tmem_ld64_nowait(s_addr + 64, r1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            sv[i] = __uint_as_float(r0[i]);
+                            sv[64 + i] = __uint_as_float(r1[i]);
+                        }
+                    }
+                    if (masked) {
 #pragma unroll
                         for (int j = 0; j < kBN; ++j) {
                             const int key = k0 + j;
-                            if (key > pos || pos - key >= p.W) s[j] = -INFINITY;
+                            if (key > pos || pos - key >= p.W) sv[j] = -INFINITY;
                         }
                     }
-                    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                    float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-                    for (int j = 4; j + 8 <= kBN; j += 8) {  // s[4 .. kBN-5]
-                        mx0 = max3f(mx0, s[j], s[j + 1]);
-                        mx1 = max3f(mx1, s[j + 2], s[j + 3]);
-                        mx2 = max3f(mx2, s[j + 4], s[j + 5]);
-                        mx3 = max3f(mx3, s[j + 6], s[j + 7]);
+                    for (int j = 4; j + 8 <= kBN; j += 8) {
+                        mx0 = max3f(mx0, sv[j], sv[j + 1]);
+                        mx1 = max3f(mx1, sv[j + 2], sv[j + 3]);
+                        mx2 = max3f(mx2, sv[j + 4], sv[j + 5]);
+                        mx3 = max3f(mx3, sv[j + 6], sv[j + 7]);
                     }
-                    mx0 = max3f(mx0, s[kBN - 4], s[kBN - 3]);
-                    mx1 = max3f(mx1, s[kBN - 2], s[kBN - 1]);
+                    mx0 = max3f(mx0, sv[kBN - 4], sv[kBN - 3]);
+                    mx1 = max3f(mx1, sv[kBN - 2], sv[kBN - 1]);
                     const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-                    if (it == 0) {
+                    if (first) {
                         m_run = m_cand;
-                    } else {
-                        const bool want = m_cand > m_run + kRescaleThreshold;
-                        if (__any_sync(0xffffffffu, want)) {
-                            const float m_new = fmaxf(m_run, m_cand);
-                            const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
-                            m_run = m_new;
-                            l_run *= alpha;
+                    } else if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleThreshold)) {
+                        const float m_new = fmaxf(m_run, m_cand);
+                        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
+                        m_run = m_new;
+                        l_run *= alpha;
+#pragma unroll 1
+                        for (int d = 0; d < D / 32; ++d) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + d * 32, r);
 #pragma unroll
-                            for (int c = 0; c < D / 32; ++c) {
-                                uint32_t r[32];
-                                tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                                tmem_st32(o_addr + c * 32, r);
-                            }
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(o_addr + d * 32, r);
                         }
                     }
-                    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                    const float m_use = m_run == -INFINITY ? 0.f : m_run;
                     float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
                     for (int c = 0; c < kBN / 64; ++c) {
@@ -551,8 +581,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         for (int i = 0; i < 32; i += 2) {
                             float x0, x1, x2, x3;
                             const int j = c * 64 + 2 * i;
-                            fma_f32x2(x0, x1, s[j], s[j + 1], sl2, sl2, -m_use, -m_use);
-                            fma_f32x2(x2, x3, s[j + 2], s[j + 3], sl2, sl2, -m_use, -m_use);
+                            fma_f32x2(x0, x1, sv[j], sv[j + 1], sl2, sl2, -m_use, -m_use);
+                            fma_f32x2(x2, x3, sv[j + 2], sv[j + 3], sl2, sl2, -m_use, -m_use);
                             const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
                             const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
                             add_f32x2(sum0, sum1, sum0, sum1, e0, e1);
@@ -568,79 +598,110 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     mbar_arrive(&bars.p_full[t]);
                 }
             }
-            // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2; then hand both O tiles back
-            if (ok) ok = mbar_wait_warp(&bars.o_final, ip & 1) && !aborted(bars);
+            // hand the row's statistics to the epilogue: slot ip % 2, once the epilogue has read what
+            // this slot held two items ago
+            const int slot = ip & 1, use = ip >> 1;
+            if (ok) ok = mbar_wait_warp(&bars.stats_empty[slot][t], (use & 1) ^ 1) && !aborted(bars);
+            if (!ok) break;
+            stats[(slot * 2 + t) * kBM + row_in_tile] = make_float2(m_run, l_run);
+            mbar_arrive(&bars.stats_full[slot][t]);
             ++ip;
-            ok = named_bar_and(1 + t, 128, ok);  // leave together: the epilogue synchronises the warpgroup
+        }
+        if (!ok) record_timeout(bars, p.err);
+    } else {
+        // ------------------------------------------------------------ epilogue of both query tiles
+        // thread = row of both tiles.  Tile by tile, O is read out of TMEM, scaled by 1/l and packed to
+        // bf16 in registers, and the tile's TMEM is handed back (o_free) before any of its store work,
+        // so the next item's first products wait only for these reads.  The rows then leave through
+        // TMA stores of 64-column slices staged in shared memory (128-byte swizzle, the layout of the
+        // TMA map): whole-line global writes.
+        regs_decrease<96>();
+        const int row_in_tile = threadIdx.x - 384;  // 0..127 == TMEM lane
+        const int lane_base = 32 * (warp % 4);
+        uint8_t* stage = smem + L::kStageOff;
+        bool ok = true;
+        int ip = 0;
+        for (int ii = 0; ok; ++ii) {
+            const int w = next_item<kMode>(bars, ii, my_items);
+            if (!named_bar_and(3, 128, w != -2)) {
+                ok = false;
+                break;
+            }
+            if (w < 0) break;
+            const FwdItem item = fwd_item<kMode>(w, p);
+            if (item.empty) continue;
+            const int slot = ip & 1, use = ip >> 1;
+            ok = mbar_wait_warp(&bars.o_final, ip & 1) && mbar_wait_warp(&bars.stats_full[slot][0], use & 1) &&
+                 mbar_wait_warp(&bars.stats_full[slot][1], use & 1) && !aborted(bars);
+            ok = named_bar_and(3, 128, ok);  // leave together: the stores below synchronise the warpgroup
             if (!ok) break;
             tc_fence_after();
-            if (tile_on) {
-                const float inv_l = item.bad ? __int_as_float(0x7fc00000) : 1.f / l_run;  // NaN rows for a bad length
+            const float2 st0 = stats[(slot * 2 + 0) * kBM + row_in_tile];
+            const float2 st1 = stats[(slot * 2 + 1) * kBM + row_in_tile];
+            mbar_arrive(&bars.stats_empty[slot][0]);
+            mbar_arrive(&bars.stats_empty[slot][1]);
+            if (item.bad && row_in_tile == 0) set_device_error(p.err, NC_ERR_BAD_CACHE_LEN);
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                const bool tile_on = (t == 0) || item.active1;
+                const float2 st = t ? st1 : st0;
+                uint32_t po[D / 2];  // this row of the tile's O, scaled and packed
+                if (tile_on) {
+                    const float inv_l = item.bad ? __int_as_float(0x7fc00000) : 1.f / st.y;  // NaN rows for a bad length
+                    const uint32_t o_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + (t ? col_o[1] : col_o[0]);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            po[c * 16 + i] =
+                                pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.o_free[t]);
+                if (!tile_on) continue;
+                const int tr0 = t ? item.r0[1] : item.r0[0];
+                const int row = tr0 + row_in_tile;
                 const bool in_range = row < item.len;
-                if (item.bad && row_in_tile == 0 && t == 0) set_device_error(p.err, NC_ERR_BAD_CACHE_LEN);
-                // O leaves through TMA stores of 64-column slices staged in shared memory (128-byte
-                // swizzle, the layout of the TMA map), so the global writes go out as whole lines; rows
-                // past the end of the tensor are clipped by the store.  A varlen tile that runs past its
-                // document is written row by row instead, so the next document's rows are left alone.
+                // a varlen tile that runs past its document is written row by row, so the next
+                // document's rows are left alone; otherwise the TMA store clips rows past the tensor
                 const bool whole = (kMode != kModeVarlen) || (tr0 + kBM <= item.len);
                 if (whole) {
-                    uint8_t* stage = smem + L::kStageOff + t * (kBM * 128);
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         if (row_in_tile == 0) bulk_wait_read();  // the previous store has read the slice
-                        named_bar_sync(1 + t, 128);
+                        named_bar_sync(3, 128);
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            uint32_t r[32];
-                            tmem_ld32(o_addr + c * 64 + h2 * 32, r);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                uint4 pkt;
-                                pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                                pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                                pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                                pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                                const int unit = 4 * h2 + v;  // 16-byte unit of the row's 128-byte slice
-                                *reinterpret_cast<uint4*>(stage + row_in_tile * 128 + ((unit ^ (row_in_tile & 7)) << 4)) = pkt;
-                            }
+                        for (int u = 0; u < 8; ++u) {  // 16-byte unit u of the row's 128-byte slice
+                            const uint4 pkt = make_uint4(po[c * 32 + 4 * u], po[c * 32 + 4 * u + 1],
+                                                         po[c * 32 + 4 * u + 2], po[c * 32 + 4 * u + 3]);
+                            *reinterpret_cast<uint4*>(stage + row_in_tile * 128 + ((u ^ (row_in_tile & 7)) << 4)) = pkt;
                         }
                         fence_async_smem();
-                        named_bar_sync(1 + t, 128);
+                        named_bar_sync(3, 128);
                         if (row_in_tile == 0) {
                             tma_store_4d(&tm_o, stage, c * 64, item.h, item.base + tr0, item.b);
                             bulk_commit();
                         }
                     }
-                } else {
+                } else if (in_range) {
                     __nv_bfloat16* orow =
                         p.o + ((static_cast<size_t>(item.b) * p.Tq + item.base + row) * p.H + item.h) * D;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + c * 32, r);
-                        if (in_range) {
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                uint4 pkt;
-                                pkt.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                                pkt.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                                pkt.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                                pkt.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                                reinterpret_cast<uint4*>(orow + c * 32)[v] = pkt;
-                            }
-                        }
-                    }
+                    for (int u = 0; u < D / 8; ++u)
+                        reinterpret_cast<uint4*>(orow)[u] = make_uint4(po[4 * u], po[4 * u + 1], po[4 * u + 2], po[4 * u + 3]);
                 }
                 if (in_range)
                     p.lse[(static_cast<size_t>(item.b) * p.H + item.h) * p.Tq + item.base + row] =
-                        item.bad ? __int_as_float(0x7fc00000) : (m_run + __log2f(l_run)) * kLn2;
+                        item.bad ? __int_as_float(0x7fc00000) : (st.x + __log2f(st.y)) * kLn2;
             }
-            tc_fence_before();
-            mbar_arrive(&bars.o_free);
+            ++ip;
         }
         if (!ok) record_timeout(bars, p.err);
+        if (row_in_tile == 0) bulk_wait_all();  // the O stores have landed
     }
-    if (warp >= 4 && (threadIdx.x & 127) == 0) bulk_wait_all();  // the O stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -676,7 +737,7 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.scale_log2 = scale * kLog2e;
     p.n_pairs = ((cu != nullptr ? max_len : Tq) + 2 * kBM - 1) / (2 * kBM);
     p.err = err;
-    const int smem = FwdSmem<D>::kBytes + 1024;
+    const int smem = FwdSmem<D>::kBytes;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
