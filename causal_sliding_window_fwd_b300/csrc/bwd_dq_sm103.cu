@@ -489,23 +489,14 @@ cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void
     p.err = err;
     p.dq32 = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     const int smem = DqSmem<D>::kBytes;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // kernel attribute and SM count are looked up on every call (no host-side cache to race on)
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set[dev] = true;
-    }
-    static int sms[64] = {0};
-    if (dev < 64 && sms[dev] == 0) {
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int n_sm = 0;
+    e = multiprocessor_count(&n_sm);
+    if (e != cudaSuccess) return e;
     const int n_pairs = B * H;
     const long n_items = (long)p.n_qb * n_pairs;
-    const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_qb - 1) / p.n_qb;

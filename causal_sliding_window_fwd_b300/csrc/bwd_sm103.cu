@@ -957,44 +957,28 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     p.n_docs = n_docs;
     p.err = err;
     const int smem = BwdSmem<D>::kBytes;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // kernel attribute and SM count are looked up on every call (no host-side cache to race on)
+    auto kern = deterministic ? bwd_main_kernel<D, false, true>
+                              : (cu != nullptr ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(bwd_main_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_main_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_main_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set[dev] = true;
-    }
     // persistent: one CTA per SM (its shared memory and TMEM allow one), looping over the items
-    static int sms[64] = {0};
-    if (dev < 64 && sms[dev] == 0) {
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int n_sm = 0;
+    e = multiprocessor_count(&n_sm);
+    if (e != cudaSuccess) return e;
     const int n_pairs = (cu != nullptr ? n_docs : B) * H;
     const long n_items = (long)p.n_kb * n_pairs;
-    const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_kb - 1) / p.n_kb;
     if (p.group > n_pairs) p.group = n_pairs;
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     if (deterministic) {
-        bwd_main_kernel<D, false, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
         count_launches(2);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_bwd_dq(q, k, v, dO, lse, delta, dq, B, T, H, D, window, scale, work + 1, err, st);
     }
-    if (cu != nullptr)
-        bwd_main_kernel<D, true><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
-    else
-        bwd_main_kernel<D, false><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     const size_t n8 = (size_t)rows * D / 8;
     bwd_post_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
                                                                  scale);

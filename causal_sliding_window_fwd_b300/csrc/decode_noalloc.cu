@@ -10,11 +10,12 @@
 // file-scope __device__ array, so every GPU that loads the library holds it
 // until the process exits).  It runs the same kernels as nc_attn_decode.
 //
-// The first call on each device looks up the array's device address
-// (cudaGetSymbolAddress) with that device current; make that first call
-// before any stream capture.  All calls on a device share the one array, so
-// calls whose work overlaps on the GPU (other streams, other host threads)
-// race on it and must be serialised by the caller.
+// Every call looks up the array's device address (cudaGetSymbolAddress) with
+// the caller's device current; the first call on a device may load the
+// library's device code, so make it before any stream capture.  All calls on
+// a device share the one array, so calls whose work overlaps on the GPU (other
+// streams, other host threads) race on it and must be serialised by the
+// caller.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -29,26 +30,29 @@ namespace {
 // zero, because the combine pass reads only the splits the split pass wrote.
 static __device__ __align__(256) unsigned char g_decode_scratch[NC_DECODE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device.  Looked up once
-// per device: host code may not pass the symbol itself to a kernel, since in
-// host code it names a host-side stand-in, not device memory.
+// Device address of the scratch array on the current device, looked up on every call (host code
+// may not pass the symbol itself to a kernel: in host code it names a host-side stand-in, not
+// device memory).  No per-device cache, so concurrent first calls need no synchronisation and a
+// device reset leaves nothing stale behind.
 void* scratch_address() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
-    }
-    return g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// The size limits nc_attn_decode applies (index ranges of its kernels).
+bool sizes_supported(int N, int Tmax, int H, int D) {
+    return (int64_t)N * H < (int64_t(1) << 31) && (int64_t)Tmax * H * D < (int64_t(1) << 40);
+}
 
 }  // namespace
 
@@ -56,6 +60,7 @@ extern "C" {
 
 size_t nc_attn_decode_noalloc_scratch_bytes(int N, int Tmax, int H, int D, int window) {
     if (N <= 0 || Tmax <= 0 || H <= 0 || (D != 64 && D != 128) || (window < 1 && window != NC_WINDOW_FULL)) return 0;
+    if (!sizes_supported(N, Tmax, H, D)) return 0;
     const int chunk = nc::decode_chunk_rows(D);
     const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
     const size_t parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
@@ -68,12 +73,19 @@ nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* 
     if (N <= 0 || Tmax <= 0 || H <= 0 || D <= 0) return NC_ERR_INVALID;
     if ((window < 1 && window != NC_WINDOW_FULL) || !(scale > 0.f) || scale > 3.4e38f) return NC_ERR_INVALID;
     if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
-    if ((int64_t)N * H >= (int64_t(1) << 31) || (int64_t)Tmax * H * D >= (int64_t(1) << 40)) return NC_ERR_UNSUPPORTED;
+    if (!sizes_supported(N, Tmax, H, D)) return NC_ERR_UNSUPPORTED;
     if (!q || !kcache || !vcache || !cache_lens || !o) return NC_ERR_INVALID;
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return NC_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return NC_ERR_INVALID;
-    if (o == q || o == kcache || o == vcache || (lse != nullptr && (void*)lse == o)) return NC_ERR_INVALID;
+    // the same byte-range checks as nc_attn_decode: no output may overlap an input or the other output
+    const size_t nq = (size_t)N * H * D * 2, nc_ = (size_t)N * Tmax * H * D * 2, nl = (size_t)N * H * 4;
+    const void* ins[4] = {q, kcache, vcache, cache_lens};
+    const size_t in_n[4] = {nq, nc_, nc_, (size_t)N * 4};
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_n[i], o, nq) || (lse != nullptr && overlap(ins[i], in_n[i], lse, nl)))
+            return NC_ERR_INVALID;
+    if (lse != nullptr && overlap(o, nq, lse, nl)) return NC_ERR_INVALID;
     const size_t need = nc_attn_decode_noalloc_scratch_bytes(N, Tmax, H, D, window);
     if (need > (size_t)NC_DECODE_NOALLOC_SCRATCH_BYTES) return NC_ERR_WORKSPACE;
     unsigned char* scratch = static_cast<unsigned char*>(scratch_address());

@@ -738,47 +738,27 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.n_pairs = ((cu != nullptr ? max_len : Tq) + 2 * kBM - 1) / (2 * kBM);
     p.err = err;
     const int smem = FwdSmem<D>::kBytes;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // Host-side state is looked up on every call (kernel attribute, SM count, the counter ring's
+    // address) rather than cached, so concurrent first calls from several host threads, and calls
+    // after a device reset, need no synchronisation.
+    auto kern = cu != nullptr ? fwd_tc_kernel<D, kModeVarlen>
+                              : (lens != nullptr ? fwd_tc_kernel<D, kModeCache> : fwd_tc_kernel<D, kModePlain>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModePlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModeCache>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fwd_tc_kernel<D, kModeVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set[dev] = true;
-    }
     // persistent: one CTA per SM (shared memory and TMEM allow one), looping over the items
-    static int sms[64] = {0};
-    if (dev < 64 && sms[dev] == 0) {
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int n_sm = 0;
+    e = multiprocessor_count(&n_sm);
+    if (e != cudaSuccess) return e;
     const long n_items = (long)p.n_pairs * H * (cu != nullptr ? n_docs : B);
-    const int n_sm = dev < 64 ? sms[dev] : 148;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     if (cu != nullptr) {
-        static int* work_base[64] = {nullptr};
         static std::atomic<unsigned> work_seq{0};
-        int* wb = dev < 64 ? work_base[dev] : nullptr;
-        if (wb == nullptr) {
-            void* ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_fwd_work);
-            if (e != cudaSuccess) return e;
-            wb = static_cast<int*>(ptr);
-            if (dev < 64) work_base[dev] = wb;
-        }
-        p.work = wb + 2 * (work_seq.fetch_add(1u) % kWorkSlots);
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_fwd_work);
+        if (e != cudaSuccess) return e;
+        p.work = static_cast<int*>(ptr) + 2 * (work_seq.fetch_add(1u) % kWorkSlots);
     }
-    if (cu != nullptr)
-        fwd_tc_kernel<D, kModeVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
-    else if (lens != nullptr)
-        fwd_tc_kernel<D, kModeCache><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
-    else
-        fwd_tc_kernel<D, kModePlain><<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, p);
     count_launches(1);
     return cudaGetLastError();
 }

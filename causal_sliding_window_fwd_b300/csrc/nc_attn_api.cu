@@ -14,19 +14,13 @@ namespace {
 
 __device__ int g_nc_error_word;
 
-constexpr int kMaxDevices = 64;
-int* g_err_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the error word on the current device (looked up once per device).
+// Device address of the error word on the current device.  Looked up on every call (a cheap
+// runtime query) instead of being cached per device, so concurrent first calls from several host
+// threads need no synchronisation and a device reset leaves nothing stale behind.
 int* error_word() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (g_err_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_nc_error_word) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<int*>(p);
-    }
-    return g_err_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_nc_error_word) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -297,6 +291,12 @@ namespace {
 std::atomic<unsigned long long> g_launches{0};
 }
 int* device_error_word() { return error_word(); }
+cudaError_t multiprocessor_count(int* n) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+}
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 }  // namespace nc

@@ -9,7 +9,11 @@ void count_launches(unsigned n);
 unsigned long long launch_count();
 
 // Device address of the library's sticky error word on the current device (nullptr on failure).
+// Looked up on every call: the library keeps no per-device host-side cache.
 int* device_error_word();
+
+// Number of SMs of the current device.
+cudaError_t multiprocessor_count(int* n);
 
 // Forward: o [B,T,H,D] bf16, lse [B,H,T] fp32.  `err` is the device error word.
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,

@@ -36,6 +36,13 @@
  * must be 16-byte aligned (the kernels move data with TMA and 16-byte
  * vectors).  Outputs must not alias inputs or each other.
  *
+ * Threads: every entry point may be called from any host thread, including
+ * several threads making their first calls at the same time.  The library keeps
+ * no per-device host-side cache: each call looks up what it needs (kernel
+ * attributes, the SM count, the device addresses of its own __device__
+ * variables) with the caller's device current.  The only shared host state is
+ * an atomic launch counter.
+ *
  * Errors: host-side argument checks return a status synchronously and launch
  * nothing.  Conditions only the device can see (a decode cache length
  * outside [1, Tmax], a pipeline wait that exceeded its time limit) set a
@@ -191,9 +198,10 @@ nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
  *   o          : bf16 [N, Tq, H, D] device, written
  *   lse        : fp32 [N, H, Tq] device, written
  * The cache is read in 128-row blocks: rows from L up to the end of the
- * 128-row block that holds row L - 1 are loaded and masked out, so they must
- * hold finite values (any finite values, e.g. the zeros of a fresh cache).
- * Rows beyond that block are never read.  Needs no workspace; Tq <= Tmax.
+ * 128-row block that holds row L - 1 are loaded and masked out (their value
+ * rows are zeroed on chip before use), so they may hold anything, NaN
+ * included.  Rows beyond that block are never read.  Needs no workspace;
+ * Tq <= Tmax.
  */
 nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
                           void* o, float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
@@ -231,15 +239,18 @@ nc_status nc_debug_watchdog_selftest(unsigned long long limit_cycles, cudaStream
  * scratch than that (see nc_attn_decode_noalloc_scratch_bytes) return
  * NC_ERR_WORKSPACE and launch nothing.  The call never allocates.
  *
- * The first call on a device looks up the scratch array's device address with
- * that device current; make it before any stream capture.  All calls on a
- * device share the array (it keeps the last call's contents; nothing in it
- * needs to start at zero), so calls whose GPU work overlaps race on it: the
- * caller must order them, e.g. on one stream.
+ * Every call looks up the scratch array's device address with the caller's
+ * device current; the first call on a device may load the library's device
+ * code, so make it before any stream capture.  All calls on a device share the
+ * array (it keeps the last call's contents; nothing in it needs to start at
+ * zero), so calls whose GPU work overlaps race on it: the caller must order
+ * them, e.g. on one stream.  The outputs may not overlap any input or each
+ * other (byte ranges, as for nc_attn_decode).
  */
 #define NC_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
-/* Scratch bytes nc_attn_decode_noalloc would use for these sizes (0 if invalid). */
+/* Scratch bytes nc_attn_decode_noalloc would use for these sizes; 0 for sizes or a window that it
+ * rejects (non-positive sizes, D not 64 or 128, a bad window, or N*H >= 2^31 or Tmax*H*D >= 2^40). */
 size_t nc_attn_decode_noalloc_scratch_bytes(int N, int Tmax, int H, int D, int window);
 
 nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* cache_lens,

@@ -5,8 +5,10 @@ import ctypes
 import math
 import os
 import re
+import threading
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -56,8 +58,12 @@ def test_workspace_sizes(lib):
 
 
 # Fake, 16-byte aligned and non-overlapping "device" addresses: validation must
-# reject each call below before any CUDA call is made.
+# reject each call below before any CUDA call is made.  These tests run only where
+# no GPU is present, so a change in the order of the checks can never hand a fake
+# address to a kernel on a real device.
 A = [0x10000000 + i * 0x10000000 for i in range(12)]
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="passes fake device addresses; run on a host without a GPU")
 GOOD = dict(B=2, T=64, H=2, D=64, window=16, scale=0.125)
 
 
@@ -68,6 +74,7 @@ def _fwd(lib, ptrs=None, **kw):
                                ctypes.c_float(a["scale"]), None)
 
 
+@host_only
 @pytest.mark.parametrize("kw,code", [
     (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1),
     (dict(D=96), 2), (dict(D=256), 2),
@@ -78,6 +85,7 @@ def test_fwd_rejects_bad_sizes(lib, kw, code):
     assert _fwd(lib, **kw) == code
 
 
+@host_only
 def test_fwd_rejects_null_misaligned_and_aliased(lib):
     for i in range(5):
         p = list(A[:5]); p[i] = 0
@@ -100,6 +108,7 @@ def _bwd(lib, ptrs=None, ws=None, ws_bytes=None, fn="nc_attn_bwd", **kw):
                                 ctypes.c_float(a["scale"]), ctypes.c_void_p(ws), ws_bytes, None)
 
 
+@host_only
 @pytest.mark.parametrize("fn", ["nc_attn_bwd", "nc_attn_bwd_deterministic"])
 def test_bwd_rejects_bad_arguments(lib, fn):
     assert _bwd(lib, D=80, fn=fn) == lib.NC_ERR_UNSUPPORTED
@@ -129,6 +138,7 @@ def _dec(lib, ptrs=None, ws_bytes=None, **kw):
                                   ctypes.c_void_p(A[10]), ws_bytes, None)
 
 
+@host_only
 def test_decode_rejects_bad_arguments(lib):
     assert _dec(lib, N=0) == lib.NC_ERR_INVALID
     assert _dec(lib, D=32) == lib.NC_ERR_UNSUPPORTED
@@ -154,6 +164,7 @@ def _pre(lib, ptrs=None, **kw):
                                    ctypes.c_float(a["scale"]), None)
 
 
+@host_only
 def test_prefill_rejects_bad_arguments(lib):
     assert _pre(lib, N=0) == lib.NC_ERR_INVALID
     assert _pre(lib, Tq=0) == lib.NC_ERR_INVALID
@@ -181,6 +192,7 @@ def _fvl(lib, ptrs=None, **kw):
                                       ctypes.c_float(a["scale"]), None)
 
 
+@host_only
 def test_fwd_varlen_rejects_bad_arguments(lib):
     assert lib.status_string(7) == "NC_ERR_BAD_SEQLENS"
     assert _fvl(lib, n_docs=0) == lib.NC_ERR_INVALID
@@ -198,6 +210,7 @@ def test_fwd_varlen_rejects_bad_arguments(lib):
     assert _fvl(lib, p) == lib.NC_ERR_INVALID
 
 
+@host_only
 def test_bwd_varlen_rejects_bad_arguments(lib):
     def call(ptrs=None, ws_bytes=None, **kw):
         a = dict(n_docs=3, total=512, max_seqlen=300, H=2, D=128, window=64, scale=0.1)
@@ -217,3 +230,64 @@ def test_bwd_varlen_rejects_bad_arguments(lib):
         assert call(p) == lib.NC_ERR_INVALID
     p = list(A[:10]); p[7] = p[1]            # dq aliases k
     assert call(p) == lib.NC_ERR_INVALID
+
+
+def _noalloc(lib, ptrs, N=4, Tmax=256, H=2, D=128, window=64):
+    return lib.lib.nc_attn_decode_noalloc(*[ctypes.c_void_p(x) if x is not None else None for x in ptrs],
+                                          N, Tmax, H, D, window, ctypes.c_float(0.1), None)
+
+
+@host_only
+def test_decode_noalloc_rejects_the_overlaps_decode_rejects(lib):
+    """Byte ranges, not just pointer equality: no output may overlap an input or the other output."""
+    N, Tmax, H, D = 4, 256, 2, 128
+    p = list(A[:6]); p[4] = p[1] + 4096          # o inside the key cache
+    assert _noalloc(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[5] = p[0] + 16            # lse overlapping q
+    assert _noalloc(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[5] = p[3]                 # lse over cache_lens
+    assert _noalloc(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[5] = p[4] + 32            # lse inside o
+    assert _noalloc(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:6]); p[4] = p[2] + 2 * N * Tmax * H * D - 16   # o straddling the end of the value cache
+    assert _noalloc(lib, p) == lib.NC_ERR_INVALID
+    # the same placements are refused by the workspace decode
+    p = list(A[:6]); p[4] = p[1] + 4096
+    assert _dec(lib, p) == lib.NC_ERR_INVALID
+
+
+def test_noalloc_scratch_bytes_follow_the_call_limits(lib):
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(64, 8192, 10, 128, 1024) > 0
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(0, 8192, 10, 128, 1024) == 0
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(64, 8192, 10, 96, 1024) == 0
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(64, 8192, 10, 128, 0) == 0
+    # sizes the call refuses as unsupported (N*H >= 2^31, Tmax*H*D >= 2^40) get 0, not a size
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(1 << 22, 256, 1 << 9, 64, 64) == 0
+    assert lib.nc_attn_decode_noalloc_scratch_bytes(1, 1 << 30, 1 << 4, 128, 64) == 0
+
+
+@host_only
+def test_abi_calls_from_many_threads(lib):
+    """Entry points called from many host threads at once give each caller its own answer (the
+    library keeps no per-device host state that first calls could race on)."""
+    errors = []
+
+    def worker(k):
+        try:
+            for i in range(200):
+                assert _fwd(lib, D=96) == lib.NC_ERR_UNSUPPORTED
+                assert _fwd(lib, window=0) == lib.NC_ERR_INVALID
+                p = list(A[:5]); p[3] = p[0]
+                assert _fwd(lib, p) == lib.NC_ERR_INVALID
+                assert _bwd(lib, ws_bytes=16) == lib.NC_ERR_WORKSPACE
+                assert lib.nc_attn_bwd_workspace_bytes(2, 64 + i, 2, 64) > 0
+                assert lib.status_string((i + k) % 8).startswith("NC_")
+        except AssertionError as e:  # pragma: no cover - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(16)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]
