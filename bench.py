@@ -1,13 +1,15 @@
 #!/usr/bin/env python
 """Benchmark: sliding-window causal attention forward+backward on one B300.
 
-One step = forward + backward of the depth-20-like training layer pair
-(B=16, T=2048, H=10, D=128; one call with window 1024 and one full-causal
-call), inputs resident in HBM.  The metric is useful TFLOP/s: 14 * D flops
-per in-window (query, key) pair (4*D forward, 10*D backward), divided by the
-device time of the step.  Single-token KV-cache decode (64 sequences, lengths
-U[256, 8192], windows 1024 and full) is timed after the step loop and
-reported in its own object.
+One step = the attention of a depth-20 model's 20 layers: 10 passes of the
+depth-20-like training layer pair (B=16, T=2048, H=10, D=128; one call with
+window 1024 and one full-causal call), forward + backward, inputs resident in
+HBM.  The metric is useful TFLOP/s: 14 * D flops per in-window (query, key)
+pair (4*D forward, 10*D backward), divided by the device time of the step.
+The other training configurations (the depth-30-like alternating layer, the
+long-context layer, the tiny case), single-token KV-cache decode, prefill,
+document-masked attention and the deterministic backward are timed after the
+step loop and reported in their own objects.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -36,6 +38,30 @@ import torch  # noqa: E402
 from causal_sliding_window_fwd_b300 import workloads  # noqa: E402
 
 METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor peak"
+
+# DRAM traffic per call, read + write (ncu dram__bytes_read.sum + dram__bytes_write.sum on the layer pair's
+# shapes, profiles/dram_traffic_d20_pair.md), valid only while the kernel source is the one that was captured
+# (sha256 of the .cu file); otherwise the bench reports null.
+TRAFFIC = {
+    "nc_attn_bwd": {"src": "causal_sliding_window_fwd_b300/csrc/bwd_sm103.cu",
+                    "sha256": "82ffd1d919772ba21bd100369fecee9b1ddf349a99f3dc7000b3ff4451a638a3",
+                    "bytes": {1024: 167795712 + 118093056 + 506067712 + 284666368 + 167781632 + 46675968,
+                              2048: 167796224 + 118525696 + 506013952 + 284948736 + 167776512 + 47624448}},
+    "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
+                    "sha256": "5ee54cad6b1e648f194109827e3cfcf874b631b1a4998509fb1ba606b3ebb113",
+                    "bytes": {1024: 609840640 + 61052160, 2048: 736825088 + 61344512}},
+}
+
+
+def traffic_per_call(call_name: str, window: int):
+    """Measured DRAM bytes of one call of `call_name` at `window` on the layer pair, or None when the kernel
+    source no longer matches the capture."""
+    import hashlib
+    t = TRAFFIC[call_name]
+    path = os.path.join(ROOT, t["src"])
+    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != t["sha256"]:
+        return None
+    return t["bytes"].get(window)
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -49,6 +75,9 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the depth-30, long-context and tiny lines")
+    ap.add_argument("--pairs-per-step", type=int, default=10,
+                    help="layer pairs per step (10: the 20 attention layers of a depth-20 model)")
     return ap.parse_args()
 
 
@@ -66,6 +95,14 @@ def useful_flops(call) -> float:
 
 def fwd_flops(call) -> float:
     return 4.0 * call.D * call.B * call.H * workloads.pairs_in_window(call.T, call.window)
+
+
+def min_bytes(call, which: str) -> int:
+    """Algorithmic HBM bytes of one call: fwd reads q, k, v and writes o, lse; bwd reads q, k, v, o, dO, lse
+    and writes dq, dk, dv."""
+    t = call.B * call.T * call.H * call.D * 2
+    lse = call.B * call.H * call.T * 4
+    return 3 * t + t + lse if which == "fwd" else 5 * t + lse + 3 * t
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -229,7 +266,7 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
 
     def step(ev_list=None):
-        for call, b in zip(calls, bufs):
+        for call, b in [cb for _ in range(args.pairs_per_step) for cb in zip(calls, bufs)]:
             if ev_list is not None:
                 e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
                 e0.record(stream)
@@ -271,7 +308,7 @@ def run_ours(args, dist: Dist):
     ms_total = start.elapsed_time(end)
     ms_total = dist.max(ms_total)
     ms_per_step = ms_total / args.steps
-    flops_step = sum(useful_flops(c) for c in calls)
+    flops_step = args.pairs_per_step * sum(useful_flops(c) for c in calls)
     value = dist.world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
 
     fwd_ms = sum(e0.elapsed_time(e1) for _, e0, e1, _ in evs)
@@ -291,18 +328,32 @@ def run_ours(args, dist: Dist):
 
     dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
     dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
-    roofline = {"bound": "tensor", "kernel": "nc_attn_bwd (all kernels of the call)" if dominant == "bwd"
-                else "nc_attn_fwd", "achieved": round(dom_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": round(dom_tf / peak_tf, 4), "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                "traffic": None,
-                "fwd": {"achieved": round(fwd_tf, 2), "frac": round(fwd_tf / peak_tf, 4)},
-                "bwd": {"achieved": round(bwd_tf, 2), "frac": round(bwd_tf / peak_tf, 4)},
-                "step_frac": round(value / dist.world / peak_tf, 4)}
+    # The timed region runs a few hundred ms of back-to-back kernels, long enough for the board to reach
+    # its power cap, so the denominator is the measured sustained bf16 peak (a seconds-long cuBLAS loop);
+    # the fraction of the burst peak is reported beside it.
+    peak_sus = peaks.get("bf16_tflops_sustained", peak_tf)
+    name = "nc_attn_bwd" if dominant == "bwd" else "nc_attn_fwd"
+    tr = [traffic_per_call(name, c.window) for c in calls]
+    traffic = None if any(t is None for t in tr) else int(sum(tr) / len(tr))
+    roofline = {"bound": "tensor", "kernel": f"{name} (all kernels of the call)", "achieved": round(dom_tf, 2),
+                "peak": peak_sus, "unit": "TFLOP/s", "frac": round(dom_tf / peak_sus, 4),
+                "peak_kind": f"{peak_kind} bf16 dense (sustained; timed region {ms_total:.0f} ms)",
+                "frac_of_burst_peak": round(dom_tf / peak_tf, 4), "burst_peak": peak_tf,
+                "traffic": traffic, "traffic_unit": "bytes per call (DRAM read + write, ncu)",
+                "algorithmic_bytes_per_call": int(sum(min_bytes(c, dominant) for c in calls) / len(calls)),
+                "fwd": {"achieved": round(fwd_tf, 2), "frac": round(fwd_tf / peak_sus, 4),
+                        "frac_of_burst_peak": round(fwd_tf / peak_tf, 4)},
+                "bwd": {"achieved": round(bwd_tf, 2), "frac": round(bwd_tf / peak_sus, 4),
+                        "frac_of_burst_peak": round(bwd_tf / peak_tf, 4)},
+                "step_frac": round(value / dist.world / peak_sus, 4),
+                "step_frac_of_burst_peak": round(value / dist.world / peak_tf, 4)}
 
     out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic N(0,1) bf16, seeded",
            "config": {"workload": wl.name, "model": "depth-20-like attention layer pair (fwd+bwd)",
+                      "pairs_per_step": args.pairs_per_step,
+                      "timed_region_ms": round(ms_total, 2),
                       "global_batch": 16 * dist.world, "seq_len": 2048, "heads": 10, "head_dim": 128,
                       "windows": [c.window for c in calls], "parallelism": f"replicas x{dist.world}",
                       "l2": "inputs larger than L2 (q,k,v,dO = 335 MB per call, 671 MB per step)",
@@ -311,6 +362,9 @@ def run_ours(args, dist: Dist):
 
     if not args.no_e2e:
         out["e2e"] = run_e2e(calls, bufs, stream, dist, nc_attn, args)
+    if not args.no_configs:
+        out["training_configs"] = run_training_configs(dev, stream, nc_attn, peaks, peak_kind,
+                                                       with_oracle=(dist.rank == 0 and not args.no_cpu_baseline))
     if not args.no_decode:
         out["decode"] = run_decode(dev, stream, nc_attn, peaks, peak_kind)
         out["prefill"] = run_prefill(dev, stream, nc_attn, peaks, peak_kind)
@@ -320,8 +374,10 @@ def run_ours(args, dist: Dist):
 
 
 def run_e2e(calls, bufs, stream, dist, nc_attn, args):
-    """Same metric through the C-ABI calls with host buffers: H2D of the step's inputs
-    from pinned memory, fwd + bwd, D2H of o, lse, dq, dk, dv, every step."""
+    """Same metric through the C-ABI calls with host buffers: every step copies each call's q, k, v,
+    dO from pinned host memory, runs fwd + bwd, and copies o, lse, dq, dk, dv back.  Host-to-device
+    copies, kernels and device-to-host copies run on three streams ordered by events, so one call's
+    copies overlap the other call's kernels (PCIe is full duplex)."""
     host_in, host_out = [], []
     for b in bufs:
         host_in.append({k: b[k].cpu().pin_memory() for k in ("q", "k", "v", "dO")})
@@ -329,32 +385,158 @@ def run_e2e(calls, bufs, stream, dist, nc_attn, args):
                          for k in ("o", "lse", "dq", "dk", "dv")})
     h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
     d2h = sum(t.numel() * t.element_size() for d in host_out for t in d.values())
+    dev = bufs[0]["q"].device
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = len(calls)
+    out_done = [None] * n   # event: the previous device-to-host copy of call c has read its buffers
 
     def step():
-        for call, b, hi, ho in zip(calls, bufs, host_in, host_out):
-            for k in ("q", "k", "v", "dO"):
-                b[k].copy_(hi[k], non_blocking=True)
+        for c, (call, b, hi, ho) in enumerate(zip(calls, bufs, host_in, host_out)):
+            with torch.cuda.stream(s_in):
+                if out_done[c] is not None:
+                    s_in.wait_event(out_done[c])
+                for k in ("q", "k", "v", "dO"):
+                    b[k].copy_(hi[k], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
             nc_attn.nc_attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], call.window, call.scale, stream)
             nc_attn.nc_attn_bwd(b["q"], b["k"], b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"],
                                 call.window, call.scale, b["ws"], stream)
-            for k in ("o", "lse", "dq", "dk", "dv"):
-                ho[k].copy_(b[k], non_blocking=True)
+            ev_k = torch.cuda.Event()
+            ev_k.record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_k)
+                for k in ("o", "lse", "dq", "dk", "dv"):
+                    ho[k].copy_(b[k], non_blocking=True)
+                out_done[c] = torch.cuda.Event()
+                out_done[c].record(s_out)
 
     steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
+    step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(s_in)
+    stream.wait_event(s)
+    s_out.wait_event(s)
+    for _ in range(steps):
         step()
-        torch.cuda.synchronize()
-        dist.barrier()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            step()
-        e.record(stream)
+    # the end event follows the last copies back
+    s_in.wait_stream(s_out)
+    s_in.wait_stream(stream)
+    e.record(s_in)
     torch.cuda.synchronize()
     ms = dist.max(s.elapsed_time(e)) / steps
     flops = sum(useful_flops(c) for c in calls)
     return {"value": round(dist.world * flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
-            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "step": "one layer pair (both calls), copies in and out included",
+            "overlap": "host-to-device, kernels and device-to-host on three streams ordered by events"}
+
+
+def oracle_config_sample(call, slices: int, rows: int):
+    """Time the fp64 oracle (fwd + bwd) on `slices` (b, h) slices of `call`, first `rows` positions
+    (a causal prefix is itself a valid problem).  Returns (useful TFLOP/s, seconds, threads used)."""
+    import oracle
+    oracle.build()
+    T = min(rows, call.T)
+    full = workloads.make_qkvdo(workloads.AttnCall(1, call.T, min(call.H, slices), call.D, call.window, call.seed),
+                                "cpu")
+    q, k, v, dO = (x[:1, :T].contiguous() for x in full)
+    sub = workloads.AttnCall(1, T, q.shape[2], call.D, call.window, call.seed)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, call.window, call.scale)
+    oracle.bwd(q, k, v, dO, call.window, call.scale)
+    secs = time.perf_counter() - t0
+    return useful_flops(sub) / secs / 1e12, secs, min(oracle.num_threads(), q.shape[2])
+
+
+def run_training_configs(dev, stream, nc_attn, peaks, peak_kind, with_oracle: bool):
+    """The other training configurations, each call timed on its own (fwd and bwd, CUDA events on the
+    launching stream, inputs larger than L2 so each call streams them from HBM), and the tiny case as
+    a latency line."""
+    peak = peaks["bf16_tflops"]
+    res = {}
+    for wl, key, sample in ((workloads.D30_ALT, "d30", (8, 2048)), (workloads.LONG_SW, "long", (16, 2048))):
+        bufs = []
+        for call in wl.calls:
+            q, k, v, dO = workloads.make_qkvdo(call, dev)
+            B, T, H, D = call.shape
+            bufs.append((call, q, k, v, dO, torch.empty_like(q), torch.empty((B, H, T), dtype=torch.float32, device=dev),
+                         torch.empty_like(q), torch.empty_like(q), torch.empty_like(q),
+                         torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=dev)))
+        evs = []
+
+        def one_pass(record):
+            for (call, q, k, v, dO, o, lse, dq, dk, dv, ws) in bufs:
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+                nc_attn.nc_attn_fwd(q, k, v, o, lse, call.window, call.scale, stream)
+                e1.record(stream)
+                nc_attn.nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, call.window, call.scale, ws, stream)
+                e2.record(stream)
+                if record:
+                    evs.append((call, e0, e1, e2))
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                one_pass(False)
+            torch.cuda.synchronize()
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            n_pass = 20
+            for _ in range(n_pass):
+                one_pass(True)
+            end.record(stream)
+        torch.cuda.synchronize()
+        assert nc_attn.nc_get_device_error(stream) == 0
+        total_ms = start.elapsed_time(end) / n_pass
+        per_call = []
+        for i, call in enumerate(wl.calls):
+            f = statistics.median([e0.elapsed_time(e1) for c, e0, e1, _ in evs if c is call])
+            b = statistics.median([e1.elapsed_time(e2) for c, _, e1, e2 in evs if c is call])
+            per_call.append({"window": call.window, "fwd_us": round(f * 1e3, 1), "bwd_us": round(b * 1e3, 1),
+                             "fwd_TFLOP_s": round(fwd_flops(call) / (f * 1e-3) / 1e12, 1),
+                             "bwd_TFLOP_s": round((useful_flops(call) - fwd_flops(call)) / (b * 1e-3) / 1e12, 1)})
+        flops = sum(useful_flops(c) for c in wl.calls)
+        tf = flops / (total_ms * 1e-3) / 1e12
+        entry = {"workload": wl.name, "ms_per_pass": round(total_ms, 4), "TFLOP_s": round(tf, 1),
+                 "passes_timed": n_pass, "per_call": per_call,
+                 "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                              "frac": round(tf / peak, 4), "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                              "traffic": None}}
+        if with_oracle:
+            slices, rows = sample
+            v_or, secs, thr = oracle_config_sample(wl.calls[0], slices, rows)
+            entry["cpu_baseline"] = {"value": v_or, "unit": UNIT, "cores": thr, "kind": "oracle",
+                                     "sample": f"fp64 oracle fwd+bwd, {slices} (b,h) slices x first {rows} rows of "
+                                               f"the first call (W={wl.calls[0].window})",
+                                     "seconds": round(secs, 2)}
+        res[key] = entry
+        del bufs
+    # tiny: latency of one fwd + bwd call through the C ABI (correctness case; not a throughput figure)
+    call = workloads.TINY.calls[0]
+    q, k, v, dO = workloads.make_qkvdo(call, dev)
+    B, T, H, D = call.shape
+    o, lse = torch.empty_like(q), torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(60):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            nc_attn.nc_attn_fwd(q, k, v, o, lse, call.window, call.scale, stream)
+            nc_attn.nc_attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, call.window, call.scale, ws, stream)
+            e1.record(stream)
+            if i >= 10:
+                times.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median([a.elapsed_time(b) for a, b in times]) * 1e3
+    res["tiny"] = {"workload": workloads.TINY.name, "fwd_bwd_us": round(us, 2),
+                   "note": "latency-bound correctness case (four launches); not scored against the roofline"}
+    return res
 
 
 def decode_bytes(lens, wl, window):

@@ -489,8 +489,10 @@ cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void
     p.err = err;
     p.dq32 = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     const int smem = DqSmem<D>::kBytes;
-    // kernel attribute and SM count are looked up on every call (no host-side cache to race on)
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the shared-memory limit is raised once per device (atomic flags), the SM count is looked up
+    // on every call
+    static std::atomic<bool> attr_done[kAttrDevices];
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel<D>), smem, attr_done);
     if (e != cudaSuccess) return e;
     int n_sm = 0;
     e = multiprocessor_count(&n_sm);

@@ -957,10 +957,13 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     p.n_docs = n_docs;
     p.err = err;
     const int smem = BwdSmem<D>::kBytes;
-    // kernel attribute and SM count are looked up on every call (no host-side cache to race on)
-    auto kern = deterministic ? bwd_main_kernel<D, false, true>
-                              : (cu != nullptr ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the shared-memory limit is raised once per device and variant (atomic flags), the SM count
+    // is looked up on every call
+    static std::atomic<bool> attr_done[3][kAttrDevices];
+    const int variant = deterministic ? 2 : (cu != nullptr ? 1 : 0);
+    auto kern = variant == 2 ? bwd_main_kernel<D, false, true>
+                             : (variant == 1 ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, attr_done[variant]);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (its shared memory and TMEM allow one), looping over the items
     int n_sm = 0;

@@ -738,12 +738,14 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.n_pairs = ((cu != nullptr ? max_len : Tq) + 2 * kBM - 1) / (2 * kBM);
     p.err = err;
     const int smem = FwdSmem<D>::kBytes;
-    // Host-side state is looked up on every call (kernel attribute, SM count, the counter ring's
-    // address) rather than cached, so concurrent first calls from several host threads, and calls
-    // after a device reset, need no synchronisation.
-    auto kern = cu != nullptr ? fwd_tc_kernel<D, kModeVarlen>
-                              : (lens != nullptr ? fwd_tc_kernel<D, kModeCache> : fwd_tc_kernel<D, kModePlain>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The SM count and the counter ring's address are looked up on every call, the shared-memory
+    // limit is raised once per device and variant (atomic flags): nothing that concurrent first calls
+    // from several host threads could race on.
+    static std::atomic<bool> attr_done[3][kAttrDevices];
+    const int variant = cu != nullptr ? 2 : (lens != nullptr ? 1 : 0);
+    auto kern = variant == 2 ? fwd_tc_kernel<D, kModeVarlen>
+                             : (variant == 1 ? fwd_tc_kernel<D, kModeCache> : fwd_tc_kernel<D, kModePlain>);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, attr_done[variant]);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (shared memory and TMEM allow one), looping over the items
     int n_sm = 0;

@@ -291,6 +291,15 @@ namespace {
 std::atomic<unsigned long long> g_launches{0};
 }
 int* device_error_word() { return error_word(); }
+cudaError_t ensure_smem_attr(const void* kern, int bytes, std::atomic<bool>* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kAttrDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < kAttrDevices) done[dev].store(true, std::memory_order_release);
+    return e;
+}
 cudaError_t multiprocessor_count(int* n) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -1,5 +1,6 @@
 // Internal launch interface of the forward / backward attention kernels.
 #pragma once
+#include <atomic>
 #include <cuda_runtime_api.h>
 
 namespace nc {
@@ -14,6 +15,13 @@ int* device_error_word();
 
 // Number of SMs of the current device.
 cudaError_t multiprocessor_count(int* n);
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once per device and
+// kernel (`done` is that kernel's per-device flag array of kAttrDevices entries, zero at load).  Host
+// threads racing on a first call may both set it, which is harmless; the flag is atomic.  A stale flag
+// (after a device reset) can only make the launch fail with an error, never touch memory.
+constexpr int kAttrDevices = 64;
+cudaError_t ensure_smem_attr(const void* kern, int bytes, std::atomic<bool>* done);
 
 // Forward: o [B,T,H,D] bf16, lse [B,H,T] fp32.  `err` is the device error word.
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,

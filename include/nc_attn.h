@@ -37,11 +37,11 @@
  * vectors).  Outputs must not alias inputs or each other.
  *
  * Threads: every entry point may be called from any host thread, including
- * several threads making their first calls at the same time.  The library keeps
- * no per-device host-side cache: each call looks up what it needs (kernel
- * attributes, the SM count, the device addresses of its own __device__
- * variables) with the caller's device current.  The only shared host state is
- * an atomic launch counter.
+ * several threads making their first calls at the same time.  Each call looks
+ * up the device addresses of the library's own __device__ variables and the SM
+ * count with the caller's device current; the only shared host state is an
+ * atomic launch counter and atomic per-device flags recording that a kernel's
+ * shared-memory limit has been raised.
  *
  * Errors: host-side argument checks return a status synchronously and launch
  * nothing.  Conditions only the device can see (a decode cache length
