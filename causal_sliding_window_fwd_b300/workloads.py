@@ -245,3 +245,13 @@ def pairs_in_window(T: int, window: int) -> int:
     """Number of (query, key) pairs with j <= i and i - j < W in one row of length T."""
     W = T if (window <= 0 or window >= T) else window
     return T * W - W * (W - 1) // 2
+
+
+def rope_tables(T: int, D: int, base: float = 10000.0, device="cpu"):
+    """Rotary tables (cos, sin), fp32 [T, D/2], as a Llama-like model precomputes them: row t, column i
+    hold the cosine and sine of t * base^(-2i/D).  Computed in float64 and rounded once to float32; both
+    the CUDA path and the oracle receive these same numbers."""
+    t = torch.arange(T, dtype=torch.float64).unsqueeze(1)
+    inv_freq = base ** (-torch.arange(0, D, 2, dtype=torch.float64) / D)
+    ang = t * inv_freq.unsqueeze(0)
+    return ang.cos().to(torch.float32).to(device), ang.sin().to(torch.float32).to(device)

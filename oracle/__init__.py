@@ -53,6 +53,8 @@ class OracleLib:
         lib.oracle_prefill.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_int), dp, dp,
                                        L, L, L, L, L, L, ctypes.c_double]
         lib.oracle_prefill.restype = ctypes.c_int
+        lib.oracle_rotary.argtypes = [dp, dp, dp, dp, L, L, L, L, ctypes.c_int]
+        lib.oracle_rotary.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -74,6 +76,15 @@ class OracleLib:
         self.lib.oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
                             B, T, H, D, int(window), float(scale))
         return dq, dk, dv
+
+    def rotary(self, x, cos, sin, inverse: bool = False):
+        x = _f64(x)
+        c, s = _f64(cos), _f64(sin)
+        B, T, H, D = x.shape
+        assert c.shape == (T, D // 2) and s.shape == c.shape and D % 2 == 0
+        y = np.empty_like(x)
+        self.lib.oracle_rotary(_ptr(x), _ptr(c), _ptr(s), _ptr(y), B, T, H, D, 1 if inverse else 0)
+        return y
 
     def decode(self, q, kcache, vcache, cache_lens, window: int, scale: float):
         q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
@@ -200,3 +211,22 @@ def decode(q, kcache, vcache, cache_lens, window: int, scale: float):
     [1, Tmax]; that sequence's rows are NaN.
     """
     return _load().decode(q, kcache, vcache, cache_lens, window, scale)
+
+
+def rotary(x, cos, sin, inverse: bool = False):
+    """Rotary position embedding of x [B, T, H, D] (rotate-half pairing, see ``oracle_rotary``);
+    cos, sin: [T, D/2], row t for position t.  ``inverse`` applies the transpose."""
+    return _load().rotary(x, cos, sin, inverse)
+
+
+def fwd_rotary(q, k, v, cos, sin, window: int, scale: float):
+    """Attention with the rotary embedding applied to q and k first (positions 0 .. T-1).
+    Returns (o [B,T,H,D], lse [B,H,T])."""
+    return _load().fwd(rotary(q, cos, sin), rotary(k, cos, sin), v, window, scale)
+
+
+def bwd_rotary(q, k, v, dO, cos, sin, window: int, scale: float):
+    """Gradients of sum(O * dO) for the rotary forward with respect to the unrotated q, k and to v:
+    the attention gradients with respect to the rotated q and k, turned back by the transpose."""
+    dqr, dkr, dv = _load().bwd(rotary(q, cos, sin), rotary(k, cos, sin), v, dO, window, scale)
+    return rotary(dqr, cos, sin, inverse=True), rotary(dkr, cos, sin, inverse=True), dv

@@ -271,6 +271,32 @@ int oracle_prefill(const double* q, const double* kc, const double* vc, const in
     return bad ? -1 : 0;
 }
 
+/* Rotary position embedding of x [B, T, H, D] with tables cosv, sinv [T, D/2] (row t is position t).
+ * "nanochat" walkthrough (page 4, comment thread): the model is Llama-like but simpler.  Reading (the
+ * pages give no formula): Llama's rotate-half pairing, dimension i with dimension i + D/2,
+ *   y_i       = x_i c - x_{i+D/2} s
+ *   y_{i+D/2} = x_i s + x_{i+D/2} c,        c = cos[t][i], s = sin[t][i],
+ * i.e. the pair (x_i, x_{i+D/2}) turned by the angle whose cosine and sine the tables hold.  With
+ * inverse != 0 the transpose is applied (the turn back), which maps the gradient with respect to the
+ * rotated vector to the gradient with respect to x.  q and k are rotated, v is not. */
+void oracle_rotary(const double* x, const double* cosv, const double* sinv, double* y,
+                   long B, long T, long H, long D, int inverse) {
+    long half = D / 2;
+#pragma omp parallel for collapse(2)
+    for (long b = 0; b < B; ++b)
+        for (long t = 0; t < T; ++t)
+            for (long h = 0; h < H; ++h)
+                for (long i = 0; i < half; ++i) {
+                    double c = cosv[(size_t)t * half + i];
+                    double s = sinv[(size_t)t * half + i];
+                    if (inverse) s = -s;
+                    double x1 = x[idx_bthd(b, t, h, i, T, H, D)];
+                    double x2 = x[idx_bthd(b, t, h, i + half, T, H, D)];
+                    y[idx_bthd(b, t, h, i, T, H, D)] = x1 * c - x2 * s;
+                    y[idx_bthd(b, t, h, i + half, T, H, D)] = x1 * s + x2 * c;
+                }
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

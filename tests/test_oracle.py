@@ -476,3 +476,112 @@ def test_varlen_single_document_is_the_forward(oracle_mod):
     of, lf = oracle_mod.fwd(q, k, v, 4, 0.5)
     np.testing.assert_array_equal(o, of)
     np.testing.assert_array_equal(lse, lf)
+
+
+# ---------------------------------------------------------------- rotary embedding (fused prologue)
+# The oracle's rotary is the rotate-half pairing of Llama-like models: the pair (x_i, x_{i+D/2}) of
+# position t is turned by the angle whose cosine and sine the tables hold at (t, i).
+
+
+def _tables(T, D, base=10000.0):
+    c, s = workloads.rope_tables(T, D, base)
+    return c.double().numpy(), s.double().numpy()
+
+
+def test_rotary_matches_complex_rotation(oracle_mod):
+    """The same turn written as complex multiplication: z = x_i + i x_{i+D/2}, z' = z (c + i s)."""
+    B, T, H, D = 2, 9, 3, 8
+    x = _rand((B, T, H, D), 700)
+    c, s = _tables(T, D)
+    y = oracle_mod.rotary(x, c, s)
+    xt = torch.from_numpy(x)
+    z = torch.complex(xt[..., : D // 2], xt[..., D // 2:])
+    e = torch.complex(torch.from_numpy(c), torch.from_numpy(s)).view(1, T, 1, D // 2)
+    zr = z * e
+    expect = torch.cat([zr.real, zr.imag], dim=-1).numpy()
+    np.testing.assert_allclose(y, expect, rtol=0, atol=1e-12)
+
+
+def test_rotary_position_zero_is_identity(oracle_mod):
+    B, T, H, D = 1, 5, 2, 8
+    x = _rand((B, T, H, D), 701)
+    c, s = _tables(T, D)
+    y = oracle_mod.rotary(x, c, s)
+    np.testing.assert_array_equal(y[:, 0], x[:, 0])
+    assert np.abs(y[:, 1:] - x[:, 1:]).max() > 1e-3  # later positions do turn
+
+
+def test_rotary_preserves_norms_and_the_transpose_turns_back(oracle_mod):
+    B, T, H, D = 2, 7, 2, 16
+    x = _rand((B, T, H, D), 702)
+    c, s = _tables(T, D)
+    y = oracle_mod.rotary(x, c, s)
+    half = D // 2
+    pair_x = x[..., :half] ** 2 + x[..., half:] ** 2
+    pair_y = y[..., :half] ** 2 + y[..., half:] ** 2
+    r2 = (c ** 2 + s ** 2).reshape(1, T, 1, half)  # 1 up to the float32 rounding of the tables
+    np.testing.assert_allclose(pair_y, pair_x * r2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle_mod.rotary(y, c, s, inverse=True), x * np.concatenate([r2, r2], -1),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_rotary_scores_depend_on_relative_position(oracle_mod):
+    """With angles t * f_i, the score of a rotated query at position p and a rotated key at p' depends
+    only on p - p'."""
+    T, D = 12, 8
+    a, b = _rand((D,), 703), _rand((D,), 704)
+    c, s = workloads.rope_tables(T, D)
+    # exact angles in float64 (the float32 tables are only used for the layout)
+    ang = np.arange(T)[:, None] * (10000.0 ** (-np.arange(0, D, 2) / D))[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    qa = oracle_mod.rotary(np.broadcast_to(a, (1, T, 1, D)).copy(), c, s)[0, :, 0]
+    kb = oracle_mod.rotary(np.broadcast_to(b, (1, T, 1, D)).copy(), c, s)[0, :, 0]
+    S = qa @ kb.T  # S[p, p']
+    for dlt in range(-(T - 1), T):
+        diag = np.diagonal(S, offset=dlt)
+        np.testing.assert_allclose(diag, diag[0], rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("window", [1, 3, -1])
+def test_rotary_attention_gradients_match_finite_differences(oracle_mod, window):
+    """Gradients of L = sum(O * G) for O = attention(rotary(q), rotary(k), v) with respect to the
+    unrotated q, k and v: the attention gradients turned back by the transpose."""
+    B, T, H, D = 1, 7, 1, 4
+    scale = 0.5
+    c, s = _tables(T, D)
+    base = [_rand((B, T, H, D), 710 + i) for i in range(3)]
+    G = _rand((B, T, H, D), 713)
+
+    def fwd(q, k, v):
+        return oracle_mod.fwd(oracle_mod.rotary(q, c, s), oracle_mod.rotary(k, c, s), v, window, scale)[0]
+
+    dqr, dkr, dv = oracle_mod.bwd(oracle_mod.rotary(base[0], c, s), oracle_mod.rotary(base[1], c, s), base[2],
+                                  G, window, scale)
+    grads = [oracle_mod.rotary(dqr, c, s, inverse=True), oracle_mod.rotary(dkr, c, s, inverse=True), dv]
+    eps = 1e-6
+    rng = np.random.default_rng(9)
+    for which in range(3):
+        for _ in range(10):
+            idx = (0, int(rng.integers(T)), 0, int(rng.integers(D)))
+            plus = [x.copy() for x in base]; plus[which][idx] += eps
+            minus = [x.copy() for x in base]; minus[which][idx] -= eps
+            fd = ((fwd(*plus) * G).sum() - (fwd(*minus) * G).sum()) / (2 * eps)
+            assert abs(fd - grads[which][idx]) < 1e-7, (which, idx, fd, grads[which][idx])
+
+
+def test_rotary_module_functions_compose_as_stated(oracle_mod):
+    """fwd_rotary / bwd_rotary (used by the GPU tests) are the attention of the rotated q, k and the
+    gradients turned back."""
+    import oracle
+    B, T, H, D = 1, 6, 2, 8
+    c, s = workloads.rope_tables(T, D)
+    q, k, v, dO = (torch.from_numpy(_rand((B, T, H, D), 720 + i)) for i in range(4))
+    o, lse = oracle.fwd_rotary(q, k, v, c, s, 3, 0.3)
+    o2, lse2 = oracle_mod.fwd(oracle_mod.rotary(q, c, s), oracle_mod.rotary(k, c, s), v, 3, 0.3)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    g = oracle.bwd_rotary(q, k, v, dO, c, s, 3, 0.3)
+    gr = oracle_mod.bwd(oracle_mod.rotary(q, c, s), oracle_mod.rotary(k, c, s), v, dO, 3, 0.3)
+    np.testing.assert_array_equal(g[0], oracle_mod.rotary(gr[0], c, s, inverse=True))
+    np.testing.assert_array_equal(g[1], oracle_mod.rotary(gr[1], c, s, inverse=True))
+    np.testing.assert_array_equal(g[2], gr[2])

@@ -30,6 +30,13 @@ MUTANTS = {
     "prefill window one key short": (": i - window + 1;\n                    const double* qrow",
                                      ": i - window + 2;\n                    const double* qrow"),
     "prefill reads value of the key row": ("j <= i; ++j) acc += p[j - lo] * vc[", "j <= i; ++j) acc += p[j - lo] * kc["),
+    "rotary sine sign flipped": ("y[idx_bthd(b, t, h, i, T, H, D)] = x1 * c - x2 * s;",
+                                 "y[idx_bthd(b, t, h, i, T, H, D)] = x1 * c + x2 * s;"),
+    "rotary pairs neighbouring dimensions": ("double x2 = x[idx_bthd(b, t, h, i + half, T, H, D)];",
+                                             "double x2 = x[idx_bthd(b, t, h, (i + 1) % D, T, H, D)];"),
+    "rotary transpose not applied": ("if (inverse) s = -s;", "(void)inverse;"),
+    "rotary position off by one": ("double c = cosv[(size_t)t * half + i];\n                    double s = sinv[(size_t)t * half + i];",
+                                   "double c = cosv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];\n                    double s = sinv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];"),
 }
 
 PIN_SUITE = [
@@ -41,6 +48,10 @@ PIN_SUITE = [
     (pins.test_decode_equals_last_forward_row, {"window": 5}),
     (pins.test_prefill_rows_equal_forward_rows, {"window": 4}),
     (pins.test_prefill_brute_force_tiny, {"Tq": 3, "window": 2}),
+    (pins.test_rotary_matches_complex_rotation, {}),
+    (pins.test_rotary_position_zero_is_identity, {}),
+    (pins.test_rotary_preserves_norms_and_the_transpose_turns_back, {}),
+    (pins.test_rotary_attention_gradients_match_finite_differences, {"window": 3}),
 ]
 
 
