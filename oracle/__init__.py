@@ -55,6 +55,8 @@ class OracleLib:
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_rotary.argtypes = [dp, dp, dp, dp, L, L, L, L, ctypes.c_int]
         lib.oracle_rotary.restype = None
+        lib.oracle_round_bf16.argtypes = [dp, L]
+        lib.oracle_round_bf16.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -84,6 +86,11 @@ class OracleLib:
         assert c.shape == (T, D // 2) and s.shape == c.shape and D % 2 == 0
         y = np.empty_like(x)
         self.lib.oracle_rotary(_ptr(x), _ptr(c), _ptr(s), _ptr(y), B, T, H, D, 1 if inverse else 0)
+        return y
+
+    def round_bf16(self, x):
+        y = _f64(x).copy()
+        self.lib.oracle_round_bf16(_ptr(y), y.size)
         return y
 
     def decode(self, q, kcache, vcache, cache_lens, window: int, scale: float):
@@ -219,14 +226,22 @@ def rotary(x, cos, sin, inverse: bool = False):
     return _load().rotary(x, cos, sin, inverse)
 
 
+def round_bf16(x):
+    """x rounded to the nearest bfloat16 value (ties to even), as float64."""
+    return _load().round_bf16(x)
+
+
 def fwd_rotary(q, k, v, cos, sin, window: int, scale: float):
-    """Attention with the rotary embedding applied to q and k first (positions 0 .. T-1).
+    """Attention with the rotary embedding applied to q and k first (positions 0 .. T-1).  The turned
+    q and k are rounded to bf16 (the model's dtype) before the attention.
     Returns (o [B,T,H,D], lse [B,H,T])."""
-    return _load().fwd(rotary(q, cos, sin), rotary(k, cos, sin), v, window, scale)
+    return _load().fwd(round_bf16(rotary(q, cos, sin)), round_bf16(rotary(k, cos, sin)), v, window, scale)
 
 
 def bwd_rotary(q, k, v, dO, cos, sin, window: int, scale: float):
     """Gradients of sum(O * dO) for the rotary forward with respect to the unrotated q, k and to v:
-    the attention gradients with respect to the rotated q and k, turned back by the transpose."""
-    dqr, dkr, dv = _load().bwd(rotary(q, cos, sin), rotary(k, cos, sin), v, dO, window, scale)
+    the attention gradients at the (bf16-rounded) turned q and k, turned back by the transpose.  The
+    rounding is a change of dtype, not of the function: its gradient is taken as the identity."""
+    dqr, dkr, dv = _load().bwd(round_bf16(rotary(q, cos, sin)), round_bf16(rotary(k, cos, sin)), v, dO, window,
+                               scale)
     return rotary(dqr, cos, sin, inverse=True), rotary(dkr, cos, sin, inverse=True), dv

@@ -297,6 +297,24 @@ void oracle_rotary(const double* x, const double* cosv, const double* sinv, doub
                 }
 }
 
+/* Round every value to the nearest bfloat16 (8 significant bits), ties to even, straight from
+ * double (no intermediate float, so no double rounding).  The rotary attention takes the turned q
+ * and k as bf16 tensors, the dtype of the model's activations ("nanochat GPT-2 speedrun" post,
+ * page 2: the attention runs through a bf16 FlashAttention kernel), so the oracle rounds its exact
+ * turn once before the attention.  Values are assumed inside bf16's range (|x| < 2^128); zeros,
+ * infinities and NaN are left as they are. */
+void oracle_round_bf16(double* x, long n) {
+    for (long i = 0; i < n; ++i) {
+        double v = x[i];
+        if (v == 0.0 || !isfinite(v)) continue;
+        int e;
+        frexp(v, &e);          /* v = m 2^e, 0.5 <= |m| < 1: the leading bit has weight 2^(e-1) */
+        int ue = e - 8;        /* weight of the 8th significant bit: bf16's unit in the last place */
+        if (ue < -133) ue = -133; /* below 2^-126 bf16 is subnormal with a fixed unit 2^-133 */
+        x[i] = ldexp(nearbyint(ldexp(v, -ue)), ue); /* nearest integer multiple, ties to even */
+    }
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

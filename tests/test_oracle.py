@@ -576,12 +576,40 @@ def test_rotary_module_functions_compose_as_stated(oracle_mod):
     B, T, H, D = 1, 6, 2, 8
     c, s = workloads.rope_tables(T, D)
     q, k, v, dO = (torch.from_numpy(_rand((B, T, H, D), 720 + i)) for i in range(4))
+    # the turned q and k are rounded to bf16 (values a bf16 tensor can hold) before the attention
+    rq = oracle_mod.round_bf16(oracle_mod.rotary(q, c, s))
+    rk = oracle_mod.round_bf16(oracle_mod.rotary(k, c, s))
+    for r in (rq, rk):
+        np.testing.assert_array_equal(torch.from_numpy(r).to(torch.bfloat16).double().numpy(), r)
     o, lse = oracle.fwd_rotary(q, k, v, c, s, 3, 0.3)
-    o2, lse2 = oracle_mod.fwd(oracle_mod.rotary(q, c, s), oracle_mod.rotary(k, c, s), v, 3, 0.3)
+    o2, lse2 = oracle_mod.fwd(rq, rk, v, 3, 0.3)
     np.testing.assert_array_equal(o, o2)
     np.testing.assert_array_equal(lse, lse2)
     g = oracle.bwd_rotary(q, k, v, dO, c, s, 3, 0.3)
-    gr = oracle_mod.bwd(oracle_mod.rotary(q, c, s), oracle_mod.rotary(k, c, s), v, dO, 3, 0.3)
+    gr = oracle_mod.bwd(rq, rk, v, dO, 3, 0.3)
     np.testing.assert_array_equal(g[0], oracle_mod.rotary(gr[0], c, s, inverse=True))
     np.testing.assert_array_equal(g[1], oracle_mod.rotary(gr[1], c, s, inverse=True))
     np.testing.assert_array_equal(g[2], gr[2])
+
+
+def test_round_bf16_hand_values(oracle_mod):
+    """Nearest bf16 value (8 significant bits), ties to even, worked by hand."""
+    u = 2.0 ** -7  # spacing of bf16 values in [1, 2)
+    cases = [
+        (1.0, 1.0), (1 + u / 2, 1.0), (1 + 3 * u / 2, 1 + 2 * u), (1 + u / 2 + 2.0 ** -30, 1 + u),
+        (-(1 + u / 2 + 2.0 ** -30), -(1 + u)), (1 + u / 2 - 2.0 ** -30, 1.0), (3.0, 3.0),
+        (2 + u, 2.0), (2 + 3 * u, 2 + 4 * u), (0.0, 0.0), (1.0 / 3.0, 0.333984375),
+        (2.0 ** -130 + 2.0 ** -134, 2.0 ** -130), (2.0 ** -130 + 3 * 2.0 ** -134, 2.0 ** -130 + 2.0 ** -132),
+    ]
+    got = oracle_mod.round_bf16(np.array([a for a, _ in cases]))
+    np.testing.assert_array_equal(got, np.array([b for _, b in cases]))
+
+
+def test_round_bf16_matches_torch_float32(oracle_mod):
+    """For values a float32 holds, torch's float32 -> bfloat16 conversion is the same single rounding."""
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(20000) * 2.0 ** rng.integers(-30, 30, 20000)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    got = oracle_mod.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(oracle_mod.round_bf16(got), got)  # already bf16 values stay put

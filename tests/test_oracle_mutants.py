@@ -37,6 +37,8 @@ MUTANTS = {
     "rotary transpose not applied": ("if (inverse) s = -s;", "(void)inverse;"),
     "rotary position off by one": ("double c = cosv[(size_t)t * half + i];\n                    double s = sinv[(size_t)t * half + i];",
                                    "double c = cosv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];\n                    double s = sinv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];"),
+    "bf16 rounding truncates": ("x[i] = ldexp(nearbyint(ldexp(v, -ue)), ue);", "x[i] = ldexp(trunc(ldexp(v, -ue)), ue);"),
+    "bf16 rounding keeps a bit too many": ("int ue = e - 8;", "int ue = e - 9;"),
 }
 
 PIN_SUITE = [
@@ -52,6 +54,8 @@ PIN_SUITE = [
     (pins.test_rotary_position_zero_is_identity, {}),
     (pins.test_rotary_preserves_norms_and_the_transpose_turns_back, {}),
     (pins.test_rotary_attention_gradients_match_finite_differences, {"window": 3}),
+    (pins.test_round_bf16_hand_values, {}),
+    (pins.test_round_bf16_matches_torch_float32, {}),
 ]
 
 
