@@ -27,10 +27,10 @@ WINDOW_FULL = -1
 
 
 def build(force: bool = False) -> str:
-    """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no fast-math)."""
+    """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no fast-math, no contraction of a*b+c)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11",
                                _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -55,6 +55,8 @@ class OracleLib:
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_rotary.argtypes = [dp, dp, dp, dp, L, L, L, L, ctypes.c_int]
         lib.oracle_rotary.restype = None
+        lib.oracle_rotary_f32.argtypes = [dp, dp, dp, dp, L, L, L, L]
+        lib.oracle_rotary_f32.restype = None
         lib.oracle_round_bf16.argtypes = [dp, L]
         lib.oracle_round_bf16.restype = None
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -86,6 +88,15 @@ class OracleLib:
         assert c.shape == (T, D // 2) and s.shape == c.shape and D % 2 == 0
         y = np.empty_like(x)
         self.lib.oracle_rotary(_ptr(x), _ptr(c), _ptr(s), _ptr(y), B, T, H, D, 1 if inverse else 0)
+        return y
+
+    def rotary_f32(self, x, cos, sin):
+        x = _f64(x)
+        c, s = _f64(cos), _f64(sin)
+        B, T, H, D = x.shape
+        assert c.shape == (T, D // 2) and s.shape == c.shape and D % 2 == 0
+        y = np.empty_like(x)
+        self.lib.oracle_rotary_f32(_ptr(x), _ptr(c), _ptr(s), _ptr(y), B, T, H, D)
         return y
 
     def round_bf16(self, x):
@@ -231,17 +242,26 @@ def round_bf16(x):
     return _load().round_bf16(x)
 
 
+def rotary_f32(x, cos, sin):
+    """The rotary turn evaluated in float32 as the CUDA kernels evaluate it (see ``oracle_rotary_f32``)."""
+    return _load().rotary_f32(x, cos, sin)
+
+
+def rotary_bf16(x, cos, sin):
+    """The turned rows as the attention receives them: the float32 turn rounded to bf16."""
+    return round_bf16(rotary_f32(x, cos, sin))
+
+
 def fwd_rotary(q, k, v, cos, sin, window: int, scale: float):
     """Attention with the rotary embedding applied to q and k first (positions 0 .. T-1).  The turned
-    q and k are rounded to bf16 (the model's dtype) before the attention.
+    q and k are bf16 values (the model's dtype) when the attention takes them.
     Returns (o [B,T,H,D], lse [B,H,T])."""
-    return _load().fwd(round_bf16(rotary(q, cos, sin)), round_bf16(rotary(k, cos, sin)), v, window, scale)
+    return _load().fwd(rotary_bf16(q, cos, sin), rotary_bf16(k, cos, sin), v, window, scale)
 
 
 def bwd_rotary(q, k, v, dO, cos, sin, window: int, scale: float):
     """Gradients of sum(O * dO) for the rotary forward with respect to the unrotated q, k and to v:
-    the attention gradients at the (bf16-rounded) turned q and k, turned back by the transpose.  The
+    the attention gradients at the (bf16) turned q and k, turned back by the exact transpose.  The
     rounding is a change of dtype, not of the function: its gradient is taken as the identity."""
-    dqr, dkr, dv = _load().bwd(round_bf16(rotary(q, cos, sin)), round_bf16(rotary(k, cos, sin)), v, dO, window,
-                               scale)
+    dqr, dkr, dv = _load().bwd(rotary_bf16(q, cos, sin), rotary_bf16(k, cos, sin), v, dO, window, scale)
     return rotary(dqr, cos, sin, inverse=True), rotary(dkr, cos, sin, inverse=True), dv

@@ -297,11 +297,37 @@ void oracle_rotary(const double* x, const double* cosv, const double* sinv, doub
                 }
 }
 
+/* The rotary turn evaluated in float32 the way the CUDA kernels evaluate it: with x (bf16 values)
+ * and the fp32 tables exact in float,
+ *   y_i       = fmaf(x_i, c, -(x_{i+D/2} * s))
+ *   y_{i+D/2} = fmaf(x_i, s,   x_{i+D/2} * c),
+ * each product and each fused multiply-add rounded once to float32.  The rotary attention rounds the
+ * turned q and k to bf16, a quantisation that floating point decides; both sides take that decision
+ * in the same precision, so the oracle rounds this float32 turn (oracle_round_bf16), not its exact one.
+ * Everything after the rounding is fp64 again. */
+void oracle_rotary_f32(const double* x, const double* cosv, const double* sinv, double* y,
+                       long B, long T, long H, long D) {
+    long half = D / 2;
+#pragma omp parallel for collapse(2)
+    for (long b = 0; b < B; ++b)
+        for (long t = 0; t < T; ++t)
+            for (long h = 0; h < H; ++h)
+                for (long i = 0; i < half; ++i) {
+                    float c = (float)cosv[(size_t)t * half + i];
+                    float s = (float)sinv[(size_t)t * half + i];
+                    float x1 = (float)x[idx_bthd(b, t, h, i, T, H, D)];
+                    float x2 = (float)x[idx_bthd(b, t, h, i + half, T, H, D)];
+                    float p2s = x2 * s, p2c = x2 * c;
+                    y[idx_bthd(b, t, h, i, T, H, D)] = (double)fmaf(x1, c, -p2s);
+                    y[idx_bthd(b, t, h, i + half, T, H, D)] = (double)fmaf(x1, s, p2c);
+                }
+}
+
 /* Round every value to the nearest bfloat16 (8 significant bits), ties to even, straight from
  * double (no intermediate float, so no double rounding).  The rotary attention takes the turned q
  * and k as bf16 tensors, the dtype of the model's activations ("nanochat GPT-2 speedrun" post,
- * page 2: the attention runs through a bf16 FlashAttention kernel), so the oracle rounds its exact
- * turn once before the attention.  Values are assumed inside bf16's range (|x| < 2^128); zeros,
+ * page 2: the attention runs through a bf16 FlashAttention kernel), so the oracle rounds its
+ * float32 turn (oracle_rotary_f32) once before the attention.  Values are assumed inside bf16's range (|x| < 2^128); zeros,
  * infinities and NaN are left as they are. */
 void oracle_round_bf16(double* x, long n) {
     for (long i = 0; i < n; ++i) {

@@ -570,15 +570,15 @@ def test_rotary_attention_gradients_match_finite_differences(oracle_mod, window)
 
 
 def test_rotary_module_functions_compose_as_stated(oracle_mod):
-    """fwd_rotary / bwd_rotary (used by the GPU tests) are the attention of the rotated q, k and the
-    gradients turned back."""
+    """fwd_rotary / bwd_rotary (used by the GPU tests) are the attention of the rotated q, k (the float32
+    turn rounded to bf16) and the gradients turned back."""
     import oracle
     B, T, H, D = 1, 6, 2, 8
     c, s = workloads.rope_tables(T, D)
     q, k, v, dO = (torch.from_numpy(_rand((B, T, H, D), 720 + i)) for i in range(4))
     # the turned q and k are rounded to bf16 (values a bf16 tensor can hold) before the attention
-    rq = oracle_mod.round_bf16(oracle_mod.rotary(q, c, s))
-    rk = oracle_mod.round_bf16(oracle_mod.rotary(k, c, s))
+    rq = oracle_mod.round_bf16(oracle_mod.rotary_f32(q, c, s))
+    rk = oracle_mod.round_bf16(oracle_mod.rotary_f32(k, c, s))
     for r in (rq, rk):
         np.testing.assert_array_equal(torch.from_numpy(r).to(torch.bfloat16).double().numpy(), r)
     o, lse = oracle.fwd_rotary(q, k, v, c, s, 3, 0.3)
@@ -613,3 +613,37 @@ def test_round_bf16_matches_torch_float32(oracle_mod):
     got = oracle_mod.round_bf16(x.astype(np.float64))
     np.testing.assert_array_equal(got, ref)
     np.testing.assert_array_equal(oracle_mod.round_bf16(got), got)  # already bf16 values stay put
+
+
+def _bf16_rows(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(torch.bfloat16).double().numpy()
+
+
+def test_rotary_f32_matches_a_numpy_restatement(oracle_mod):
+    """The float32 turn: each product of a bf16 value and a float32 table entry is exact in float64, so
+    fmaf(x1, c, -fl(x2 s)) is x1 c - fl(x2 s) rounded once to float32 (numpy float32 ops round per op)."""
+    B, T, H, D = 2, 50, 3, 64
+    x = _bf16_rows((B, T, H, D), 730)
+    c32, s32 = workloads.rope_tables(T, D)
+    c = c32.numpy().reshape(1, T, 1, D // 2).astype(np.float64)
+    s = s32.numpy().reshape(1, T, 1, D // 2).astype(np.float64)
+    x1, x2 = x[..., : D // 2], x[..., D // 2:]
+    p2s = (x2.astype(np.float32) * s.astype(np.float32)).astype(np.float64)
+    p2c = (x2.astype(np.float32) * c.astype(np.float32)).astype(np.float64)
+    y1 = (x1 * c - p2s).astype(np.float32).astype(np.float64)
+    y2 = (x1 * s + p2c).astype(np.float32).astype(np.float64)
+    got = oracle_mod.rotary_f32(x, c32.numpy(), s32.numpy())
+    np.testing.assert_array_equal(got, np.concatenate([y1, y2], axis=-1))
+
+
+def test_rotary_f32_is_the_turn_to_float_precision(oracle_mod):
+    B, T, H, D = 1, 40, 2, 32
+    x = _bf16_rows((B, T, H, D), 731)
+    c, s = workloads.rope_tables(T, D)
+    exact = oracle_mod.rotary(x, c, s)
+    got = oracle_mod.rotary_f32(x, c, s)
+    half = D // 2
+    mag = np.abs(x[..., :half]) + np.abs(x[..., half:])
+    bound = 2.0 ** -22 * np.concatenate([mag, mag], axis=-1) + 1e-30
+    assert (np.abs(got - exact) <= bound).all()

@@ -39,6 +39,8 @@ MUTANTS = {
                                    "double c = cosv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];\n                    double s = sinv[(size_t)(t + 1 < T ? t + 1 : t) * half + i];"),
     "bf16 rounding truncates": ("x[i] = ldexp(nearbyint(ldexp(v, -ue)), ue);", "x[i] = ldexp(trunc(ldexp(v, -ue)), ue);"),
     "bf16 rounding keeps a bit too many": ("int ue = e - 8;", "int ue = e - 9;"),
+    "rotary float32 turn without the fused multiply-add": ("(double)fmaf(x1, c, -p2s);", "(double)(x1 * c - p2s);"),
+    "rotary float32 turn sine sign flipped": ("(double)fmaf(x1, s, p2c);", "(double)fmaf(-x1, s, p2c);"),
 }
 
 PIN_SUITE = [
@@ -56,6 +58,8 @@ PIN_SUITE = [
     (pins.test_rotary_attention_gradients_match_finite_differences, {"window": 3}),
     (pins.test_round_bf16_hand_values, {}),
     (pins.test_round_bf16_matches_torch_float32, {}),
+    (pins.test_rotary_f32_matches_a_numpy_restatement, {}),
+    (pins.test_rotary_f32_is_the_turn_to_float_precision, {}),
 ]
 
 
@@ -71,7 +75,7 @@ def _caught(lib) -> list:
 
 def test_unmutated_copy_passes_every_pin(tmp_path):
     out = tmp_path / "lib_clean.so"
-    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", SRC, "-o", str(out), "-lm"])
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11", SRC, "-o", str(out), "-lm"])
     assert _caught(oracle.OracleLib(str(out))) == []
 
 
@@ -83,6 +87,6 @@ def test_mutant_is_caught(tmp_path, name):
     mutated = tmp_path / "mutant.c"
     mutated.write_text(src.replace(old, new))
     out = tmp_path / "lib_mutant.so"
-    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", str(mutated), "-o", str(out), "-lm"])
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11", str(mutated), "-o", str(out), "-lm"])
     caught = _caught(oracle.OracleLib(str(out)))
     assert caught, f"no pin caught mutant: {name}"
