@@ -370,6 +370,7 @@ def run_ours(args, dist: Dist):
         out["prefill"] = run_prefill(dev, stream, nc_attn, peaks, peak_kind)
         out["varlen"] = run_varlen(dev, stream, nc_attn, peaks, peak_kind)
         out["deterministic_bwd"] = run_deterministic(bufs, calls, dev, stream, nc_attn, peaks, peak_kind)
+        out["rotary"] = run_rotary(bufs, calls, dev, stream, nc_attn, peaks, peak_kind)
     return out
 
 
@@ -629,6 +630,70 @@ def run_deterministic(bufs, calls, dev, stream, nc_attn, peaks, peak_kind):
                     "roofline": {"bound": "tensor", "achieved": round(executed, 1), "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": round(executed / peaks["bf16_tflops"], 4),
                                  "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
+    assert nc_attn.nc_get_device_error(stream) == 0
+    return res
+
+
+def run_rotary(bufs, calls, dev, stream, nc_attn, peaks, peak_kind):
+    """Rotary embedding on the layer pair: the fused forward + backward (q and k turned in shared memory, dq
+    and dk turned back in the epilogues) against the unfused sequence a model without fusion runs: turn q
+    and k with the standalone kernel, plain forward and backward, turn dq and dk back.  L2 flushed before
+    each timed call; useful TFLOP/s counts 14*D flops per visible pair, as the headline does."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {"l2": "flushed (256 MB write) before every timed call",
+           "unfused": "nc_rotary(q), nc_rotary(k), nc_attn_fwd, nc_attn_bwd, nc_rotary^T(dq), nc_rotary^T(dk)"}
+
+    def timed(fn, n=15):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            evs = []
+            for _ in range(n):
+                flush.fill_(1)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                fn()
+                e.record(stream)
+                evs.append((s, e))
+            torch.cuda.synchronize()
+        return statistics.median([s.elapsed_time(e) for s, e in evs])
+
+    for call, b in zip(calls, bufs):
+        c, sn = workloads.rope_tables(call.T, call.D, device=dev)
+        qr, kr = torch.empty_like(b["q"]), torch.empty_like(b["k"])
+
+        def fused():
+            nc_attn.nc_attn_fwd_rotary(b["q"], b["k"], b["v"], c, sn, b["o"], b["lse"], call.window, call.scale,
+                                       stream)
+            nc_attn.nc_attn_bwd_rotary(b["q"], b["k"], b["v"], c, sn, b["o"], b["dO"], b["lse"], b["dq"], b["dk"],
+                                       b["dv"], call.window, call.scale, b["ws"], stream)
+
+        def unfused():
+            nc_attn.nc_rotary(b["q"], c, sn, qr, False, stream)
+            nc_attn.nc_rotary(b["k"], c, sn, kr, False, stream)
+            nc_attn.nc_attn_fwd(qr, kr, b["v"], b["o"], b["lse"], call.window, call.scale, stream)
+            nc_attn.nc_attn_bwd(qr, kr, b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"], call.window,
+                                call.scale, b["ws"], stream)
+            nc_attn.nc_rotary(b["dq"], c, sn, b["dq"], True, stream)
+            nc_attn.nc_rotary(b["dk"], c, sn, b["dk"], True, stream)
+
+        def plain():
+            nc_attn.nc_attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], call.window, call.scale, stream)
+            nc_attn.nc_attn_bwd(b["q"], b["k"], b["v"], b["o"], b["dO"], b["lse"], b["dq"], b["dk"], b["dv"],
+                                call.window, call.scale, b["ws"], stream)
+
+        turn_ms = timed(lambda: nc_attn.nc_rotary(b["q"], c, sn, qr, False, stream))
+        f_ms, u_ms, p_ms = timed(fused), timed(unfused), timed(plain)
+        x_bytes = call.B * call.T * call.H * call.D * 2
+        key = "w1024" if call.window < call.T else "full"
+        res[key] = {"window": call.window, "fused_us": round(f_ms * 1e3, 1), "unfused_us": round(u_ms * 1e3, 1),
+                    "no_rotary_us": round(p_ms * 1e3, 1), "fused_saves_us": round((u_ms - f_ms) * 1e3, 1),
+                    "fused_cost_over_no_rotary": round(f_ms / p_ms - 1.0, 4),
+                    "fused_useful_TFLOP_s": round(useful_flops(call) / (f_ms * 1e-3) / 1e12, 1),
+                    "standalone_turn": {"us": round(turn_ms * 1e3, 1),
+                                        "GB_s": round(2 * x_bytes / (turn_ms * 1e-3) / 1e9, 1),
+                                        "frac_of_hbm": round(2 * x_bytes / (turn_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                                             4)}}
     assert nc_attn.nc_get_device_error(stream) == 0
     return res
 

@@ -26,6 +26,10 @@ namespace {
 
 // Up to 10 warps (one per head for the depth-20 shape); two CTAs fit per SM.
 constexpr int kDecodeMaxThreads = 320;
+// The balanced split serves up to this many sequences (its CTAs scan their visible-row counts in
+// shared memory) and cuts ranges of at least kMinRowsPerCta rows.
+constexpr int kBalancedMaxSeqs = 1024;
+constexpr int kMinRowsPerCta = 16;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -59,25 +63,118 @@ __device__ __forceinline__ float fast_ex2(float x) {
     return y;
 }
 
-// One CTA per (split s, sequence n) work item; item = s + n_splits * n.
-// Warp w handles heads w, w + nwarps, ...  Lanes are grouped G = D / 8 per token
-// row of one head; a warp covers TPS = 32 / G tokens per step and keeps U steps of
-// K and V loads in flight before it does any arithmetic on them.
+// Online softmax of one head's query over cache rows [t_begin, t_end) of sequence n, by one warp:
+// lanes are grouped G = D / 8 per token row, a warp covers TPS = 32 / G tokens per step and keeps U
+// steps of K and V loads in flight before it does any arithmetic on them.  The partial (running max
+// in log2 units, sum, unnormalised output) goes to part_ml[pidx], part_o[pidx].
+template <int D>
+__device__ __forceinline__ void decode_rows(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                                            const __nv_bfloat16* __restrict__ vc, int n, int h, int H, int Tmax,
+                                            int t_begin, int t_end, float scale_log2, size_t pidx,
+                                            float* __restrict__ part_ml, float* __restrict__ part_o) {
+    constexpr int G = D / 8;          // lanes per token row of one head
+    constexpr int TPS = 32 / G;       // tokens per warp step
+    constexpr int U = 4;              // steps in flight per iteration
+    const int lane = threadIdx.x & 31;
+    const int g = lane / G;           // token slot within a step
+    const int c = lane % G;           // 8-element column group
+    const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
+    float qf[8];
+    bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+    float m = -INFINITY, l = 0.f, acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+    const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+    for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * TPS + g;
+            kr[u] = make_uint4(0, 0, 0, 0);
+            vr[u] = make_uint4(0, 0, 0, 0);
+            if (t < t_end) {
+                kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
+                vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
+            }
+        }
+        // scores of the U tokens of this slot (log2 units), reduced across the G lanes
+        float sc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float kf[8];
+            bf16x8_to_f32(kr[u], kf);
+            float dot = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+            sc[u] = dot;
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+            for (int u = 0; u < U; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+        float mc = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (t0 + u * TPS + g >= t_end) sc[u] = -INFINITY;
+            mc = fmaxf(mc, sc[u]);
+        }
+        const float m_new = fmaxf(m, mc);
+        if (m_new == -INFINITY) continue;  // every token of this slot lies past the end
+        const float alpha = fast_ex2(m - m_new);
+        l *= alpha;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= alpha;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float p = fast_ex2(sc[u] - m_new);
+            float vf[8];
+            bf16x8_to_f32(vr[u], vf);
+            l += p;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
+        }
+        m = m_new;
+    }
+    // merge the TPS token slots of this warp (lanes with equal c)
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1) {
+        const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
+        const float l_o = __shfl_xor_sync(0xffffffffu, l, off);
+        const float m_new = fmaxf(m, m_o);
+        const float a_s = (m == -INFINITY) ? 0.f : fast_ex2(m - m_new);
+        const float a_o = (m_o == -INFINITY) ? 0.f : fast_ex2(m_o - m_new);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o_o = __shfl_xor_sync(0xffffffffu, acc[i], off);
+            acc[i] = acc[i] * a_s + o_o * a_o;
+        }
+        l = l * a_s + l_o * a_o;
+        m = m_new;
+    }
+    if (lane < G) {
+        float4* po = reinterpret_cast<float4*>(part_o + pidx * D + c * 8);
+        po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (lane == 0) {
+        part_ml[pidx * 2 + 0] = m;
+        part_ml[pidx * 2 + 1] = l;
+    }
+}
+
+// Chunked split (many sequences): one CTA per (split s, sequence n) work item; item = s + n_splits * n.
+// Warp w handles heads w, w + nwarps, ...
 template <int D>
 __global__ void __launch_bounds__(kDecodeMaxThreads, 2)
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
                     float* __restrict__ part_ml, float* __restrict__ part_o, int N, int Tmax, int H,
                     int window, float scale_log2, int n_splits, int chunk) {
-    constexpr int G = D / 8;          // lanes per token row of one head
-    constexpr int TPS = 32 / G;       // tokens per warp step
-    constexpr int U = 4;              // steps in flight per iteration
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int g = lane / G;           // token slot within a step
-    const int c = lane % G;           // 8-element column group
-    const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int n_items = n_splits * N;
-
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int s = item % n_splits, n = item / n_splits;
         const int L = lens[n];
@@ -86,97 +183,156 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         const int t_begin = lo + s * chunk;
         const int t_end = min(L, t_begin + chunk);
         if (t_begin >= t_end) continue;  // this split lies past the sequence's visible rows
-        for (int h = warp; h < H; h += nwarps) {
-            float qf[8];
-            bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
-            float m = -INFINITY, l = 0.f, acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-            const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-            for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
-                uint4 kr[U], vr[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int t = t0 + u * TPS + g;
-                    kr[u] = make_uint4(0, 0, 0, 0);
-                    vr[u] = make_uint4(0, 0, 0, 0);
-                    if (t < t_end) {
-                        kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
-                        vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
-                    }
-                }
-                // scores of the U tokens of this slot (log2 units), reduced across the G lanes
-                float sc[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    float kf[8];
-                    bf16x8_to_f32(kr[u], kf);
-                    float dot = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
-                    sc[u] = dot;
-                }
-#pragma unroll
-                for (int off = G / 2; off > 0; off >>= 1)
-#pragma unroll
-                    for (int u = 0; u < U; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
-                float mc = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (t0 + u * TPS + g >= t_end) sc[u] = -INFINITY;
-                    mc = fmaxf(mc, sc[u]);
-                }
-                const float m_new = fmaxf(m, mc);
-                if (m_new == -INFINITY) continue;  // every token of this slot lies past the end
-                const float alpha = fast_ex2(m - m_new);
-                l *= alpha;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] *= alpha;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float p = fast_ex2(sc[u] - m_new);
-                    float vf[8];
-                    bf16x8_to_f32(vr[u], vf);
-                    l += p;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
-                }
-                m = m_new;
-            }
-            // merge the TPS token slots of this warp (lanes with equal c)
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1) {
-                const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
-                const float l_o = __shfl_xor_sync(0xffffffffu, l, off);
-                const float m_new = fmaxf(m, m_o);
-                const float a_s = (m == -INFINITY) ? 0.f : fast_ex2(m - m_new);
-                const float a_o = (m_o == -INFINITY) ? 0.f : fast_ex2(m_o - m_new);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float o_o = __shfl_xor_sync(0xffffffffu, acc[i], off);
-                    acc[i] = acc[i] * a_s + o_o * a_o;
-                }
-                l = l * a_s + l_o * a_o;
-                m = m_new;
-            }
-            const size_t pidx = ((size_t)n * n_splits + s) * H + h;
-            if (lane < G) {
-                float4* po = reinterpret_cast<float4*>(part_o + pidx * D + c * 8);
-                po[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                po[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            }
-            if (lane == 0) {
-                part_ml[pidx * 2 + 0] = m;
-                part_ml[pidx * 2 + 1] = l;
-            }
-        }
+        for (int h = warp; h < H; h += nwarps)
+            decode_rows<D>(q, kc, vc, n, h, H, Tmax, t_begin, t_end, scale_log2, ((size_t)n * n_splits + s) * H + h,
+                           part_ml, part_o);
     }
     // this CTA's partials are written: once every CTA is here the combine kernel may be scheduled
     // (it still waits for this grid's completion before reading them)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Balanced split (up to kBalancedMaxSeqs sequences): the visible rows of all sequences, laid end to end
+// (sequence n's at offsets P_n .. P_n + V_n - 1, P the exclusive prefix sum of the visible counts V),
+// are cut into gridDim.x equal ranges of `per` rows, one per CTA, so every CTA streams the same number
+// of bytes and the grid ends together (no partial last wave).  CTA c's piece of sequence n writes its
+// partial to slot n + c: slots increase with (c, n), so they are distinct and below N + gridDim.x.
+// Every CTA computes the prefix sums itself; CTA 0 also stores them (and `per`) in meta for the combine.
+template <int D>
+__global__ void __launch_bounds__(kDecodeMaxThreads, 2)
+decode_balanced_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                       const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
+                       float* __restrict__ part_ml, float* __restrict__ part_o, int* __restrict__ meta, int N,
+                       int Tmax, int H, int window, float scale_log2) {
+    __shared__ int s_vis[kBalancedMaxSeqs];
+    __shared__ int s_pre[kBalancedMaxSeqs + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    for (int n = tid; n < N; n += blockDim.x) {
+        const int L = lens[n];
+        s_vis[n] = (L < 1 || L > Tmax) ? 0 : L - visible_lo(L, window);  // bad lengths: no rows
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan by one warp: lane i sums a run of consecutive sequences, then the runs are scanned
+        const int run = (N + 31) / 32;
+        const int a = min(N, lane * run), b = min(N, a + run);
+        int sum = 0;
+        for (int n = a; n < b; ++n) sum += s_vis[n];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int p = incl - sum;
+        for (int n = a; n < b; ++n) {
+            s_pre[n] = p;
+            p += s_vis[n];
+        }
+        if (lane == 31) s_pre[N] = incl;
+    }
+    __syncthreads();
+    const int R = s_pre[N];
+    const int per = max((R + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), kMinRowsPerCta);
+    if (blockIdx.x == 0) {
+        for (int n = tid; n <= N; n += blockDim.x) meta[n] = s_pre[n];
+        if (tid == 0) meta[N + 1] = per;
+    }
+    const int r0 = static_cast<int>(blockIdx.x) * per;
+    const int r1 = min(R, r0 + per);
+    if (r0 < r1) {
+        // first sequence whose rows reach past r0
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_pre[mid + 1] > r0) hi = mid;
+            else lo = mid + 1;
+        }
+        for (int n = lo; n < N && s_pre[n] < r1; ++n) {
+            const int P = s_pre[n], V = s_vis[n];
+            if (V == 0) continue;
+            const int first = visible_lo(lens[n], window);
+            const int t_begin = first + max(r0, P) - P, t_end = first + min(r1, P + V) - P;
+            const size_t slot = (size_t)n + blockIdx.x;
+            for (int h = warp; h < H; h += nwarps)
+                decode_rows<D>(q, kc, vc, n, h, H, Tmax, t_begin, t_end, scale_log2, slot * H + h, part_ml, part_o);
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Balanced combine, one warp per (sequence, head): the CTAs c0 .. c1 whose ranges hold sequence n's rows
+// left partials in slots n + c0 .. n + c1.  Three dependent rounds of loads: the maxima, the sums with
+// their weights, then the outputs, issued four partials at a time.
+template <int D>
+__global__ void __launch_bounds__(256)
+decode_balanced_combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
+                               const int* __restrict__ meta, const int* __restrict__ lens,
+                               __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int N, int Tmax, int H,
+                               int* err) {
+    constexpr int E = D / 32;  // elements per lane
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (gw >= N * H) return;
+    const int n = gw / H, h = gw % H;
+    const int L = lens[n];
+    __nv_bfloat16* orow = o + (size_t)gw * D;
+    if (L < 1 || L > Tmax) {
+        if (lane == 0) set_device_error(err, NC_ERR_BAD_CACHE_LEN);
+#pragma unroll
+        for (int i = 0; i < E; ++i) orow[lane * E + i] = __float2bfloat16(NAN);
+        if (lse != nullptr && lane == 0) lse[gw] = NAN;
+        return;
+    }
+    const int P = meta[n], V = meta[n + 1] - P, per = meta[N + 1];
+    const int c0 = P / per, k = (P + V - 1) / per - c0 + 1;
+    const size_t base = ((size_t)n + c0) * H + h;  // partial s at base + s * H
+    float M = -INFINITY;
+    for (int s = lane; s < k; s += 32) M = fmaxf(M, part_ml[(base + (size_t)s * H) * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float lsum = 0.f, acc[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] = 0.f;
+    for (int s0 = 0; s0 < k; s0 += 32) {
+        const int cnt = min(32, k - s0);
+        float w = 0.f, lw = 0.f;
+        if (lane < cnt) {
+            const float* ml = part_ml + (base + (size_t)(s0 + lane) * H) * 2;
+            w = exp2f(ml[0] - M);
+            lw = ml[1] * w;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+        lsum += lw;
+        int j = 0;
+        for (; j + 4 <= cnt; j += 4) {
+            float ov[4][E];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float* po = part_o + (base + (size_t)(s0 + j + u) * H) * D + lane * E;
+#pragma unroll
+                for (int i = 0; i < E; ++i) ov[u][i] = po[i];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float wu = __shfl_sync(0xffffffffu, w, j + u);
+#pragma unroll
+                for (int i = 0; i < E; ++i) acc[i] = fmaf(ov[u][i], wu, acc[i]);
+            }
+        }
+        for (; j < cnt; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float* po = part_o + (base + (size_t)(s0 + j) * H) * D + lane * E;
+#pragma unroll
+            for (int i = 0; i < E; ++i) acc[i] = fmaf(po[i], wj, acc[i]);
+        }
+    }
+    const float inv = 1.f / lsum;
+#pragma unroll
+    for (int i = 0; i < E; ++i) orow[lane * E + i] = __float2bfloat16_rn(acc[i] * inv);
+    if (lse != nullptr && lane == 0) lse[gw] = (M + log2f(lsum)) * kLn2;
 }
 
 // One warp per (sequence, head): merge the partials of the splits that saw rows.
@@ -266,36 +422,79 @@ static void launch_combine(void (*kern)(KArgs...), int blocks, cudaStream_t stre
 
 int decode_chunk_rows(int D) { return D == 64 ? 128 : 64; }
 
-int decode_max_splits(int Tmax, int D) {
-    const int chunk = decode_chunk_rows(D);
-    return (Tmax + chunk - 1) / chunk;
+bool decode_balanced(int N, int Tmax) {
+    return N <= kBalancedMaxSeqs && (int64_t)N * Tmax < (int64_t(1) << 30);  // row offsets stay far from overflow
+}
+
+namespace {
+size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+DecodeLayout decode_layout(int N, int Tmax, int H, int D, int window) {
+    DecodeLayout d;
+    size_t parts;
+    if (decode_balanced(N, Tmax)) {
+        parts = ((size_t)N + kDecodeMaxGrid) * H;
+    } else {
+        const int chunk = decode_chunk_rows(D);
+        const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
+        parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
+    }
+    d.off_ml = 0;
+    d.off_o = round_up256(parts * 2 * 4);
+    d.off_meta = d.off_o + round_up256(parts * D * 4);
+    d.bytes = d.off_meta + round_up256(((size_t)N + 2) * 4);
+    return d;
 }
 
 cudaError_t launch_decode(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
-                          float* lse, int N, int Tmax, int H, int D, int window, float scale, float* part_ml,
-                          float* part_o, int* err, cudaStream_t stream) {
-    const int chunk = decode_chunk_rows(D);
-    const int max_splits = decode_max_splits(Tmax, D);
-    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
-    const int n_splits = (w_eff + chunk - 1) / chunk;  // splits any sequence can need
+                          float* lse, int N, int Tmax, int H, int D, int window, float scale, void* workspace,
+                          int* err, cudaStream_t stream) {
+    const DecodeLayout lay = decode_layout(N, Tmax, H, D, window);
+    char* ws = static_cast<char*>(workspace);
+    float* part_ml = reinterpret_cast<float*>(ws + lay.off_ml);
+    float* part_o = reinterpret_cast<float*>(ws + lay.off_o);
+    int* meta = reinterpret_cast<int*>(ws + lay.off_meta);
     const float scale_log2 = scale * kLog2e;
-    (void)max_splits;
     const int threads = 32 * (H < kDecodeMaxThreads / 32 ? H : kDecodeMaxThreads / 32);
-    const long items = (long)n_splits * N;
-    const int grid = (int)items;
     const int cblocks = (N * H * 32 + 255) / 256;
-    if (D == 128) {
-        decode_split_kernel<128><<<grid, threads, 0, stream>>>(
-            (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
-            part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
-        launch_combine(decode_combine_kernel<128>, cblocks, stream, part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
-                       Tmax, H, window, n_splits, chunk, err);
+    auto bq = static_cast<const __nv_bfloat16*>(q);
+    auto bk = static_cast<const __nv_bfloat16*>(kcache);
+    auto bv = static_cast<const __nv_bfloat16*>(vcache);
+    auto bo = static_cast<__nv_bfloat16*>(o);
+    if (decode_balanced(N, Tmax)) {
+        // as many CTAs as fit on the GPU at once (looked up per call), at most kDecodeMaxGrid
+        auto split = D == 128 ? decode_balanced_kernel<128> : decode_balanced_kernel<64>;
+        int sms = 0, per_sm = 0;
+        cudaError_t e = multiprocessor_count(&sms);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split, threads, 0);
+        if (e != cudaSuccess) return e;
+        const long want = (long)sms * (per_sm > 0 ? per_sm : 1);
+        const int grid = static_cast<int>(want < kDecodeMaxGrid ? want : kDecodeMaxGrid);
+        split<<<grid, threads, 0, stream>>>(bq, bk, bv, lens, part_ml, part_o, meta, N, Tmax, H, window, scale_log2);
+        if (D == 128)
+            launch_combine(decode_balanced_combine_kernel<128>, cblocks, stream, (const float*)part_ml,
+                           (const float*)part_o, (const int*)meta, lens, bo, lse, N, Tmax, H, err);
+        else
+            launch_combine(decode_balanced_combine_kernel<64>, cblocks, stream, (const float*)part_ml,
+                           (const float*)part_o, (const int*)meta, lens, bo, lse, N, Tmax, H, err);
     } else {
-        decode_split_kernel<64><<<grid, threads, 0, stream>>>(
-            (const __nv_bfloat16*)q, (const __nv_bfloat16*)kcache, (const __nv_bfloat16*)vcache, lens, part_ml,
-            part_o, N, Tmax, H, window, scale_log2, n_splits, chunk);
-        launch_combine(decode_combine_kernel<64>, cblocks, stream, part_ml, part_o, lens, (__nv_bfloat16*)o, lse, N,
-                       Tmax, H, window, n_splits, chunk, err);
+        const int chunk = decode_chunk_rows(D);
+        const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
+        const int n_splits = (w_eff + chunk - 1) / chunk;  // splits any sequence can need
+        const int grid = n_splits * N;
+        if (D == 128) {
+            decode_split_kernel<128><<<grid, threads, 0, stream>>>(bq, bk, bv, lens, part_ml, part_o, N, Tmax, H,
+                                                                   window, scale_log2, n_splits, chunk);
+            launch_combine(decode_combine_kernel<128>, cblocks, stream, (const float*)part_ml, (const float*)part_o,
+                           lens, bo, lse, N, Tmax, H, window, n_splits, chunk, err);
+        } else {
+            decode_split_kernel<64><<<grid, threads, 0, stream>>>(bq, bk, bv, lens, part_ml, part_o, N, Tmax, H,
+                                                                  window, scale_log2, n_splits, chunk);
+            launch_combine(decode_combine_kernel<64>, cblocks, stream, (const float*)part_ml, (const float*)part_o,
+                           lens, bo, lse, N, Tmax, H, window, n_splits, chunk, err);
+        }
     }
     count_launches(2);
     return cudaGetLastError();

@@ -26,8 +26,9 @@
 namespace {
 
 // Scratch for the partial (max, sum) pairs and unnormalised outputs of every
-// split.  Shared by all calls on a device; no part of it needs to start at
-// zero, because the combine pass reads only the splits the split pass wrote.
+// split, and the balanced split's row offsets.  Shared by all calls on a
+// device; no part of it needs to start at zero, because the combine pass reads
+// only what the split pass of the same call wrote.
 static __device__ __align__(256) unsigned char g_decode_scratch[NC_DECODE_NOALLOC_SCRATCH_BYTES];
 
 // Device address of the scratch array on the current device, looked up on every call (host code
@@ -39,8 +40,6 @@ void* scratch_address() {
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
     return p;
 }
-
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -61,10 +60,7 @@ extern "C" {
 size_t nc_attn_decode_noalloc_scratch_bytes(int N, int Tmax, int H, int D, int window) {
     if (N <= 0 || Tmax <= 0 || H <= 0 || (D != 64 && D != 128) || (window < 1 && window != NC_WINDOW_FULL)) return 0;
     if (!sizes_supported(N, Tmax, H, D)) return 0;
-    const int chunk = nc::decode_chunk_rows(D);
-    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
-    const size_t parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
-    return round_up(parts * 2 * 4, 256) + parts * D * 4;
+    return nc::decode_layout(N, Tmax, H, D, window).bytes;
 }
 
 nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
@@ -91,13 +87,8 @@ nc_status nc_attn_decode_noalloc(const void* q, const void* kcache, const void* 
     unsigned char* scratch = static_cast<unsigned char*>(scratch_address());
     int* err = nc::device_error_word();
     if (scratch == nullptr || err == nullptr) return NC_ERR_CUDA;
-    const int chunk = nc::decode_chunk_rows(D);
-    const int w_eff = (window <= 0 || window >= Tmax) ? Tmax : window;
-    const size_t parts = (size_t)N * ((w_eff + chunk - 1) / chunk) * H;
-    float* part_ml = reinterpret_cast<float*>(scratch);
-    float* part_o = reinterpret_cast<float*>(scratch + round_up(parts * 2 * 4, 256));
     const cudaError_t e = nc::launch_decode(q, kcache, vcache, cache_lens, o, lse, N, Tmax, H, D, window, scale,
-                                            part_ml, part_o, err, stream);
+                                            scratch, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

@@ -80,6 +80,41 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
+nc_status nc_attn_fwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
+                             void* o, float* lse, int B, int T, int H, int D, int window, float scale,
+                             cudaStream_t stream) {
+    nc_status st = check_shape(B, T, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (!q || !k || !v || !rope_cos || !rope_sin || !o || !lse) return NC_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
+        !aligned16(o) || !aligned16(lse))
+        return NC_ERR_INVALID;
+    const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4, nt = (size_t)T * (D / 2) * 4;
+    const void* ins[5] = {q, k, v, rope_cos, rope_sin};
+    const size_t in_n[5] = {nb, nb, nb, nt, nt};
+    for (int i = 0; i < 5; ++i)
+        if (overlap(ins[i], in_n[i], o, nb) || overlap(ins[i], in_n[i], lse, nl)) return NC_ERR_INVALID;
+    if (overlap(o, nb, lse, nl)) return NC_ERR_INVALID;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const cudaError_t e =
+        nc::launch_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, B, T, H, D, window, scale, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_rotary(const void* x, const float* rope_cos, const float* rope_sin, void* y, int B, int T, int H,
+                    int D, int inverse, cudaStream_t stream) {
+    if (B < 1 || T < 1 || H < 1) return NC_ERR_INVALID;
+    if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
+    if (!x || !rope_cos || !rope_sin || !y) return NC_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(rope_cos) || !aligned16(rope_sin) || !aligned16(y)) return NC_ERR_INVALID;
+    const size_t nb = (size_t)B * T * H * D * 2, nt = (size_t)T * (D / 2) * 4;
+    if (x != y && overlap(x, nb, y, nb)) return NC_ERR_INVALID;
+    if (overlap(rope_cos, nt, y, nb) || overlap(rope_sin, nt, y, nb)) return NC_ERR_INVALID;
+    const cudaError_t e = nc::launch_rotary(x, rope_cos, rope_sin, y, B, T, H, D, inverse != 0, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const int* cu_seqlens, void* o, float* lse,
                              int n_docs, int total, int max_seqlen, int H, int D, int window, float scale,
                              cudaStream_t stream) {
@@ -218,6 +253,43 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
                     false);
 }
 
+nc_status nc_attn_bwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
+                             const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                             int T, int H, int D, int window, float scale, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    nc_status st = check_shape(B, T, H, D, window, scale);
+    if (st != NC_OK) return st;
+    if (!q || !k || !v || !rope_cos || !rope_sin || !o || !dO || !lse || !dq || !dk || !dv) return NC_ERR_INVALID;
+    const void* all[11] = {q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv};
+    for (const void* p : all)
+        if (!aligned16(p)) return NC_ERR_INVALID;
+    const size_t need = nc_attn_bwd_workspace_bytes(B, T, H, D);
+    if (workspace == nullptr || workspace_bytes < need) return NC_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return NC_ERR_INVALID;
+    const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4, nt = (size_t)T * (D / 2) * 4;
+    const void* ins[8] = {q, k, v, rope_cos, rope_sin, o, dO, lse};
+    const size_t in_n[8] = {nb, nb, nb, nt, nt, nb, nb, nl};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_n[4] = {nb, nb, nb, need};
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 8; ++i)
+            if (overlap(ins[i], in_n[i], outs[a], out_n[a])) return NC_ERR_INVALID;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], out_n[a], outs[b], out_n[b])) return NC_ERR_INVALID;
+    }
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)B * T * H * D * 4, 256);
+    float* delta = reinterpret_cast<float*>(ws);
+    ws += round_up((size_t)B * H * T * 4, 256);
+    int* work = reinterpret_cast<int*>(ws);
+    const cudaError_t e = nc::launch_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, B, T, H, D,
+                                                window, scale, dq_acc, delta, work, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 nc_status nc_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                     const float* lse, void* dq, void* dk, void* dv, int B, int T, int H, int D,
                                     int window, float scale, void* workspace, size_t workspace_bytes,
@@ -228,8 +300,7 @@ nc_status nc_attn_bwd_deterministic(const void* q, const void* k, const void* v,
 
 size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D) {
     if (N <= 0 || Tmax <= 0 || H <= 0 || (D != 64 && D != 128)) return 0;
-    const size_t parts = (size_t)N * nc::decode_max_splits(Tmax, D) * H;
-    return round_up(parts * 2 * 4, 256) + round_up(parts * D * 4, 256);
+    return nc::decode_layout(N, Tmax, H, D, NC_WINDOW_FULL).bytes;  // the largest over windows
 }
 
 nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, const int* cache_lens, void* o,
@@ -260,11 +331,8 @@ nc_status nc_attn_decode(const void* q, const void* kcache, const void* vcache, 
     }
     int* err = error_word();
     if (err == nullptr) return NC_ERR_CUDA;
-    const size_t parts = (size_t)N * nc::decode_max_splits(Tmax, D) * H;
-    float* part_ml = static_cast<float*>(workspace);
-    float* part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(parts * 2 * 4, 256));
     const cudaError_t e = nc::launch_decode(q, kcache, vcache, cache_lens, o, lse, N, Tmax, H, D, window, scale,
-                                            part_ml, part_o, err, stream);
+                                            workspace, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 

@@ -27,7 +27,14 @@ cudaError_t ensure_smem_attr(const void* kern, int bytes, std::atomic<bool>* don
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);
 
+// Forward with the rotary embedding of q and k (tables rcos, rsin fp32 [T, D/2]) fused into the load stage.
+cudaError_t launch_fwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin, void* o,
+                              float* lse, int B, int T, int H, int D, int window, float scale, int* err,
+                              cudaStream_t st);
+
 // Document-masked forward over packed rows: q/k/v/o [total,H,D] bf16, lse [H,total] fp32, cu device int32 [n_docs+1].
+cudaError_t launch_rotary(const void* x, const float* rcos, const float* rsin, void* y, int B, int T, int H, int D,
+                          bool inverse, cudaStream_t st);
 cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const int* cu, int n_docs, int max_len,
                               void* o, float* lse, int total, int H, int D, int window, float scale, int* err,
                               cudaStream_t st);
@@ -47,6 +54,12 @@ cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
                        float* dq_acc, float* delta, int* work, int* err, cudaStream_t st);
+
+// Backward of the rotary forward: dq and dk with respect to the unrotated q and k.  Workspace as for launch_bwd.
+cudaError_t launch_bwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin,
+                              const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                              int T, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
+                              int* err, cudaStream_t st);
 
 // Deterministic backward: dK and dV from the main kernel without its dQ product, then dq from the
 // query-stationary pass (launch_bwd_dq).  Workspace as for launch_bwd (dq_acc is not touched).

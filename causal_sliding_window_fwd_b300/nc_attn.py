@@ -31,7 +31,7 @@ NC_WINDOW_FULL = -1
 EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "nc_attn_bwd",
             "nc_attn_bwd_deterministic",
             "nc_attn_decode_workspace_bytes", "nc_attn_decode", "nc_attn_prefill", "nc_attn_fwd_varlen",
-            "nc_attn_bwd_varlen",
+            "nc_attn_bwd_varlen", "nc_attn_fwd_rotary", "nc_attn_bwd_rotary", "nc_rotary",
             "nc_get_device_error",
             "nc_launch_count",
             "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
@@ -72,6 +72,12 @@ def _load():
     lib.nc_attn_fwd_varlen.restype = i
     lib.nc_attn_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_bwd_varlen.restype = i
+    lib.nc_attn_fwd_rotary.argtypes = [vp] * 7 + [i, i, i, i, i, f, vp]
+    lib.nc_attn_fwd_rotary.restype = i
+    lib.nc_attn_bwd_rotary.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_bwd_rotary.restype = i
+    lib.nc_rotary.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.nc_rotary.restype = i
     lib.nc_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
     lib.nc_get_device_error.restype = i
     lib.nc_launch_count.argtypes = []
@@ -165,6 +171,77 @@ def _bwd_call(name, q, k, v, o, dO, lse, dq, dk, dv, window, scale, workspace, s
     _check(getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                               B, T, H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
                               _stream(q.device, stream)), name)
+
+
+def _rope_tables(rope_cos, rope_sin, T, D):
+    _need(rope_cos, "rope_cos", torch.float32, (T, D // 2))
+    _need(rope_sin, "rope_sin", torch.float32, (T, D // 2))
+
+
+def nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, window: int, scale: float, stream=None) -> None:
+    """Forward with the rotary embedding of q and k (tables fp32 [T, D/2]) fused into the load stage."""
+    B, T, H, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(t, n, torch.bfloat16, (B, T, H, D))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    _rope_tables(rope_cos, rope_sin, T, D)
+    _check(lib.nc_attn_fwd_rotary(_ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(o), _ptr(lse),
+                                  B, T, H, D, int(window), float(scale), _stream(q.device, stream)),
+           "nc_attn_fwd_rotary")
+
+
+def nc_attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace,
+                       stream=None) -> None:
+    """Backward of nc_attn_fwd_rotary: dq, dk with respect to the unrotated q, k."""
+    B, T, H, D = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, n, torch.bfloat16, (B, T, H, D))
+    _need(lse, "lse", torch.float32, (B, H, T))
+    _rope_tables(rope_cos, rope_sin, T, D)
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib.nc_attn_bwd_rotary(_ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(o), _ptr(dO),
+                                  _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, T, H, D, int(window), float(scale),
+                                  _ptr(workspace), workspace.numel(), _stream(q.device, stream)),
+           "nc_attn_bwd_rotary")
+
+
+def nc_rotary(x, rope_cos, rope_sin, y, inverse: bool = False, stream=None) -> None:
+    """The rotary turn of x [B, T, H, D] bf16 into y (x itself for in place); the transpose with inverse."""
+    B, T, H, D = x.shape
+    _need(x, "x", torch.bfloat16, (B, T, H, D))
+    _need(y, "y", torch.bfloat16, (B, T, H, D))
+    _rope_tables(rope_cos, rope_sin, T, D)
+    _check(lib.nc_rotary(_ptr(x), _ptr(rope_cos), _ptr(rope_sin), _ptr(y), B, T, H, D, int(bool(inverse)),
+                         _stream(x.device, stream)), "nc_rotary")
+
+
+def rotary(x, rope_cos, rope_sin, inverse: bool = False, stream=None):
+    """Returns the rotary turn of x (a new tensor)."""
+    y = torch.empty_like(x)
+    nc_rotary(x, rope_cos, rope_sin, y, inverse, stream)
+    return y
+
+
+def attn_fwd_rotary(q, k, v, rope_cos, rope_sin, window: int, scale: float | None = None, stream=None):
+    """Returns (o, lse) of attention over the rotary-embedded q and k."""
+    B, T, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, window, scale, stream)
+    return o, lse
+
+
+def attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, window: int, scale: float | None = None,
+                    workspace=None, stream=None):
+    """Returns (dq, dk, dv) of the rotary forward, dq and dk with respect to the unrotated q and k."""
+    B, T, H, D = q.shape
+    scale = default_scale(D) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    nc_attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+    return dq, dk, dv
 
 
 def nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window: int, scale: float, workspace, stream=None) -> None:

@@ -4,6 +4,9 @@
     python -m causal_sliding_window_fwd_b300.profile_case --op bwd ...
     python -m causal_sliding_window_fwd_b300.profile_case --op bwd_det ...   (nc_attn_bwd_deterministic)
     python -m causal_sliding_window_fwd_b300.profile_case --op decode --window 1024
+    python -m causal_sliding_window_fwd_b300.profile_case --op prefill --window 1024   (prefill workload)
+    python -m causal_sliding_window_fwd_b300.profile_case --op varlen_bwd --window 1024 (packed documents)
+    python -m causal_sliding_window_fwd_b300.profile_case --op rope_fwd / rope_bwd ...  (rotary variants)
 
 The inputs are made and the forward (needed by the backward) is run before
 the profiled launches; ``--iters`` calls of the chosen op follow.
@@ -20,7 +23,8 @@ from causal_sliding_window_fwd_b300 import nc_attn, workloads
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["fwd", "bwd", "bwd_det", "decode"], default="fwd")
+    ap.add_argument("--op", choices=["fwd", "bwd", "bwd_det", "decode", "prefill", "varlen_fwd", "varlen_bwd",
+                                     "rope_fwd", "rope_bwd"], default="fwd")
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--H", type=int, default=10)
@@ -39,6 +43,40 @@ def main():
         lse = torch.empty((wl.N, wl.H), dtype=torch.float32, device=dev)
         for _ in range(a.iters):
             nc_attn.nc_attn_decode(q, kc, vc, lens, o, lse, a.window, wl.scale, ws)
+    elif a.op == "prefill":
+        wl = workloads.PREFILL
+        q, kc, vc, lens = workloads.make_prefill(wl, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((wl.N, wl.H, wl.Tq), dtype=torch.float32, device=dev)
+        for _ in range(a.iters):
+            nc_attn.nc_attn_prefill(q, kc, vc, lens, o, lse, a.window, wl.scale)
+    elif a.op in ("varlen_fwd", "varlen_bwd"):
+        wl = workloads.VARLEN
+        q, k, v, dO, cu, max_len = workloads.make_varlen(wl, dev)
+        scale = 1.0 / math.sqrt(wl.D)
+        o, lse = nc_attn.attn_fwd_varlen(q, k, v, cu, max_len, a.window, scale)
+        if a.op == "varlen_fwd":
+            for _ in range(a.iters):
+                nc_attn.nc_attn_fwd_varlen(q, k, v, cu, o, lse, max_len, a.window, scale)
+        else:
+            total = q.shape[0]
+            ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(1, total, wl.H, wl.D), dtype=torch.uint8, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            for _ in range(a.iters):
+                nc_attn.nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu, dq, dk, dv, max_len, a.window, scale, ws)
+    elif a.op in ("rope_fwd", "rope_bwd"):
+        scale = 1.0 / math.sqrt(a.D)
+        q, k, v, dO = workloads.make_qkvdo_shape(a.B, a.T, a.H, a.D, a.seed, dev)
+        c, s = workloads.rope_tables(a.T, a.D, device=dev)
+        o, lse = nc_attn.attn_fwd_rotary(q, k, v, c, s, a.window, scale)
+        if a.op == "rope_fwd":
+            for _ in range(a.iters):
+                nc_attn.nc_attn_fwd_rotary(q, k, v, c, s, o, lse, a.window, scale)
+        else:
+            ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(a.B, a.T, a.H, a.D), dtype=torch.uint8, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            for _ in range(a.iters):
+                nc_attn.nc_attn_bwd_rotary(q, k, v, c, s, o, dO, lse, dq, dk, dv, a.window, scale, ws)
     else:
         scale = 1.0 / math.sqrt(a.D)
         q, k, v, dO = workloads.make_qkvdo_shape(a.B, a.T, a.H, a.D, a.seed, dev)

@@ -127,7 +127,9 @@ nc_status nc_attn_bwd_deterministic(const void* q, const void* k, const void* v,
                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of device workspace nc_attn_decode needs for its split-K partial
- * results (fp32 running max, sum and output per split). */
+ * results (fp32 running max, sum and output per split) and, for up to 1024
+ * sequences, the per-sequence row offsets of its balanced split.  Its
+ * contents on entry do not matter. */
 size_t nc_attn_decode_workspace_bytes(int N, int Tmax, int H, int D);
 
 /*
@@ -206,6 +208,56 @@ nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
 nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
                           void* o, float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
                           cudaStream_t stream);
+
+/*
+ * Forward with the rotary position embedding of q and k fused into the load
+ * stage ("nanochat" walkthrough, page 4, comment thread: the model is
+ * Llama-like; the pages give no formula, and the rotate-half pairing of Llama
+ * is the reading taken).  Each query and key row of position t (0 .. T-1) has
+ * every pair (x_i, x_{i+D/2}), i < D/2, turned by the angle whose cosine and
+ * sine the tables hold at (t, i):
+ *   x_i' = x_i c - x_{i+D/2} s,   x_{i+D/2}' = x_i s + x_{i+D/2} c,
+ * and o, lse are those of nc_attn_fwd on the turned q and k (v unchanged).
+ * The turn is applied to the tiles in shared memory between their arrival and
+ * the first tensor-core product; the rotated q and k never go to memory.
+ *   rope_cos, rope_sin : const fp32 [T, D/2] device, 16-byte aligned (row t,
+ *                        column i; e.g. cos / sin of t * base^(-2i/D))
+ * Other arguments, layouts and errors as nc_attn_fwd.
+ */
+nc_status nc_attn_fwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos,
+                             const float* rope_sin, void* o, float* lse, int B, int T, int H, int D,
+                             int window, float scale, cudaStream_t stream);
+
+/*
+ * Backward of nc_attn_fwd_rotary: dq and dk are the gradients with respect to
+ * the unrotated q and k (the gradients with respect to the turned rows, turned
+ * back by the transpose), dv as nc_attn_bwd.  o and lse are those that
+ * nc_attn_fwd_rotary produced with the same arguments; the workspace is sized
+ * by nc_attn_bwd_workspace_bytes.  Other arguments, layouts and errors as
+ * nc_attn_bwd.
+ */
+nc_status nc_attn_bwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos,
+                             const float* rope_sin, const void* o, const void* dO, const float* lse,
+                             void* dq, void* dk, void* dv, int B, int T, int H, int D, int window,
+                             float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The rotary turn on its own (the unfused form of what nc_attn_fwd_rotary does
+ * in shared memory): y = the turn of x, row t of each sequence by the tables'
+ * row t, as nc_attn_fwd_rotary defines it; with inverse != 0 the transpose
+ * (the turn back, which maps gradients with respect to the turned tensor to
+ * gradients with respect to x).  For positions that do not start at 0 pass
+ * tables offset to the first position.
+ *   x                  : const bf16 [B, T, H, D] device, 16-byte aligned
+ *   rope_cos, rope_sin : const fp32 [T, D/2] device, 16-byte aligned
+ *   y                  : bf16 [B, T, H, D] device, written; either x itself
+ *                        (in place) or a range that does not overlap x
+ * D is 64 or 128.  Errors: NC_ERR_INVALID for a null or unaligned pointer, a
+ * partial overlap, or B, T, H < 1; NC_ERR_UNSUPPORTED for another D;
+ * NC_ERR_CUDA if the launch fails.  One kernel launch, asynchronous.
+ */
+nc_status nc_rotary(const void* x, const float* rope_cos, const float* rope_sin, void* y, int B, int T,
+                    int H, int D, int inverse, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that

@@ -291,3 +291,60 @@ def test_abi_calls_from_many_threads(lib):
     for t in threads:
         t.join()
     assert not errors, errors[:3]
+
+
+def _fwd_rot(lib, ptrs=None, **kw):
+    a = dict(GOOD, **kw)
+    p = list(A[:7]) if ptrs is None else ptrs
+    return lib.lib.nc_attn_fwd_rotary(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"],
+                                      a["window"], ctypes.c_float(a["scale"]), None)
+
+
+def _rot(lib, ptrs=None, inverse=0, **kw):
+    a = dict(GOOD, **kw)
+    p = list(A[:4]) if ptrs is None else ptrs
+    return lib.lib.nc_rotary(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"], inverse, None)
+
+
+@host_only
+def test_rotary_entries_reject_bad_arguments(lib):
+    # forward: q k v cos sin o lse
+    assert _fwd_rot(lib, D=96) == lib.NC_ERR_UNSUPPORTED
+    assert _fwd_rot(lib, window=0) == lib.NC_ERR_INVALID
+    for i in range(7):
+        p = list(A[:7]); p[i] = 0
+        assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+        p = list(A[:7]); p[i] += 8
+        assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:7]); p[5] = p[3] + 256       # o over the cosine table
+    assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:7]); p[6] = p[4]             # lse over the sine table
+    assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+    # backward: q k v cos sin o dO lse dq dk dv, workspace
+    need = lib.nc_attn_bwd_workspace_bytes(2, 64, 2, 64)
+
+    def bwd_rot(p, ws=A[11], ws_bytes=need, **kw):
+        a = dict(GOOD, **kw)
+        return lib.lib.nc_attn_bwd_rotary(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"],
+                                          a["window"], ctypes.c_float(a["scale"]), ctypes.c_void_p(ws), ws_bytes,
+                                          None)
+    assert bwd_rot(list(A[:11]), D=96) == lib.NC_ERR_UNSUPPORTED
+    assert bwd_rot(list(A[:11]), ws_bytes=need - 1) == lib.NC_ERR_WORKSPACE
+    for i in range(11):
+        p = list(A[:11]); p[i] = 0
+        assert bwd_rot(p) == lib.NC_ERR_INVALID
+    p = list(A[:11]); p[8] = p[3]            # dq over the cosine table
+    assert bwd_rot(p) == lib.NC_ERR_INVALID
+    assert bwd_rot(list(A[:11]), ws=A[4]) == lib.NC_ERR_INVALID   # workspace over the sine table
+    # the standalone turn: x cos sin y
+    assert _rot(lib, D=96) == lib.NC_ERR_UNSUPPORTED
+    assert _rot(lib, B=0) == lib.NC_ERR_INVALID
+    for i in range(4):
+        p = list(A[:4]); p[i] = 0
+        assert _rot(lib, p) == lib.NC_ERR_INVALID
+        p = list(A[:4]); p[i] += 8
+        assert _rot(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:4]); p[3] = p[0] + 128       # y partly over x (in place means y == x exactly)
+    assert _rot(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:4]); p[3] = p[1]             # y over the cosine table
+    assert _rot(lib, p) == lib.NC_ERR_INVALID

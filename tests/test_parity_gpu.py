@@ -250,6 +250,43 @@ def test_decode_small(nc, oracle_mod, D, window):
     assert abs_err(lse, lse_ref) <= LSE_TOL
 
 
+@pytest.mark.parametrize("window", [5000, -1])
+def test_decode_one_long_sequence_over_many_ctas(nc, oracle_mod, window):
+    """Few sequences take the balanced split: the visible rows of all of them are cut into one equal range
+    per CTA, so the 8000-row sequence here is spread over a few hundred CTAs (its combine merges more than
+    32 partials, in several rounds) while the two short ones sit inside one CTA's range."""
+    wl = workloads.DecodeWorkload("uneven", 3, 8000, 3, 128, 1, 8000, (window,), 515)
+    q, kc, vc, _ = workloads.make_decode(wl, "cuda")
+    lens = torch.tensor([1, 8000, 5], dtype=torch.int32, device="cuda")
+    dead = (torch.arange(wl.Tmax, device="cuda").view(1, -1) >= lens.view(-1, 1)).view(wl.N, wl.Tmax, 1, 1)
+    kc.masked_fill_(dead, float("nan"))
+    vc.masked_fill_(dead, float("nan"))
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
+                                           window, wl.scale)
+    assert ok
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
+@pytest.mark.parametrize("window", [100, -1])
+def test_decode_many_sequences_fixed_chunks(nc, oracle_mod, window):
+    """More than 1024 sequences take fixed 128-row chunks (D = 64) per CTA instead of the balanced split."""
+    wl = workloads.DecodeWorkload("many", 1100, 300, 2, 64, 1, 300, (window,), 616)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda")
+    dead = (torch.arange(wl.Tmax, device="cuda").view(1, -1) >= lens.view(-1, 1)).view(wl.N, wl.Tmax, 1, 1)
+    kc.masked_fill_(dead, float("nan"))
+    vc.masked_fill_(dead, float("nan"))
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
+                                           window, wl.scale)
+    assert ok
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
 def test_decode_equals_last_forward_row(nc):
     B, T, H, D, W = 2, 600, 2, 128, 256
     q, k, v, _ = workloads.make_qkvdo_shape(B, T, H, D, seed=31, device="cuda")

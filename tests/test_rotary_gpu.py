@@ -1,0 +1,147 @@
+"""GPU parity of the rotary variants (rotary embedding of q and k fused into the attention kernels'
+load stage) against the fp64 oracle's rotary attention.
+
+Tolerances as in test_parity_gpu: output <= 2e-2 max|ref|, lse <= 1e-3 absolute, gradients <= 3e-2
+max|ref| (per (b, h) slice at full size).  The kernels round the turned q and k to bf16 in shared memory
+before the products; the oracle turns the same bf16 inputs in fp64 and rounds the turned q and k to the
+nearest bf16 before its attention (the attention takes bf16 q and k in both).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from causal_sliding_window_fwd_b300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL, G_TOL = 2e-2, 1e-3, 3e-2
+
+
+@pytest.fixture(scope="module")
+def nc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_sliding_window_fwd_b300 import nc_attn
+    return nc_attn
+
+
+def rel_err(got, ref):
+    got = got.detach().float().cpu().numpy() if torch.is_tensor(got) else np.asarray(got)
+    ref = np.asarray(ref)
+    assert np.isfinite(got).all(), "non-finite values in GPU output"
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
+
+
+def abs_err(got, ref):
+    got = got.detach().float().cpu().numpy() if torch.is_tensor(got) else np.asarray(got)
+    assert np.isfinite(got).all(), "non-finite values in GPU output"
+    return float(np.abs(got - np.asarray(ref)).max())
+
+
+def run(nc, q, k, v, dO, c, s, window, scale):
+    B, T, H, D = q.shape
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, T), float("nan"), dtype=torch.float32, device=q.device)
+    nc.nc_attn_fwd_rotary(q, k, v, c, s, o, lse, window, scale)
+    ws = torch.full((nc.nc_attn_bwd_workspace_bytes(B, T, H, D),), 0xFF, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    nc.nc_attn_bwd_rotary(q, k, v, c, s, o, dO, lse, dq, dk, dv, window, scale, ws)
+    assert nc.nc_get_device_error() == 0
+    return o, lse, dq, dk, dv
+
+
+CASES = [
+    # (B, T, H, D, window)
+    (1, 128, 2, 64, 32), (1, 1, 1, 128, -1), (2, 200, 1, 128, 1), (1, 257, 2, 128, 129), (1, 333, 1, 64, 100),
+    (2, 384, 3, 128, -1), (1, 700, 2, 128, 512), (2, 800, 40, 64, 300), (1, 1100, 24, 128, 200),
+]
+
+
+@pytest.mark.parametrize("B,T,H,D,window", CASES)
+def test_rotary_matches_oracle(nc, oracle_mod, B, T, H, D, window):
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4000 + T + window, device="cuda")
+    c, s = workloads.rope_tables(T, D, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    o, lse, dq, dk, dv = run(nc, q, k, v, dO, c, s, window, scale)
+    args = [x.cpu() for x in (q, k, v)]
+    o_r, lse_r = oracle_mod.fwd_rotary(*args, c.cpu(), s.cpu(), window, scale)
+    assert rel_err(o, o_r) <= O_TOL
+    assert abs_err(lse, lse_r) <= LSE_TOL
+    dq_r, dk_r, dv_r = oracle_mod.bwd_rotary(*args, dO.cpu(), c.cpu(), s.cpu(), window, scale)
+    assert rel_err(dq, dq_r) <= G_TOL, "dq"
+    assert rel_err(dk, dk_r) <= G_TOL, "dk"
+    assert rel_err(dv, dv_r) <= G_TOL, "dv"
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_identity_tables_give_the_plain_kernels(nc, D):
+    """cos = 1, sin = 0 turns nothing: every output equals the plain forward / backward (dq up to the
+    order in which its fp32 partials are added)."""
+    B, T, H, W = 2, 333, 3, 100
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4100 + D, device="cuda")
+    c = torch.ones((T, D // 2), dtype=torch.float32, device="cuda")
+    s = torch.zeros((T, D // 2), dtype=torch.float32, device="cuda")
+    o, lse, dq, dk, dv = run(nc, q, k, v, dO, c, s, W, 0.09)
+    o2, lse2 = nc.attn_fwd(q, k, v, W, 0.09)
+    dq2, dk2, dv2 = nc.attn_bwd(q, k, v, o2, dO, lse2, W, 0.09)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert (dq.float() - dq2.float()).abs().max().item() <= 1e-2 * dq2.float().abs().max().item()
+
+
+@pytest.mark.parametrize("wl_name,call_idx", [("D20_PAIR", 0), ("D20_PAIR", 1), ("LONG_SW", 0)])
+def test_rotary_full_size(nc, oracle_mod, wl_name, call_idx):
+    """Training shapes at full size: the first and last (b, h) of every backward scheduling group."""
+    call = getattr(workloads, wl_name).calls[call_idx]
+    q, k, v, dO = workloads.make_qkvdo(call, "cuda")
+    c, s = workloads.rope_tables(call.T, call.D, device="cuda")
+    o, lse, dq, dk, dv = run(nc, q, k, v, dO, c, s, call.window, call.scale)
+    n_kb = (call.T + 127) // 128
+    pairs = call.B * call.H
+    group = min(pairs, (148 + n_kb - 1) // n_kb)
+    picks = sorted({divmod(bh, call.H) for g0 in range(0, pairs, group) for bh in (g0, min(g0 + group, pairs) - 1)})
+
+    def sel(x):
+        return torch.stack([x[b, :, h] for b, h in picks]).unsqueeze(2)
+
+    qs, ks, vs, dos = (sel(x).cpu() for x in (q, k, v, dO))
+    o_r, lse_r = oracle_mod.fwd_rotary(qs, ks, vs, c.cpu(), s.cpu(), call.window, call.scale)
+    dq_r, dk_r, dv_r = oracle_mod.bwd_rotary(qs, ks, vs, dos, c.cpu(), s.cpu(), call.window, call.scale)
+    got = [sel(x).float().cpu().numpy() for x in (o, dq, dk, dv)]
+    got_lse = torch.stack([lse[b, h] for b, h in picks]).cpu().numpy()
+    for i, (b, h) in enumerate(picks):
+        assert rel_err(got[0][i], o_r[i]) <= O_TOL, ("o", b, h)
+        assert abs_err(got_lse[i], lse_r[i, 0]) <= LSE_TOL, ("lse", b, h)
+        for name, g, r in zip(("dq", "dk", "dv"), got[1:], (dq_r, dk_r, dv_r)):
+            assert rel_err(g[i], r[i]) <= G_TOL, (name, b, h)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("inverse", [False, True])
+def test_standalone_turn_matches_oracle(nc, oracle_mod, D, inverse):
+    """The unfused turn: every element within one bf16 rounding of the fp64 turn (|err| <= 2^-8 |ref|,
+    plus 1e-5 for the fp32 products), and in place equal to out of place."""
+    B, T, H = 3, 301, 5
+    x = workloads.make_qkvdo_shape(B, T, H, D, seed=4200 + D, device="cuda")[0]
+    c, s = workloads.rope_tables(T, D, device="cuda")
+    y = nc.rotary(x, c, s, inverse=inverse)
+    ref = np.asarray(oracle_mod.rotary(x.cpu(), c.cpu(), s.cpu(), inverse=inverse))
+    got = y.float().cpu().numpy()
+    assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5).all()
+    x2 = x.clone()
+    nc.nc_rotary(x2, c, s, x2, inverse)
+    assert torch.equal(x2, y)
+    assert nc.nc_get_device_error() == 0
+
+
+def test_unfused_composition_equals_fused(nc):
+    """Turning q and k first and running the plain kernels gives the fused forward's o and lse bit for bit
+    (the fused kernels turn the same bf16 values with the same fp32 arithmetic before the products)."""
+    B, T, H, D, W = 2, 500, 3, 128, 200
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4300, device="cuda")
+    c, s = workloads.rope_tables(T, D, device="cuda")
+    o, lse = nc.attn_fwd_rotary(q, k, v, c, s, W, 0.1)
+    o2, lse2 = nc.attn_fwd(nc.rotary(q, c, s), nc.rotary(k, c, s), v, W, 0.1)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
