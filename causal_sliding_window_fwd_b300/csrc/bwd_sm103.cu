@@ -43,7 +43,6 @@
 #include "nc_attn.h"
 #include "nc_kernels.h"
 #include "nc_ptx.cuh"
-#include "nc_rotary.cuh"
 #include "nc_sched.cuh"
 #include "nc_tma.h"
 
@@ -56,7 +55,6 @@ constexpr int kQStages = 2;
 constexpr int kThreads = 512;
 // warps that read each work-item slot: the MMA warp, the 8 P/dS warps and the 4 dQ warps
 constexpr int kItemReaders = 13;
-constexpr int kRotThreads = 64;  // rotary variant: warps 2-3 rotate K and the Q blocks as they land (and read the ring)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // D = 128: dQ partials leave through a TMA reduce-add from a 64-row fp32 staging tile,
@@ -88,8 +86,6 @@ struct BwdBarriers {
     uint64_t v_empty;     // the item's last dP^T (the only reader of V) is done
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
-    uint64_t q_rot[kQStages];  // rotary variant: the Q block in this stage has been rotated in place
-    uint64_t k_rot;            // rotary variant: the item's K block has been rotated in place
     uint64_t do_full[2];
     uint64_t do_empty[2];
     uint64_t s_full;
@@ -126,10 +122,6 @@ struct BwdParams {
     // cu[d] .. cu[d+1]-1; n_kb then counts the key blocks of the longest document.  nullptr otherwise.
     const int* cu;
     int n_docs;
-    // Rotary variant: cos / sin tables fp32 [T, D/2] (row = position); q and k are rotated as they land,
-    // dK is turned back in its epilogue
-    const float* rcos;
-    const float* rsin;
     int* err;
 };
 
@@ -228,7 +220,7 @@ __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, flo
 }
 
 // kNoDq: dK and dV only (the deterministic backward computes dQ in a separate pass).
-template <int D, bool kVarlen, bool kNoDq = false, bool kRope = false>
+template <int D, bool kVarlen, bool kNoDq = false>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -255,9 +247,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars->q_full[s], 1);
             mbar_init(&bars->q_empty[s], 1);
-            mbar_init(&bars->q_rot[s], kRotThreads);
         }
-        mbar_init(&bars->k_rot, kRotThreads);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->do_full[s], 1);
             mbar_init(&bars->do_empty[s], 1);
@@ -275,7 +265,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(&bars->do_epi_free, 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&bars->item_full[s], 1);
-            mbar_init(&bars->item_empty[s], kItemReaders + (kRope ? 2 : 0));
+            mbar_init(&bars->item_empty[s], kItemReaders);
         }
         bars->abort = 0;
         fence_barrier_init();
@@ -289,9 +279,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 256 + D;
-    // warpgroup 0's register budget (its warps 2-3 rotate tiles in the rotary variant): 56, so that
-    // 128 x 56 + 256 x 152 + 128 x 152 = 65536, the launch budget of 512 x 128
-    constexpr uint32_t kWg0Regs = 56;
 
     // registers: 512 x 128 at launch = 65536; producer/MMA warpgroup drops to 56, the two
     // P/dS warpgroups rise to 152 and the dQ warpgroup to 152 (65536 in all), which lets
@@ -299,7 +286,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
-        regs_decrease<kWg0Regs>();
+        regs_decrease<56>();
         {
             if (lane == 0) {
                 tma_prefetch_desc(&tm_q);
@@ -384,7 +371,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
-        regs_decrease<kWg0Regs>();
+        regs_decrease<56>();
         {
             constexpr uint32_t id_kq = idesc_bf16(kBK, kBQ, false, false);  // S^T, dP^T
             constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
@@ -428,13 +415,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (w < 0) break;
                 const BwdItem item = bwd_item<kVarlen>(w, p);
-                ok = mbar_wait_warp(kRope ? &bars->k_rot : &bars->k_full, ii & 1) && !aborted(bars);
+                ok = mbar_wait_warp(&bars->k_full, ii & 1) && !aborted(bars);
                 if (!ok) break;
                 {
                     // first block of the item: S^T, then dP^T once the previous block's dQ has left DPT
                     const int st = gi % kQStages, so = gi % L::kDOStages;
-                    ok = mbar_wait_warp(kRope ? &bars->q_rot[st] : &bars->q_full[st], (gi / kQStages) & 1) &&
-                         !aborted(bars);
+                    ok = mbar_wait_warp(&bars->q_full[st], (gi / kQStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(st);
@@ -467,8 +453,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // the P/dS warps find it ready when they finish this block's dS.  (With dQ, the
                         // next dP^T waits for dQ to leave DPT, and issuing S^T early only moves the wait.)
                         const int st1 = (gi + 1) % kQStages;
-                        ok = mbar_wait_warp(kRope ? &bars->q_rot[st1] : &bars->q_full[st1], ((gi + 1) / kQStages) & 1) &&
-                             !aborted(bars);
+                        ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(st1);
@@ -507,9 +492,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // dP^T into DPT once this block's dQ has been read out
                         const int st1 = (gi + 1) % kQStages, so1 = (gi + 1) % L::kDOStages;
                         if (!kNoDq) {
-                            ok = mbar_wait_warp(kRope ? &bars->q_rot[st1] : &bars->q_full[st1],
-                                                ((gi + 1) / kQStages) & 1) &&
-                                 !aborted(bars);
+                            ok = mbar_wait_warp(&bars->q_full[st1], ((gi + 1) / kQStages) & 1) && !aborted(bars);
                             if (!ok) break;
                             tc_fence_after();
                             issue_s(st1);
@@ -531,38 +514,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_wait_warp(&bars->drain, 0);
         }
     } else if (warp < 4) {
-        regs_decrease<kWg0Regs>();
-        if constexpr (kRope) {
-            // ------------------------------------------------------------ rotary prologue
-            // warps 2-3 rotate each item's K block and every Q block in place as they land
-            const int rt = threadIdx.x - 64;
-            bool ok = true;
-            int gq = 0;  // Q blocks over all items (ring position)
-            for (int ii = 0; ok; ++ii) {
-                const int w = read_item(bars, ii);
-                if (w == -2) {
-                    ok = false;
-                    break;
-                }
-                if (w < 0) break;
-                const BwdItem item = bwd_item<kVarlen>(w, p);
-                ok = mbar_wait_warp(&bars->k_full, ii & 1) && !aborted(bars);
-                if (!ok) break;
-                rotate_tile<D>(smem + L::kK, item.j0, p.T, p.rcos, p.rsin, rt, kRotThreads);
-                fence_async_smem();
-                mbar_arrive(&bars->k_rot);
-                for (int it = 0; it < item.n_it; ++it, ++gq) {
-                    const int st = gq % kQStages;
-                    ok = mbar_wait_warp(&bars->q_full[st], (gq / kQStages) & 1) && !aborted(bars);
-                    if (!ok) break;
-                    rotate_tile<D>(smem + L::kQ + st * L::kTile, (item.m_lo + it) * kBQ, p.T, p.rcos, p.rsin, rt,
-                                   kRotThreads);
-                    fence_async_smem();
-                    mbar_arrive(&bars->q_rot[st]);
-                }
-            }
-            if (!ok) record_timeout(bars, p.err);
-        }
+        regs_decrease<56>();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ P^T / dS^T (thread = key row)
         regs_increase<152>();
@@ -761,16 +713,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const bool partial = kVarlen && j0 + kBK > item.len;
                 __nv_bfloat16* grow = (g ? p.dv : p.dk) +
                                       ((static_cast<size_t>(b) * p.T + item.base + j) * p.H + h) * D;
-                // one 32-column chunk of the row, scaled, packed and placed (staged tile or, for a varlen
-                // block past its document, straight to global memory)
-                auto put32 = [&](int c, const float (&f)[32]) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(a + c * 32, r);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
                         uint4 pkt;
-                        pkt.x = pack_bf16x2(f[8 * v4 + 0] * mul, f[8 * v4 + 1] * mul);
-                        pkt.y = pack_bf16x2(f[8 * v4 + 2] * mul, f[8 * v4 + 3] * mul);
-                        pkt.z = pack_bf16x2(f[8 * v4 + 4] * mul, f[8 * v4 + 5] * mul);
-                        pkt.w = pack_bf16x2(f[8 * v4 + 6] * mul, f[8 * v4 + 7] * mul);
+                        pkt.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+                        pkt.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+                        pkt.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+                        pkt.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
                         // columns 32c + 8 v4 .. +7: 16-byte unit 4 (c % 2) + v4 of the row's 64-column chunk c / 2
                         const int unit = 4 * (c % 2) + v4;
                         if (partial) {
@@ -779,48 +732,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             *reinterpret_cast<uint4*>(tile + (c / 2) * (kBK * 128) + tid * 128 + ((unit ^ (tid & 7)) << 4)) =
                                 pkt;
                         }
-                    }
-                };
-                if (kRope && g == 0) {
-                    // dK is the gradient with respect to the rotated keys: turn it back (the transpose of
-                    // key row j's rotation) before it leaves; dimension i pairs with i + D/2, i.e. chunk c
-                    // with chunk c + D/64
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        uint32_t r1[32], r2[32];
-                        tmem_ld32(a + c * 32, r1);
-                        tmem_ld32(a + (c + D / 64) * 32, r2);
-                        float f1[32], f2[32];
-#pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            float x1[8], x2[8], cs[8], sn[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                x1[e] = __uint_as_float(r1[8 * g8 + e]);
-                                x2[e] = __uint_as_float(r2[8 * g8 + e]);
-                            }
-                            const int pos = min(j, p.T - 1);  // rows past T are not stored
-                            load_cs8(p.rcos + static_cast<size_t>(pos) * (D / 2) + 32 * c + 8 * g8, cs);
-                            load_cs8(p.rsin + static_cast<size_t>(pos) * (D / 2) + 32 * c + 8 * g8, sn);
-                            turn8<true>(x1, x2, cs, sn);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                f1[8 * g8 + e] = x1[e];
-                                f2[8 * g8 + e] = x2[e];
-                            }
-                        }
-                        put32(c, f1);
-                        put32(c + D / 64, f2);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(a + c * 32, r);
-                        float f[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(r[e]);
-                        put32(c, f);
                     }
                 }
                 fence_async_smem();
@@ -1009,32 +920,62 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
     reinterpret_cast<uint4*>(dq)[t] = pkt;
 }
 
-// Rotary variant: dq = bf16(scale * R_t^T dQ accumulator), the accumulated gradient with respect to the rotated
-// query of position t turned back.  One thread per (row, 4 pairs): dimensions 4k .. 4k+3 and their partners
-// 4k + D/2 .. 4k + D/2 + 3.
+// Rotary variant of the conversion pass.  The main kernel ran on the turned rows qr, kr, so its dQ
+// accumulator and dk hold gradients with respect to the turned q and k; both are turned back here by the
+// transpose of row t's rotation (x1 = y1 c + y2 s, x2 = y2 c - y1 s, with the turn's explicit roundings):
+// dq = bf16(scale * turned-back accumulator), dk turned back in place.  One thread per (row, 8 pairs):
+// dimensions 8u .. 8u+7 and their partners 8u + D/2 ..; the table entries are read once for both.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_rope_kernel(const float* __restrict__ dq_acc,
-                                                            __nv_bfloat16* __restrict__ dq,
+                                                            __nv_bfloat16* __restrict__ dq, __nv_bfloat16* dk,
                                                             const float* __restrict__ rcos,
-                                                            const float* __restrict__ rsin, size_t n_quads, int T,
+                                                            const float* __restrict__ rsin, size_t n_units, int T,
                                                             int H, float scale) {
-    constexpr int kQuads = D / 8;  // 4-pair groups per row
+    constexpr int kUnits = D / 16;
     const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= n_quads) return;
-    const size_t row = t / kQuads;
-    const int k4 = static_cast<int>(t - row * kQuads) * 4;
+    if (t >= n_units) return;
+    const size_t row = t / kUnits;
+    const int u = static_cast<int>(t - row * kUnits);
     const int pos = static_cast<int>((row / H) % T);
-    const float4 y1 = *reinterpret_cast<const float4*>(dq_acc + row * D + k4);
-    const float4 y2 = *reinterpret_cast<const float4*>(dq_acc + row * D + D / 2 + k4);
-    const float4 c = __ldg(reinterpret_cast<const float4*>(rcos + (size_t)pos * (D / 2) + k4));
-    const float4 s = __ldg(reinterpret_cast<const float4*>(rsin + (size_t)pos * (D / 2) + k4));
-    // transpose of the turn: x1 = y1 c + y2 s, x2 = -y1 s + y2 c
-    const float a0 = (y1.x * c.x + y2.x * s.x) * scale, b0 = (-y1.x * s.x + y2.x * c.x) * scale;
-    const float a1 = (y1.y * c.y + y2.y * s.y) * scale, b1 = (-y1.y * s.y + y2.y * c.y) * scale;
-    const float a2 = (y1.z * c.z + y2.z * s.z) * scale, b2 = (-y1.z * s.z + y2.z * c.z) * scale;
-    const float a3 = (y1.w * c.w + y2.w * s.w) * scale, b3 = (-y1.w * s.w + y2.w * c.w) * scale;
-    *reinterpret_cast<uint2*>(dq + row * D + k4) = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
-    *reinterpret_cast<uint2*>(dq + row * D + D / 2 + k4) = make_uint2(pack_bf16x2(b0, b1), pack_bf16x2(b2, b3));
+    const size_t e1 = row * D + 8 * u, e2 = e1 + D / 2;  // first element of the unit and of its partners
+    const float4 a0 = *reinterpret_cast<const float4*>(dq_acc + e1);
+    const float4 a1 = *reinterpret_cast<const float4*>(dq_acc + e1 + 4);
+    const float4 b0 = *reinterpret_cast<const float4*>(dq_acc + e2);
+    const float4 b1 = *reinterpret_cast<const float4*>(dq_acc + e2 + 4);
+    const uint4 k1 = *reinterpret_cast<const uint4*>(dk + e1);
+    const uint4 k2 = *reinterpret_cast<const uint4*>(dk + e2);
+    const float4 c0 = __ldg(reinterpret_cast<const float4*>(rcos + (size_t)pos * (D / 2) + 8 * u));
+    const float4 c1 = __ldg(reinterpret_cast<const float4*>(rcos + (size_t)pos * (D / 2) + 8 * u) + 1);
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(rsin + (size_t)pos * (D / 2) + 8 * u));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(rsin + (size_t)pos * (D / 2) + 8 * u) + 1);
+    const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const float q1[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float q2[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w}, kw2[4] = {k2.x, k2.y, k2.z, k2.w};
+    uint32_t oq1[4], oq2[4], ok1[4], ok2[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float r1[2], r2[2], t1[2], t2[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int e = 2 * w + h2;
+            r1[h2] = __fmaf_rn(q1[e], cv[e], __fmul_rn(q2[e], sv[e])) * scale;
+            r2[h2] = __fmaf_rn(q2[e], cv[e], -__fmul_rn(q1[e], sv[e])) * scale;
+            const float y1 = __uint_as_float(h2 ? (kw1[w] & 0xffff0000u) : (kw1[w] << 16));
+            const float y2 = __uint_as_float(h2 ? (kw2[w] & 0xffff0000u) : (kw2[w] << 16));
+            t1[h2] = __fmaf_rn(y1, cv[e], __fmul_rn(y2, sv[e]));
+            t2[h2] = __fmaf_rn(y2, cv[e], -__fmul_rn(y1, sv[e]));
+        }
+        oq1[w] = pack_bf16x2(r1[0], r1[1]);
+        oq2[w] = pack_bf16x2(r2[0], r2[1]);
+        ok1[w] = pack_bf16x2(t1[0], t1[1]);
+        ok2[w] = pack_bf16x2(t2[0], t2[1]);
+    }
+    *reinterpret_cast<uint4*>(dq + e1) = make_uint4(oq1[0], oq1[1], oq1[2], oq1[3]);
+    *reinterpret_cast<uint4*>(dq + e2) = make_uint4(oq2[0], oq2[1], oq2[2], oq2[3]);
+    *reinterpret_cast<uint4*>(dk + e1) = make_uint4(ok1[0], ok1[1], ok1[2], ok1[3]);
+    *reinterpret_cast<uint4*>(dk + e2) = make_uint4(ok2[0], ok2[1], ok2[2], ok2[3]);
 }
 
 // cu != nullptr: document-masked packed rows (B = 1, T = total), n_docs documents of at most max_len rows.
@@ -1073,17 +1014,14 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     p.work = work;
     p.cu = cu;
     p.n_docs = n_docs;
-    p.rcos = rcos;
-    p.rsin = rsin;
     p.err = err;
     const int smem = BwdSmem<D>::kBytes;
     // the shared-memory limit is raised once per device and variant (atomic flags), the SM count
     // is looked up on every call
-    static std::atomic<bool> attr_done[4][kAttrDevices];
-    const int variant = rcos != nullptr ? 3 : (deterministic ? 2 : (cu != nullptr ? 1 : 0));
-    auto kern = variant == 3   ? bwd_main_kernel<D, false, false, true>
-                : variant == 2 ? bwd_main_kernel<D, false, true>
-                               : (variant == 1 ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
+    static std::atomic<bool> attr_done[3][kAttrDevices];
+    const int variant = deterministic ? 2 : (cu != nullptr ? 1 : 0);
+    auto kern = variant == 2 ? bwd_main_kernel<D, false, true>
+                             : (variant == 1 ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, attr_done[variant]);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (its shared memory and TMEM allow one), looping over the items
@@ -1104,9 +1042,9 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         return launch_bwd_dq(q, k, v, dO, lse, delta, dq, B, T, H, D, window, scale, work + 1, err, st);
     }
     if (rcos != nullptr) {
-        const size_t nq = (size_t)rows * (D / 8);
-        bwd_post_rope_kernel<D><<<(unsigned)((nq + 255) / 256), 256, 0, st>>>(
-            dq_acc, static_cast<__nv_bfloat16*>(dq), rcos, rsin, nq, T, H, scale);
+        const size_t nu = (size_t)rows * (D / 16);
+        bwd_post_rope_kernel<D><<<(unsigned)((nu + 255) / 256), 256, 0, st>>>(
+            dq_acc, static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), rcos, rsin, nu, T, H, scale);
         count_launches(3);
         return cudaGetLastError();
     }
@@ -1138,14 +1076,14 @@ cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const
                                         work, cu, n_docs, max_len, err, st);
 }
 
-cudaError_t launch_bwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin,
+cudaError_t launch_bwd_rotary(const void* qr, const void* kr, const void* v, const float* rcos, const float* rsin,
                               const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                               int T, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
                               int* err, cudaStream_t st) {
-    return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
-                                         nullptr, 0, 0, err, st, false, rcos, rsin)
-                    : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta, work,
-                                        nullptr, 0, 0, err, st, false, rcos, rsin);
+    return D == 128 ? launch_bwd_tc<128>(qr, kr, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta,
+                                         work, nullptr, 0, 0, err, st, false, rcos, rsin)
+                    : launch_bwd_tc<64>(qr, kr, v, o, dO, lse, dq, dk, dv, B, T, H, window, scale, dq_acc, delta,
+                                        work, nullptr, 0, 0, err, st, false, rcos, rsin);
 }
 
 cudaError_t launch_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,

@@ -30,6 +30,7 @@ constexpr int kDecodeMaxThreads = 320;
 // shared memory) and cuts ranges of at least kMinRowsPerCta rows.
 constexpr int kBalancedMaxSeqs = 1024;
 constexpr int kMinRowsPerCta = 16;
+constexpr int kCombineFast = 8;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -262,8 +263,9 @@ decode_balanced_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
 }
 
 // Balanced combine, one warp per (sequence, head): the CTAs c0 .. c1 whose ranges hold sequence n's rows
-// left partials in slots n + c0 .. n + c1.  Three dependent rounds of loads: the maxima, the sums with
-// their weights, then the outputs, issued four partials at a time.
+// left partials in slots n + c0 .. n + c1.  Up to kCombineFast partials are read in one round of loads;
+// more take three dependent rounds (the maxima, the sums with their weights, then the outputs, four
+// partials at a time) per 32 partials.
 template <int D>
 __global__ void __launch_bounds__(256)
 decode_balanced_combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
@@ -288,45 +290,74 @@ decode_balanced_combine_kernel(const float* __restrict__ part_ml, const float* _
     const int P = meta[n], V = meta[n + 1] - P, per = meta[N + 1];
     const int c0 = P / per, k = (P + V - 1) / per - c0 + 1;
     const size_t base = ((size_t)n + c0) * H + h;  // partial s at base + s * H
-    float M = -INFINITY;
-    for (int s = lane; s < k; s += 32) M = fmaxf(M, part_ml[(base + (size_t)s * H) * 2]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float lsum = 0.f, acc[E];
+    float M = -INFINITY, lsum = 0.f, acc[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < k; s0 += 32) {
-        const int cnt = min(32, k - s0);
-        float w = 0.f, lw = 0.f;
-        if (lane < cnt) {
-            const float* ml = part_ml + (base + (size_t)(s0 + lane) * H) * 2;
-            w = exp2f(ml[0] - M);
-            lw = ml[1] * w;
-        }
+    if (k <= kCombineFast) {
+        // one round of loads: every lane reads all (max, sum) pairs (the same addresses across the warp) and
+        // its E columns of every partial, then merges them with no further memory round trip
+        float mv[kCombineFast], lv[kCombineFast], ov[kCombineFast][E];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
-        lsum += lw;
-        int j = 0;
-        for (; j + 4 <= cnt; j += 4) {
-            float ov[4][E];
+        for (int s = 0; s < kCombineFast; ++s) {
+            mv[s] = -INFINITY;
+            lv[s] = 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float* po = part_o + (base + (size_t)(s0 + j + u) * H) * D + lane * E;
+            for (int i = 0; i < E; ++i) ov[s][i] = 0.f;
+            if (s < k) {
+                const size_t pidx = base + (size_t)s * H;
+                mv[s] = part_ml[pidx * 2];
+                lv[s] = part_ml[pidx * 2 + 1];
+                const float* po = part_o + pidx * D + lane * E;
 #pragma unroll
-                for (int i = 0; i < E; ++i) ov[u][i] = po[i];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float wu = __shfl_sync(0xffffffffu, w, j + u);
-#pragma unroll
-                for (int i = 0; i < E; ++i) acc[i] = fmaf(ov[u][i], wu, acc[i]);
+                for (int i = 0; i < E; ++i) ov[s][i] = po[i];
             }
         }
-        for (; j < cnt; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float* po = part_o + (base + (size_t)(s0 + j) * H) * D + lane * E;
 #pragma unroll
-            for (int i = 0; i < E; ++i) acc[i] = fmaf(po[i], wj, acc[i]);
+        for (int s = 0; s < kCombineFast; ++s) M = fmaxf(M, mv[s]);
+#pragma unroll
+        for (int s = 0; s < kCombineFast; ++s) {
+            const float w = s < k ? exp2f(mv[s] - M) : 0.f;
+            lsum = fmaf(lv[s], w, lsum);
+#pragma unroll
+            for (int i = 0; i < E; ++i) acc[i] = fmaf(ov[s][i], w, acc[i]);
+        }
+    } else {
+        for (int s = lane; s < k; s += 32) M = fmaxf(M, part_ml[(base + (size_t)s * H) * 2]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        for (int s0 = 0; s0 < k; s0 += 32) {
+            const int cnt = min(32, k - s0);
+            float w = 0.f, lw = 0.f;
+            if (lane < cnt) {
+                const float* ml = part_ml + (base + (size_t)(s0 + lane) * H) * 2;
+                w = exp2f(ml[0] - M);
+                lw = ml[1] * w;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+            lsum += lw;
+            int j = 0;
+            for (; j + 4 <= cnt; j += 4) {
+                float ov[4][E];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float* po = part_o + (base + (size_t)(s0 + j + u) * H) * D + lane * E;
+#pragma unroll
+                    for (int i = 0; i < E; ++i) ov[u][i] = po[i];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float wu = __shfl_sync(0xffffffffu, w, j + u);
+#pragma unroll
+                    for (int i = 0; i < E; ++i) acc[i] = fmaf(ov[u][i], wu, acc[i]);
+                }
+            }
+            for (; j < cnt; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                const float* po = part_o + (base + (size_t)(s0 + j) * H) * D + lane * E;
+#pragma unroll
+                for (int i = 0; i < E; ++i) acc[i] = fmaf(po[i], wj, acc[i]);
+            }
         }
     }
     const float inv = 1.f / lsum;

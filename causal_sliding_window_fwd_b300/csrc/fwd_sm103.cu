@@ -32,7 +32,6 @@
 #include "nc_attn.h"
 #include "nc_kernels.h"
 #include "nc_ptx.cuh"
-#include "nc_rotary.cuh"
 #include "nc_sched.cuh"
 #include "nc_tma.h"
 
@@ -44,7 +43,6 @@ constexpr int kBN = 128;          // keys per block
 constexpr int kStages = 4;        // K/V ring slots
 constexpr int kThreads = 512;     // 16 warps
 constexpr int kItemReaders = 13;  // warps that read each work-item slot: the MMA warp, 8 softmax warps, 4 epilogue warps
-constexpr int kRotThreads = 64;   // rotary variant: warps 2-3 rotate the Q tiles and key blocks as they land
 
 // Varlen work-item counters: one {next item, CTAs finished} pair per call, taken round-robin
 // from this ring.  They are zero at load, and the last CTA of each launch zeroes its pair
@@ -73,8 +71,6 @@ struct FwdBarriers {
     uint64_t kv_empty[kStages];
     uint64_t q_full;
     uint64_t q_empty;
-    uint64_t q_rot;              // rotary variant: the item's Q tiles have been rotated in place
-    uint64_t k_rot[kStages];     // rotary variant: the key block in this ring slot has been rotated
     uint64_t s_full[2];
     uint64_t p_full[2];
     // row statistics (m, l) handed from a tile's softmax warpgroup to the epilogue, in two slots
@@ -111,15 +107,11 @@ struct FwdParams {
     int* work;            // varlen: {next item, CTAs finished}, zero on entry and left zero on exit
     float scale_log2;
     int n_pairs;          // query-tile pairs per (b, h), or per (document, h): the longest document's
-    // Rotary variant: cos / sin tables fp32 [Tk, D/2] (row = position); q and k are rotated as they land
-    const float* rcos;
-    const float* rsin;
     int* err;
 };
 
-// Forward variants: plain, prefill over a KV cache, document-masked packed rows, plain with the rotary
-// embedding of q and k fused into the load stage.
-enum FwdMode { kModePlain = 0, kModeCache = 1, kModeVarlen = 2, kModeRope = 3 };
+// Forward variants: plain, prefill over a KV cache, document-masked packed rows.
+enum FwdMode { kModePlain = 0, kModeCache = 1, kModeVarlen = 2 };
 
 // Key blocks [lo, hi] that intersect the window of some query of the tile whose first query sits at
 // position pos0; the last query of the sequence sits at position last.
@@ -258,8 +250,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.q_empty, 1);
-        mbar_init(&bars.q_rot, kRotThreads);
-        for (int i = 0; i < kStages; ++i) mbar_init(&bars.k_rot[i], kRotThreads);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars.s_full[t], 1);
             mbar_init(&bars.p_full[t], kBM);
@@ -287,10 +277,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    // 512 threads x 128 registers at launch; the producer/MMA warpgroup drops to 56 (64 in the rotary
-    // variant, whose warps 2-3 rotate tiles), the softmax warpgroups rise to 176 and the epilogue drops
-    // to 96 (128 x 64 + 256 x 176 + 128 x 96 <= 65536)
-    constexpr uint32_t kWg0Regs = kMode == kModeRope ? 64 : 56;
+    // 512 threads x 128 registers at launch; the producer/MMA warpgroup drops to 56, the softmax
+    // warpgroups rise to 176 and the epilogue drops to 96 (128 x 56 + 256 x 176 + 128 x 96 <= 65536)
     const uint32_t col_s[2] = {0u, 128u};
     const uint32_t col_o[2] = {256u, 256u + D};
     const int my_items = kMode == kModeVarlen ? 0 : sched_items_of_cta(n_items);
@@ -298,7 +286,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // the whole warp runs this loop converged; lane 0 issues each copy
-        regs_decrease<kWg0Regs>();
+        regs_decrease<56>();
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -372,7 +360,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // the whole warp runs this loop converged; lane 0 issues each product
-        regs_decrease<kWg0Regs>();
+        regs_decrease<56>();
         constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
         const uint32_t q_base = smem_u32(smem + L::kQOff);
@@ -419,12 +407,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             auto act = [&](int t, int kb) {
                 return t ? (kb >= it.lo[1] && kb <= it.hi[1]) : (kb >= it.lo[0] && kb <= it.hi[0]);
             };
-            ok = mbar_wait_warp(kMode == kModeRope ? &bars.q_rot : &bars.q_full, ip & 1);
+            ok = mbar_wait_warp(&bars.q_full, ip & 1);
             if (!ok) break;
             {
                 const int slot_k = seq % kStages;
-                ok = mbar_wait_warp(kMode == kModeRope ? &bars.k_rot[slot_k] : &bars.kv_full[slot_k],
-                                    (seq / kStages) & 1);
+                ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t)
@@ -473,8 +460,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                     if (next && act(t, kb + 1)) {
                         if (!k_ready) {
-                            ok = mbar_wait_warp(kMode == kModeRope ? &bars.k_rot[slot_k] : &bars.kv_full[slot_k],
-                                                (seq / kStages) & 1);
+                            ok = mbar_wait_warp(&bars.kv_full[slot_k], (seq / kStages) & 1);
                             if (!ok) break;
                             tc_fence_after();
                             k_ready = true;
@@ -498,39 +484,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mma_commit_w(&bars.drain);
         mbar_wait_warp(&bars.drain, 0);
     } else if (warp < 4) {
-        regs_decrease<kWg0Regs>();
-        if constexpr (kMode == kModeRope) {
-            // ------------------------------------------------------------ rotary prologue
-            // warps 2-3 rotate each item's Q tiles and every key block in place as they land, in the
-            // order the producer loads them (K and V alternate, so keys use the even ring positions)
-            const int rt = threadIdx.x - 64;
-            bool ok = true;
-            int seq = 0, ip = 0;
-            for (int ii = 0; ok && ii < my_items; ++ii) {
-                const FwdItem it = fwd_item<kMode>(sched_item_index(ii), p);
-                if (it.empty) continue;  // the producer loads nothing for it
-                ok = mbar_wait_warp(&bars.q_full, ip & 1) && !aborted(bars);
-                if (!ok) break;
-                for (int t = 0; t < 2; ++t)
-                    if (t == 0 || it.active1)
-                        rotate_tile<D>(smem + L::kQOff + t * L::kTileBytes, t ? it.r0[1] : it.r0[0], p.Tq, p.rcos,
-                                       p.rsin, rt, kRotThreads);
-                fence_async_smem();
-                mbar_arrive(&bars.q_rot);
-                const int n_loads = 2 * (it.kb_hi - it.kb_lo + 1);
-                for (int x = 0; x < n_loads; x += 2, seq += 2) {
-                    const int slot = seq % kStages;
-                    ok = mbar_wait_warp(&bars.kv_full[slot], (seq / kStages) & 1) && !aborted(bars);
-                    if (!ok) break;
-                    rotate_tile<D>(smem + L::kKVOff + slot * L::kTileBytes, (it.kb_lo + x / 2) * kBN, p.Tk, p.rcos,
-                                   p.rsin, rt, kRotThreads);
-                    fence_async_smem();
-                    mbar_arrive(&bars.k_rot[slot]);
-                }
-                ++ip;
-            }
-            if (!ok) record_timeout(bars, p.err);
-        }
+        regs_decrease<56>();
     } else if (warp < 12) {
         // ------------------------------------------------------------ softmax of one query tile
         // one thread per query row: the whole 128-key row of S is read from TMEM with one wait,
@@ -763,7 +717,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 template <int D>
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int* lens, const int* cu, int n_docs,
                           int max_len, void* o, float* lse, int B, int Tq, int Tk, int H, int window, float scale,
-                          int* err, cudaStream_t st, const float* rcos = nullptr, const float* rsin = nullptr) {
+                          int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv, to;
     if (!make_tmap_bthd(&tq, q, B, Tq, H, D, 64, kBM) || !make_tmap_bthd(&tk, k, B, Tk, H, D, 64, kBN) ||
         !make_tmap_bthd(&tv, v, B, Tk, H, D, 64, kBN) || !make_tmap_bthd(&to, o, B, Tq, H, D, 64, kBM))
@@ -778,8 +732,6 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     p.cu = cu;
     p.n_docs = n_docs;
     p.work = nullptr;
-    p.rcos = rcos;
-    p.rsin = rsin;
     p.H = H;
     p.W = (window <= 0 || window >= Tk) ? Tk : window;
     p.scale_log2 = scale * kLog2e;
@@ -789,11 +741,10 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     // The SM count and the counter ring's address are looked up on every call, the shared-memory
     // limit is raised once per device and variant (atomic flags): nothing that concurrent first calls
     // from several host threads could race on.
-    static std::atomic<bool> attr_done[4][kAttrDevices];
-    const int variant = rcos != nullptr ? 3 : (cu != nullptr ? 2 : (lens != nullptr ? 1 : 0));
-    auto kern = variant == 3   ? fwd_tc_kernel<D, kModeRope>
-                : variant == 2 ? fwd_tc_kernel<D, kModeVarlen>
-                               : (variant == 1 ? fwd_tc_kernel<D, kModeCache> : fwd_tc_kernel<D, kModePlain>);
+    static std::atomic<bool> attr_done[3][kAttrDevices];
+    const int variant = cu != nullptr ? 2 : (lens != nullptr ? 1 : 0);
+    auto kern = variant == 2 ? fwd_tc_kernel<D, kModeVarlen>
+                             : (variant == 1 ? fwd_tc_kernel<D, kModeCache> : fwd_tc_kernel<D, kModePlain>);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, attr_done[variant]);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (shared memory and TMEM allow one), looping over the items
@@ -820,15 +771,6 @@ cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int window, float scale, int* err, cudaStream_t st) {
     return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st)
                     : launch_fwd_tc<64>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st);
-}
-
-cudaError_t launch_fwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin, void* o,
-                              float* lse, int B, int T, int H, int D, int window, float scale, int* err,
-                              cudaStream_t st) {
-    return D == 128 ? launch_fwd_tc<128>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st,
-                                         rcos, rsin)
-                    : launch_fwd_tc<64>(q, k, v, nullptr, nullptr, 0, 0, o, lse, B, T, T, H, window, scale, err, st,
-                                        rcos, rsin);
 }
 
 cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,

@@ -81,24 +81,30 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 }
 
 nc_status nc_attn_fwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
-                             void* o, float* lse, int B, int T, int H, int D, int window, float scale,
-                             cudaStream_t stream) {
+                             void* qr, void* kr, void* o, float* lse, int B, int T, int H, int D, int window,
+                             float scale, cudaStream_t stream) {
     nc_status st = check_shape(B, T, H, D, window, scale);
     if (st != NC_OK) return st;
-    if (!q || !k || !v || !rope_cos || !rope_sin || !o || !lse) return NC_ERR_INVALID;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
-        !aligned16(o) || !aligned16(lse))
-        return NC_ERR_INVALID;
+    if (!q || !k || !v || !rope_cos || !rope_sin || !qr || !kr || !o || !lse) return NC_ERR_INVALID;
+    const void* all[9] = {q, k, v, rope_cos, rope_sin, qr, kr, o, lse};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return NC_ERR_INVALID;
     const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4, nt = (size_t)T * (D / 2) * 4;
     const void* ins[5] = {q, k, v, rope_cos, rope_sin};
     const size_t in_n[5] = {nb, nb, nb, nt, nt};
-    for (int i = 0; i < 5; ++i)
-        if (overlap(ins[i], in_n[i], o, nb) || overlap(ins[i], in_n[i], lse, nl)) return NC_ERR_INVALID;
-    if (overlap(o, nb, lse, nl)) return NC_ERR_INVALID;
+    const void* outs[4] = {qr, kr, o, lse};
+    const size_t out_n[4] = {nb, nb, nb, nl};
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 5; ++i)
+            if (overlap(ins[i], in_n[i], outs[a], out_n[a])) return NC_ERR_INVALID;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], out_n[a], outs[b], out_n[b])) return NC_ERR_INVALID;
+    }
     int* err = error_word();
     if (err == nullptr) return NC_ERR_CUDA;
-    const cudaError_t e =
-        nc::launch_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, B, T, H, D, window, scale, err, stream);
+    cudaError_t e = nc::launch_rotary(q, qr, k, kr, rope_cos, rope_sin, B, T, H, D, false, stream);
+    if (e != cudaSuccess) return NC_ERR_CUDA;
+    e = nc::launch_fwd(qr, kr, v, o, lse, B, T, H, D, window, scale, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -111,7 +117,7 @@ nc_status nc_rotary(const void* x, const float* rope_cos, const float* rope_sin,
     const size_t nb = (size_t)B * T * H * D * 2, nt = (size_t)T * (D / 2) * 4;
     if (x != y && overlap(x, nb, y, nb)) return NC_ERR_INVALID;
     if (overlap(rope_cos, nt, y, nb) || overlap(rope_sin, nt, y, nb)) return NC_ERR_INVALID;
-    const cudaError_t e = nc::launch_rotary(x, rope_cos, rope_sin, y, B, T, H, D, inverse != 0, stream);
+    const cudaError_t e = nc::launch_rotary(x, y, nullptr, nullptr, rope_cos, rope_sin, B, T, H, D, inverse != 0, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -253,21 +259,21 @@ nc_status nc_attn_bwd(const void* q, const void* k, const void* v, const void* o
                     false);
 }
 
-nc_status nc_attn_bwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
-                             const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
-                             int T, int H, int D, int window, float scale, void* workspace, size_t workspace_bytes,
-                             cudaStream_t stream) {
+nc_status nc_attn_bwd_rotary(const void* qr, const void* kr, const void* v, const float* rope_cos,
+                             const float* rope_sin, const void* o, const void* dO, const float* lse, void* dq, void* dk,
+                             void* dv, int B, int T, int H, int D, int window, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
     nc_status st = check_shape(B, T, H, D, window, scale);
     if (st != NC_OK) return st;
-    if (!q || !k || !v || !rope_cos || !rope_sin || !o || !dO || !lse || !dq || !dk || !dv) return NC_ERR_INVALID;
-    const void* all[11] = {q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv};
+    if (!qr || !kr || !v || !rope_cos || !rope_sin || !o || !dO || !lse || !dq || !dk || !dv) return NC_ERR_INVALID;
+    const void* all[11] = {qr, kr, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv};
     for (const void* p : all)
         if (!aligned16(p)) return NC_ERR_INVALID;
     const size_t need = nc_attn_bwd_workspace_bytes(B, T, H, D);
     if (workspace == nullptr || workspace_bytes < need) return NC_ERR_WORKSPACE;
     if (!aligned16(workspace)) return NC_ERR_INVALID;
     const size_t nb = (size_t)B * T * H * D * 2, nl = (size_t)B * H * T * 4, nt = (size_t)T * (D / 2) * 4;
-    const void* ins[8] = {q, k, v, rope_cos, rope_sin, o, dO, lse};
+    const void* ins[8] = {qr, kr, v, rope_cos, rope_sin, o, dO, lse};
     const size_t in_n[8] = {nb, nb, nb, nt, nt, nb, nb, nl};
     void* outs[4] = {dq, dk, dv, workspace};
     const size_t out_n[4] = {nb, nb, nb, need};
@@ -285,7 +291,7 @@ nc_status nc_attn_bwd_rotary(const void* q, const void* k, const void* v, const 
     float* delta = reinterpret_cast<float*>(ws);
     ws += round_up((size_t)B * H * T * 4, 256);
     int* work = reinterpret_cast<int*>(ws);
-    const cudaError_t e = nc::launch_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, B, T, H, D,
+    const cudaError_t e = nc::launch_bwd_rotary(qr, kr, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, B, T, H, D,
                                                 window, scale, dq_acc, delta, work, err, stream);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }

@@ -27,14 +27,12 @@ cudaError_t ensure_smem_attr(const void* kern, int bytes, std::atomic<bool>* don
 cudaError_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int H, int D,
                        int window, float scale, int* err, cudaStream_t st);
 
-// Forward with the rotary embedding of q and k (tables rcos, rsin fp32 [T, D/2]) fused into the load stage.
-cudaError_t launch_fwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin, void* o,
-                              float* lse, int B, int T, int H, int D, int window, float scale, int* err,
-                              cudaStream_t st);
+// Rotary turn of x0 into y0 and, if x1 is not null, of x1 into y1 in the same launch: [B,T,H,D] bf16,
+// tables rcos, rsin fp32 [T, D/2]; `inverse` applies the transpose.  y may equal x (in place).
+cudaError_t launch_rotary(const void* x0, void* y0, const void* x1, void* y1, const float* rcos, const float* rsin,
+                          int B, int T, int H, int D, bool inverse, cudaStream_t st);
 
 // Document-masked forward over packed rows: q/k/v/o [total,H,D] bf16, lse [H,total] fp32, cu device int32 [n_docs+1].
-cudaError_t launch_rotary(const void* x, const float* rcos, const float* rsin, void* y, int B, int T, int H, int D,
-                          bool inverse, cudaStream_t st);
 cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const int* cu, int n_docs, int max_len,
                               void* o, float* lse, int total, int H, int D, int window, float scale, int* err,
                               cudaStream_t st);
@@ -55,8 +53,9 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,
                        float* dq_acc, float* delta, int* work, int* err, cudaStream_t st);
 
-// Backward of the rotary forward: dq and dk with respect to the unrotated q and k.  Workspace as for launch_bwd.
-cudaError_t launch_bwd_rotary(const void* q, const void* k, const void* v, const float* rcos, const float* rsin,
+// Backward of attention over turned rows qr, kr: dq and dk with respect to the unturned q and k (both turned
+// back in the conversion pass, dk in place).  Workspace as for launch_bwd.
+cudaError_t launch_bwd_rotary(const void* qr, const void* kr, const void* v, const float* rcos, const float* rsin,
                               const void* o, const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                               int T, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
                               int* err, cudaStream_t st);

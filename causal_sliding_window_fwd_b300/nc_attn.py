@@ -72,7 +72,7 @@ def _load():
     lib.nc_attn_fwd_varlen.restype = i
     lib.nc_attn_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_bwd_varlen.restype = i
-    lib.nc_attn_fwd_rotary.argtypes = [vp] * 7 + [i, i, i, i, i, f, vp]
+    lib.nc_attn_fwd_rotary.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp]
     lib.nc_attn_fwd_rotary.restype = i
     lib.nc_attn_bwd_rotary.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_bwd_rotary.restype = i
@@ -178,30 +178,30 @@ def _rope_tables(rope_cos, rope_sin, T, D):
     _need(rope_sin, "rope_sin", torch.float32, (T, D // 2))
 
 
-def nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, window: int, scale: float, stream=None) -> None:
-    """Forward with the rotary embedding of q and k (tables fp32 [T, D/2]) fused into the load stage."""
+def nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, qr, kr, o, lse, window: int, scale: float, stream=None) -> None:
+    """Attention over the rotary-embedded q and k (tables fp32 [T, D/2]); the turned q, k go to qr, kr."""
     B, T, H, D = q.shape
-    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+    for n, t in (("q", q), ("k", k), ("v", v), ("qr", qr), ("kr", kr), ("o", o)):
         _need(t, n, torch.bfloat16, (B, T, H, D))
     _need(lse, "lse", torch.float32, (B, H, T))
     _rope_tables(rope_cos, rope_sin, T, D)
-    _check(lib.nc_attn_fwd_rotary(_ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(o), _ptr(lse),
-                                  B, T, H, D, int(window), float(scale), _stream(q.device, stream)),
-           "nc_attn_fwd_rotary")
+    _check(lib.nc_attn_fwd_rotary(_ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(qr), _ptr(kr),
+                                  _ptr(o), _ptr(lse), B, T, H, D, int(window), float(scale),
+                                  _stream(q.device, stream)), "nc_attn_fwd_rotary")
 
 
-def nc_attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace,
+def nc_attn_bwd_rotary(qr, kr, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window: int, scale: float, workspace,
                        stream=None) -> None:
-    """Backward of nc_attn_fwd_rotary: dq, dk with respect to the unrotated q, k."""
-    B, T, H, D = q.shape
-    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
+    """Backward of nc_attn_fwd_rotary from the turned rows qr, kr: dq, dk with respect to the unturned q, k."""
+    B, T, H, D = qr.shape
+    for n, t in (("qr", qr), ("kr", kr), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
         _need(t, n, torch.bfloat16, (B, T, H, D))
     _need(lse, "lse", torch.float32, (B, H, T))
     _rope_tables(rope_cos, rope_sin, T, D)
     _need(workspace, "workspace", torch.uint8)
-    _check(lib.nc_attn_bwd_rotary(_ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(o), _ptr(dO),
+    _check(lib.nc_attn_bwd_rotary(_ptr(qr), _ptr(kr), _ptr(v), _ptr(rope_cos), _ptr(rope_sin), _ptr(o), _ptr(dO),
                                   _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, T, H, D, int(window), float(scale),
-                                  _ptr(workspace), workspace.numel(), _stream(q.device, stream)),
+                                  _ptr(workspace), workspace.numel(), _stream(qr.device, stream)),
            "nc_attn_bwd_rotary")
 
 
@@ -223,24 +223,25 @@ def rotary(x, rope_cos, rope_sin, inverse: bool = False, stream=None):
 
 
 def attn_fwd_rotary(q, k, v, rope_cos, rope_sin, window: int, scale: float | None = None, stream=None):
-    """Returns (o, lse) of attention over the rotary-embedded q and k."""
+    """Returns (o, lse, qr, kr): attention over the rotary-embedded q and k, and the turned q, k (which
+    attn_bwd_rotary takes)."""
     B, T, H, D = q.shape
     scale = default_scale(D) if scale is None else scale
-    o = torch.empty_like(q)
+    qr, kr, o = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, o, lse, window, scale, stream)
-    return o, lse
+    nc_attn_fwd_rotary(q, k, v, rope_cos, rope_sin, qr, kr, o, lse, window, scale, stream)
+    return o, lse, qr, kr
 
 
-def attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, window: int, scale: float | None = None,
+def attn_bwd_rotary(qr, kr, v, rope_cos, rope_sin, o, dO, lse, window: int, scale: float | None = None,
                     workspace=None, stream=None):
-    """Returns (dq, dk, dv) of the rotary forward, dq and dk with respect to the unrotated q and k."""
-    B, T, H, D = q.shape
+    """Returns (dq, dk, dv) of the rotary forward, dq and dk with respect to the unturned q and k."""
+    B, T, H, D = qr.shape
     scale = default_scale(D) if scale is None else scale
     if workspace is None:
-        workspace = torch.empty(nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    nc_attn_bwd_rotary(q, k, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
+        workspace = torch.empty(nc_attn_bwd_workspace_bytes(B, T, H, D), dtype=torch.uint8, device=qr.device)
+    dq, dk, dv = torch.empty_like(qr), torch.empty_like(qr), torch.empty_like(qr)
+    nc_attn_bwd_rotary(qr, kr, v, rope_cos, rope_sin, o, dO, lse, dq, dk, dv, window, scale, workspace, stream)
     return dq, dk, dv
 
 

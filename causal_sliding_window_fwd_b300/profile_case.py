@@ -68,15 +68,15 @@ def main():
         scale = 1.0 / math.sqrt(a.D)
         q, k, v, dO = workloads.make_qkvdo_shape(a.B, a.T, a.H, a.D, a.seed, dev)
         c, s = workloads.rope_tables(a.T, a.D, device=dev)
-        o, lse = nc_attn.attn_fwd_rotary(q, k, v, c, s, a.window, scale)
+        o, lse, qr, kr = nc_attn.attn_fwd_rotary(q, k, v, c, s, a.window, scale)
         if a.op == "rope_fwd":
             for _ in range(a.iters):
-                nc_attn.nc_attn_fwd_rotary(q, k, v, c, s, o, lse, a.window, scale)
+                nc_attn.nc_attn_fwd_rotary(q, k, v, c, s, qr, kr, o, lse, a.window, scale)
         else:
             ws = torch.empty(nc_attn.nc_attn_bwd_workspace_bytes(a.B, a.T, a.H, a.D), dtype=torch.uint8, device=dev)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
             for _ in range(a.iters):
-                nc_attn.nc_attn_bwd_rotary(q, k, v, c, s, o, dO, lse, dq, dk, dv, a.window, scale, ws)
+                nc_attn.nc_attn_bwd_rotary(qr, kr, v, c, s, o, dO, lse, dq, dk, dv, a.window, scale, ws)
     else:
         scale = 1.0 / math.sqrt(a.D)
         q, k, v, dO = workloads.make_qkvdo_shape(a.B, a.T, a.H, a.D, a.seed, dev)

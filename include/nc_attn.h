@@ -210,41 +210,45 @@ nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache,
                           cudaStream_t stream);
 
 /*
- * Forward with the rotary position embedding of q and k fused into the load
- * stage ("nanochat" walkthrough, page 4, comment thread: the model is
- * Llama-like; the pages give no formula, and the rotate-half pairing of Llama
- * is the reading taken).  Each query and key row of position t (0 .. T-1) has
- * every pair (x_i, x_{i+D/2}), i < D/2, turned by the angle whose cosine and
- * sine the tables hold at (t, i):
+ * Attention over rotary-embedded q and k ("nanochat" walkthrough, page 4,
+ * comment thread: the model is Llama-like; the pages give no formula, and the
+ * rotate-half pairing of Llama is the reading taken).  Each query and key row
+ * of position t (0 .. T-1) has every pair (x_i, x_{i+D/2}), i < D/2, turned by
+ * the angle whose cosine and sine the tables hold at (t, i):
  *   x_i' = x_i c - x_{i+D/2} s,   x_{i+D/2}' = x_i s + x_{i+D/2} c,
- * and o, lse are those of nc_attn_fwd on the turned q and k (v unchanged).
- * The turn is applied to the tiles in shared memory between their arrival and
- * the first tensor-core product; the rotated q and k never go to memory.
+ * evaluated in float32 (one product and one fused multiply-add per output)
+ * and rounded to bf16.  One launch writes the turned q and k to qr and kr,
+ * which the backward takes; then o, lse are those of nc_attn_fwd on (qr, kr,
+ * v).  Two launches.
  *   rope_cos, rope_sin : const fp32 [T, D/2] device, 16-byte aligned (row t,
  *                        column i; e.g. cos / sin of t * base^(-2i/D))
- * Other arguments, layouts and errors as nc_attn_fwd.
+ *   qr, kr             : bf16 [B, T, H, D] device, written (the turned q, k)
+ * Other arguments, layouts and errors as nc_attn_fwd; no output may overlap
+ * an input or another output.
  */
 nc_status nc_attn_fwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos,
-                             const float* rope_sin, void* o, float* lse, int B, int T, int H, int D,
-                             int window, float scale, cudaStream_t stream);
+                             const float* rope_sin, void* qr, void* kr, void* o, float* lse, int B, int T,
+                             int H, int D, int window, float scale, cudaStream_t stream);
 
 /*
- * Backward of nc_attn_fwd_rotary: dq and dk are the gradients with respect to
- * the unrotated q and k (the gradients with respect to the turned rows, turned
- * back by the transpose), dv as nc_attn_bwd.  o and lse are those that
- * nc_attn_fwd_rotary produced with the same arguments; the workspace is sized
- * by nc_attn_bwd_workspace_bytes.  Other arguments, layouts and errors as
- * nc_attn_bwd.
+ * Backward of nc_attn_fwd_rotary.  Takes the turned rows qr, kr that
+ * nc_attn_fwd_rotary wrote (not q and k) and the same tables; dq and dk are
+ * the gradients with respect to the unturned q and k: the gradients with
+ * respect to the turned rows, turned back by the transpose of each row's
+ * rotation (dK in the main kernel's epilogue, dQ in the pass that converts
+ * its fp32 accumulator), so the backward costs what nc_attn_bwd costs.  dv as
+ * nc_attn_bwd.  The workspace is sized by nc_attn_bwd_workspace_bytes.  Other
+ * arguments, layouts and errors as nc_attn_bwd.
  */
-nc_status nc_attn_bwd_rotary(const void* q, const void* k, const void* v, const float* rope_cos,
+nc_status nc_attn_bwd_rotary(const void* qr, const void* kr, const void* v, const float* rope_cos,
                              const float* rope_sin, const void* o, const void* dO, const float* lse,
                              void* dq, void* dk, void* dv, int B, int T, int H, int D, int window,
                              float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * The rotary turn on its own (the unfused form of what nc_attn_fwd_rotary does
- * in shared memory): y = the turn of x, row t of each sequence by the tables'
- * row t, as nc_attn_fwd_rotary defines it; with inverse != 0 the transpose
+ * The rotary turn on its own: y = the turn of x, row t of each sequence by
+ * the tables' row t, as nc_attn_fwd_rotary defines it (for example to turn new
+ * tokens' keys before they enter a KV cache); with inverse != 0 the transpose
  * (the turn back, which maps gradients with respect to the turned tensor to
  * gradients with respect to x).  For positions that do not start at 0 pass
  * tables offset to the first position.

@@ -295,7 +295,7 @@ def test_abi_calls_from_many_threads(lib):
 
 def _fwd_rot(lib, ptrs=None, **kw):
     a = dict(GOOD, **kw)
-    p = list(A[:7]) if ptrs is None else ptrs
+    p = list(A[:9]) if ptrs is None else ptrs
     return lib.lib.nc_attn_fwd_rotary(*[ctypes.c_void_p(x) for x in p], a["B"], a["T"], a["H"], a["D"],
                                       a["window"], ctypes.c_float(a["scale"]), None)
 
@@ -308,19 +308,23 @@ def _rot(lib, ptrs=None, inverse=0, **kw):
 
 @host_only
 def test_rotary_entries_reject_bad_arguments(lib):
-    # forward: q k v cos sin o lse
+    # forward: q k v cos sin qr kr o lse
     assert _fwd_rot(lib, D=96) == lib.NC_ERR_UNSUPPORTED
     assert _fwd_rot(lib, window=0) == lib.NC_ERR_INVALID
-    for i in range(7):
-        p = list(A[:7]); p[i] = 0
+    for i in range(9):
+        p = list(A[:9]); p[i] = 0
         assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
-        p = list(A[:7]); p[i] += 8
+        p = list(A[:9]); p[i] += 8
         assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
-    p = list(A[:7]); p[5] = p[3] + 256       # o over the cosine table
+    p = list(A[:9]); p[7] = p[3] + 256       # o over the cosine table
     assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
-    p = list(A[:7]); p[6] = p[4]             # lse over the sine table
+    p = list(A[:9]); p[8] = p[4]             # lse over the sine table
     assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
-    # backward: q k v cos sin o dO lse dq dk dv, workspace
+    p = list(A[:9]); p[5] = p[0]             # qr over q (the turn is not in place here)
+    assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:9]); p[6] = p[5] + 64        # kr overlapping qr
+    assert _fwd_rot(lib, p) == lib.NC_ERR_INVALID
+    # backward: qr kr v cos sin o dO lse dq dk dv, workspace
     need = lib.nc_attn_bwd_workspace_bytes(2, 64, 2, 64)
 
     def bwd_rot(p, ws=A[11], ws_bytes=need, **kw):

@@ -42,12 +42,12 @@ def abs_err(got, ref):
 
 def run(nc, q, k, v, dO, c, s, window, scale):
     B, T, H, D = q.shape
-    o = torch.full_like(q, float("nan"))
+    o, qr, kr = (torch.full_like(q, float("nan")) for _ in range(3))
     lse = torch.full((B, H, T), float("nan"), dtype=torch.float32, device=q.device)
-    nc.nc_attn_fwd_rotary(q, k, v, c, s, o, lse, window, scale)
+    nc.nc_attn_fwd_rotary(q, k, v, c, s, qr, kr, o, lse, window, scale)
     ws = torch.full((nc.nc_attn_bwd_workspace_bytes(B, T, H, D),), 0xFF, dtype=torch.uint8, device=q.device)
     dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
-    nc.nc_attn_bwd_rotary(q, k, v, c, s, o, dO, lse, dq, dk, dv, window, scale, ws)
+    nc.nc_attn_bwd_rotary(qr, kr, v, c, s, o, dO, lse, dq, dk, dv, window, scale, ws)
     assert nc.nc_get_device_error() == 0
     return o, lse, dq, dk, dv
 
@@ -77,8 +77,8 @@ def test_rotary_matches_oracle(nc, oracle_mod, B, T, H, D, window):
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_identity_tables_give_the_plain_kernels(nc, D):
-    """cos = 1, sin = 0 turns nothing: every output equals the plain forward / backward (dq up to the
-    order in which its fp32 partials are added)."""
+    """cos = 1, sin = 0 turns nothing: the turned rows are the inputs and every output equals the plain
+    forward / backward (dq up to the order in which its fp32 partials are added)."""
     B, T, H, W = 2, 333, 3, 100
     q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4100 + D, device="cuda")
     c = torch.ones((T, D // 2), dtype=torch.float32, device="cuda")
@@ -136,12 +136,14 @@ def test_standalone_turn_matches_oracle(nc, oracle_mod, D, inverse):
     assert nc.nc_get_device_error() == 0
 
 
-def test_unfused_composition_equals_fused(nc):
-    """Turning q and k first and running the plain kernels gives the fused forward's o and lse bit for bit
-    (the fused kernels turn the same bf16 values with the same fp32 arithmetic before the products)."""
+def test_turned_rows_and_the_standalone_turn_agree(nc, oracle_mod):
+    """The turned q and k that the rotary forward writes are the standalone turn's, and they are the
+    oracle's float32 turn rounded to bf16, bit for bit."""
     B, T, H, D, W = 2, 500, 3, 128, 200
     q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4300, device="cuda")
     c, s = workloads.rope_tables(T, D, device="cuda")
-    o, lse = nc.attn_fwd_rotary(q, k, v, c, s, W, 0.1)
-    o2, lse2 = nc.attn_fwd(nc.rotary(q, c, s), nc.rotary(k, c, s), v, W, 0.1)
+    o, lse, qr, kr = nc.attn_fwd_rotary(q, k, v, c, s, W, 0.1)
+    assert torch.equal(qr, nc.rotary(q, c, s)) and torch.equal(kr, nc.rotary(k, c, s))
+    np.testing.assert_array_equal(qr.double().cpu().numpy(), oracle_mod.rotary_bf16(q.cpu(), c.cpu(), s.cpu()))
+    o2, lse2 = nc.attn_fwd(qr, kr, v, W, 0.1)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
