@@ -31,6 +31,10 @@ constexpr int kDecodeMaxThreads = 320;
 constexpr int kBalancedMaxSeqs = 1024;
 constexpr int kMinRowsPerCta = 16;
 constexpr int kCombineFast = 8;
+// Bulk-copy split: a ring of kBulkStages stages of kBulkHalfStage bytes of K and as many of V, heads <= 16.
+constexpr int kBulkStages = 4;
+constexpr int kBulkHalfStage = 24 * 1024;
+constexpr int kBulkMaxHeads = 16;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -64,82 +68,74 @@ __device__ __forceinline__ float fast_ex2(float x) {
     return y;
 }
 
-// Online softmax of one head's query over cache rows [t_begin, t_end) of sequence n, by one warp:
-// lanes are grouped G = D / 8 per token row, a warp covers TPS = 32 / G tokens per step and keeps U
-// steps of K and V loads in flight before it does any arithmetic on them.  The partial (running max
-// in log2 units, sum, unnormalised output) goes to part_ml[pidx], part_o[pidx].
+// Lane layout of one warp streaming one head: lanes are grouped G = D / 8 per token row (each lane holds 8
+// columns), and a step covers TPS = 32 / G tokens.
 template <int D>
-__device__ __forceinline__ void decode_rows(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
-                                            const __nv_bfloat16* __restrict__ vc, int n, int h, int H, int Tmax,
-                                            int t_begin, int t_end, float scale_log2, size_t pidx,
-                                            float* __restrict__ part_ml, float* __restrict__ part_o) {
-    constexpr int G = D / 8;          // lanes per token row of one head
-    constexpr int TPS = 32 / G;       // tokens per warp step
-    constexpr int U = 4;              // steps in flight per iteration
-    const int lane = threadIdx.x & 31;
-    const int g = lane / G;           // token slot within a step
-    const int c = lane % G;           // 8-element column group
-    const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
-    float qf[8];
+struct RowLanes {
+    static constexpr int G = D / 8;
+    static constexpr int TPS = 32 / G;
+};
+
+// The query row of (n, h) as this lane's 8 columns, scaled into log2 units.
+template <int D>
+__device__ __forceinline__ void load_query(const __nv_bfloat16* __restrict__ q, int n, int h, int H, float (&qf)[8]) {
+    const int c = (threadIdx.x & 31) % RowLanes<D>::G;
     bf16x8_to_f32(reinterpret_cast<const uint4*>(q + ((size_t)n * H + h) * D)[c], qf);
+}
+
+// U steps of the online softmax: kr[u], vr[u] are this lane's 8 columns of the key / value of token slot u,
+// `valid` says whether the slot holds a visible token.  Updates the lane's running max m (log2 units), sum l
+// and unnormalised output acc.
+template <int D, int U>
+__device__ __forceinline__ void softmax_steps(const uint4 (&kr)[U], const uint4 (&vr)[U], const bool (&valid)[U],
+                                              const float (&qf)[8], float& m, float& l, float (&acc)[8]) {
+    constexpr int G = RowLanes<D>::G;
+    // scores of the U tokens (log2 units), reduced across the G lanes of a token
+    float sc[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
-    float m = -INFINITY, l = 0.f, acc[8];
+    for (int u = 0; u < U; ++u) {
+        float kf[8];
+        bf16x8_to_f32(kr[u], kf);
+        float dot = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-    const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
-    for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
-        uint4 kr[U], vr[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = t0 + u * TPS + g;
-            kr[u] = make_uint4(0, 0, 0, 0);
-            vr[u] = make_uint4(0, 0, 0, 0);
-            if (t < t_end) {
-                kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
-                vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
-            }
-        }
-        // scores of the U tokens of this slot (log2 units), reduced across the G lanes
-        float sc[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            float kf[8];
-            bf16x8_to_f32(kr[u], kf);
-            float dot = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
-            sc[u] = dot;
-        }
-#pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1)
-#pragma unroll
-            for (int u = 0; u < U; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
-        float mc = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (t0 + u * TPS + g >= t_end) sc[u] = -INFINITY;
-            mc = fmaxf(mc, sc[u]);
-        }
-        const float m_new = fmaxf(m, mc);
-        if (m_new == -INFINITY) continue;  // every token of this slot lies past the end
-        const float alpha = fast_ex2(m - m_new);
-        l *= alpha;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= alpha;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const float p = fast_ex2(sc[u] - m_new);
-            float vf[8];
-            bf16x8_to_f32(vr[u], vf);
-            l += p;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
-        }
-        m = m_new;
+        for (int i = 0; i < 8; ++i) dot = fmaf(qf[i], kf[i], dot);
+        sc[u] = dot;
     }
-    // merge the TPS token slots of this warp (lanes with equal c)
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < U; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+    float mc = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!valid[u]) sc[u] = -INFINITY;
+        mc = fmaxf(mc, sc[u]);
+    }
+    const float m_new = fmaxf(m, mc);
+    if (m_new == -INFINITY) return;  // no visible token in this lane's slots yet
+    const float alpha = fast_ex2(m - m_new);
+    l *= alpha;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= alpha;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float p = fast_ex2(sc[u] - m_new);
+        float vf[8];
+        bf16x8_to_f32(vr[u], vf);
+        l += p;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
+    }
+    m = m_new;
+}
+
+// Merge the TPS token slots of the warp (lanes with equal column group) and write the partial (running max
+// in log2 units, sum, unnormalised output) to part_ml[pidx], part_o[pidx].
+template <int D>
+__device__ __forceinline__ void merge_and_store(float m, float l, float (&acc)[8], size_t pidx,
+                                                float* __restrict__ part_ml, float* __restrict__ part_o) {
+    constexpr int G = RowLanes<D>::G;
+    const int lane = threadIdx.x & 31, c = lane % G;
 #pragma unroll
     for (int off = G; off < 32; off <<= 1) {
         const float m_o = __shfl_xor_sync(0xffffffffu, m, off);
@@ -164,6 +160,47 @@ __device__ __forceinline__ void decode_rows(const __nv_bfloat16* __restrict__ q,
         part_ml[pidx * 2 + 0] = m;
         part_ml[pidx * 2 + 1] = l;
     }
+}
+
+// Online softmax of one head's query over cache rows [t_begin, t_end) of sequence n, by one warp reading
+// global memory: U steps of K and V loads are in flight before any arithmetic on them.
+template <int D>
+__device__ __forceinline__ void decode_rows(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                                            const __nv_bfloat16* __restrict__ vc, int n, int h, int H, int Tmax,
+                                            int t_begin, int t_end, float scale_log2, size_t pidx,
+                                            float* __restrict__ part_ml, float* __restrict__ part_o) {
+    constexpr int G = RowLanes<D>::G, TPS = RowLanes<D>::TPS;
+    constexpr int U = 4;              // steps in flight per iteration
+    const int lane = threadIdx.x & 31;
+    const int g = lane / G;           // token slot within a step
+    const int c = lane % G;           // 8-element column group
+    const size_t row_stride = (size_t)H * D;  // elements between consecutive tokens
+    float qf[8];
+    load_query<D>(q, n, h, H, qf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+    float m = -INFINITY, l = 0.f, acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    const __nv_bfloat16* kbase = kc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+    const __nv_bfloat16* vbase = vc + (size_t)n * Tmax * row_stride + (size_t)h * D + c * 8;
+    for (int t0 = t_begin; t0 < t_end; t0 += TPS * U) {
+        uint4 kr[U], vr[U];
+        bool valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * TPS + g;
+            valid[u] = t < t_end;
+            kr[u] = make_uint4(0, 0, 0, 0);
+            vr[u] = make_uint4(0, 0, 0, 0);
+            if (valid[u]) {
+                kr[u] = ldg_stream(reinterpret_cast<const uint4*>(kbase + (size_t)t * row_stride));
+                vr[u] = ldg_stream(reinterpret_cast<const uint4*>(vbase + (size_t)t * row_stride));
+            }
+        }
+        softmax_steps<D, U>(kr, vr, valid, qf, m, l, acc);
+    }
+    merge_and_store<D>(m, l, acc, pidx, part_ml, part_o);
 }
 
 // Chunked split (many sequences): one CTA per (split s, sequence n) work item; item = s + n_splits * n.
@@ -199,15 +236,16 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 // of bytes and the grid ends together (no partial last wave).  CTA c's piece of sequence n writes its
 // partial to slot n + c: slots increase with (c, n), so they are distinct and below N + gridDim.x.
 // Every CTA computes the prefix sums itself; CTA 0 also stores them (and `per`) in meta for the combine.
-template <int D>
-__global__ void __launch_bounds__(kDecodeMaxThreads, 2)
-decode_balanced_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
-                       const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
-                       float* __restrict__ part_ml, float* __restrict__ part_o, int* __restrict__ meta, int N,
-                       int Tmax, int H, int window, float scale_log2) {
-    __shared__ int s_vis[kBalancedMaxSeqs];
-    __shared__ int s_pre[kBalancedMaxSeqs + 1];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+struct BalancedRange {
+    int per, r0, r1;  // rows per CTA and this CTA's range [r0, r1) of the laid-out rows
+    int first_seq;    // the first sequence whose rows reach past r0 (valid when r0 < r1)
+};
+
+// V_n in s_vis, P_n in s_pre (s_pre[N] = the total), this CTA's range; CTA 0 writes meta.  Called by every
+// thread of the CTA (it synchronises the CTA).
+__device__ __forceinline__ BalancedRange balanced_range(const int* __restrict__ lens, int* __restrict__ meta, int N,
+                                                        int Tmax, int window, int* s_vis, int* s_pre) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int n = tid; n < N; n += blockDim.x) {
         const int L = lens[n];
         s_vis[n] = (L < 1 || L > Tmax) ? 0 : L - visible_lo(L, window);  // bad lengths: no rows
@@ -233,30 +271,173 @@ decode_balanced_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16*
         if (lane == 31) s_pre[N] = incl;
     }
     __syncthreads();
+    BalancedRange r;
     const int R = s_pre[N];
-    const int per = max((R + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), kMinRowsPerCta);
+    r.per = max((R + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x), kMinRowsPerCta);
     if (blockIdx.x == 0) {
         for (int n = tid; n <= N; n += blockDim.x) meta[n] = s_pre[n];
-        if (tid == 0) meta[N + 1] = per;
+        if (tid == 0) meta[N + 1] = r.per;
     }
-    const int r0 = static_cast<int>(blockIdx.x) * per;
-    const int r1 = min(R, r0 + per);
-    if (r0 < r1) {
-        // first sequence whose rows reach past r0
-        int lo = 0, hi = N - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (s_pre[mid + 1] > r0) hi = mid;
-            else lo = mid + 1;
-        }
-        for (int n = lo; n < N && s_pre[n] < r1; ++n) {
-            const int P = s_pre[n], V = s_vis[n];
-            if (V == 0) continue;
-            const int first = visible_lo(lens[n], window);
-            const int t_begin = first + max(r0, P) - P, t_end = first + min(r1, P + V) - P;
+    r.r0 = static_cast<int>(blockIdx.x) * r.per;
+    r.r1 = min(R, r.r0 + r.per);
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pre[mid + 1] > r.r0) hi = mid;
+        else lo = mid + 1;
+    }
+    r.first_seq = lo;
+    return r;
+}
+
+// Sequence n's piece of a CTA's range: cache rows [t_begin, t_end).  False for a sequence without rows.
+__device__ __forceinline__ bool balanced_piece(const BalancedRange& r, const int* __restrict__ lens, int window,
+                                               const int* s_vis, const int* s_pre, int n, int& t_begin, int& t_end) {
+    const int P = s_pre[n], V = s_vis[n];
+    if (V == 0) return false;
+    const int first = visible_lo(lens[n], window);
+    t_begin = first + max(r.r0, P) - P;
+    t_end = first + min(r.r1, P + V) - P;
+    return true;
+}
+
+// Balanced split with plain loads: warps over heads, each streaming its head's slice of the rows.
+template <int D>
+__global__ void __launch_bounds__(kDecodeMaxThreads, 2)
+decode_balanced_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                       const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens,
+                       float* __restrict__ part_ml, float* __restrict__ part_o, int* __restrict__ meta, int N,
+                       int Tmax, int H, int window, float scale_log2) {
+    __shared__ int s_vis[kBalancedMaxSeqs];
+    __shared__ int s_pre[kBalancedMaxSeqs + 1];
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const BalancedRange r = balanced_range(lens, meta, N, Tmax, window, s_vis, s_pre);
+    if (r.r0 < r.r1) {
+        for (int n = r.first_seq; n < N && s_pre[n] < r.r1; ++n) {
+            int t_begin, t_end;
+            if (!balanced_piece(r, lens, window, s_vis, s_pre, n, t_begin, t_end)) continue;
             const size_t slot = (size_t)n + blockIdx.x;
             for (int h = warp; h < H; h += nwarps)
                 decode_rows<D>(q, kc, vc, n, h, H, Tmax, t_begin, t_end, scale_log2, slot * H + h, part_ml, part_o);
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Balanced split with bulk copies (up to kBulkMaxHeads heads): the same ranges, but one producer thread
+// streams whole cache rows (all heads, contiguous in memory) into a ring of shared-memory stages with 1-D
+// bulk copies (`cp.async.bulk`, completion counted on the stage's mbarrier), so up to kBulkStages x 2 x
+// kBulkHalfStage bytes per SM are in flight without holding registers.  Consumer warp h runs the online
+// softmax of head h over each stage from shared memory and releases it.  One CTA per SM.
+struct BulkSmem {
+    uint8_t stage[kBulkStages][2][kBulkHalfStage];  // [stage][K, V][rows x H x D bf16]
+    uint64_t full[kBulkStages];
+    uint64_t empty[kBulkStages];
+    int s_vis[kBalancedMaxSeqs];
+    int s_pre[kBalancedMaxSeqs + 1];
+};
+
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * (kBulkMaxHeads + 1), 1)
+decode_bulk_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+                   const __nv_bfloat16* __restrict__ vc, const int* __restrict__ lens, float* __restrict__ part_ml,
+                   float* __restrict__ part_o, int* __restrict__ meta, int N, int Tmax, int H, int window,
+                   float scale_log2, int chunk_rows, int* err) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    BulkSmem& sm = *reinterpret_cast<BulkSmem*>(smem_raw);
+    constexpr int G = RowLanes<D>::G, TPS = RowLanes<D>::TPS;
+    constexpr int U = 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kBulkStages; ++st) {
+            mbar_init(&sm.full[st], 1);
+            mbar_init(&sm.empty[st], H);  // one arrival per consumer warp
+        }
+        fence_barrier_init();
+    }
+    const BalancedRange r = balanced_range(lens, meta, N, Tmax, window, sm.s_vis, sm.s_pre);  // syncs the CTA
+    const size_t row_elems = (size_t)H * D;
+    const uint32_t row_bytes = static_cast<uint32_t>(row_elems * 2);
+    if (r.r0 < r.r1) {
+        if (warp == H) {
+            // ---------------------------------------------------------------- producer (one thread)
+            if (lane == 0) {
+                int ci = 0;  // chunks issued
+                bool ok = true;
+                for (int n = r.first_seq; ok && n < N && sm.s_pre[n] < r.r1; ++n) {
+                    int tb, te;
+                    if (!balanced_piece(r, lens, window, sm.s_vis, sm.s_pre, n, tb, te)) continue;
+                    for (int t = tb; t < te; t += chunk_rows, ++ci) {
+                        const int st = ci % kBulkStages;
+                        if (!mbar_wait(&sm.empty[st], ((ci / kBulkStages) & 1) ^ 1)) {
+                            set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bytes = static_cast<uint32_t>(min(chunk_rows, te - t)) * row_bytes;
+                        const size_t off = ((size_t)n * Tmax + t) * row_elems;
+                        mbar_arrive_expect_tx(&sm.full[st], 2 * bytes);
+                        bulk_load_1d(sm.stage[st][0], kc + off, bytes, &sm.full[st]);
+                        bulk_load_1d(sm.stage[st][1], vc + off, bytes, &sm.full[st]);
+                    }
+                }
+                // never leave while a copy into this CTA's shared memory may still land
+                for (int x = ci - kBulkStages < 0 ? 0 : ci - kBulkStages; x < ci; ++x)
+                    mbar_wait(&sm.full[x % kBulkStages], (x / kBulkStages) & 1);
+            }
+        } else if (warp < H) {
+            // ---------------------------------------------------------------- consumer: head h = warp
+            const int h = warp, g = lane / G, c = lane % G;
+            int ci = 0;  // chunks consumed
+            bool ok = true;
+            for (int n = r.first_seq; ok && n < N && sm.s_pre[n] < r.r1; ++n) {
+                int tb, te;
+                if (!balanced_piece(r, lens, window, sm.s_vis, sm.s_pre, n, tb, te)) continue;
+                float qf[8];
+                load_query<D>(q, n, h, H, qf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) qf[i] *= scale_log2;
+                float m = -INFINITY, l = 0.f, acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                for (int t = tb; t < te; t += chunk_rows, ++ci) {
+                    const int st = ci % kBulkStages;
+                    if (!mbar_wait_warp(&sm.full[st], (ci / kBulkStages) & 1)) {
+                        if (lane == 0) set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const int rows = min(chunk_rows, te - t);
+                    const uint8_t* kst = sm.stage[st][0] + (size_t)h * D * 2 + c * 16;
+                    const uint8_t* vst = sm.stage[st][1] + (size_t)h * D * 2 + c * 16;
+                    for (int j0 = 0; j0 < rows; j0 += TPS * U) {
+                        uint4 kr[U], vr[U];
+                        bool valid[U];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int j = j0 + u * TPS + g;
+                            valid[u] = j < rows;
+                            kr[u] = make_uint4(0, 0, 0, 0);
+                            vr[u] = make_uint4(0, 0, 0, 0);
+                            if (valid[u]) {
+                                kr[u] = *reinterpret_cast<const uint4*>(kst + (size_t)j * row_bytes);
+                                vr[u] = *reinterpret_cast<const uint4*>(vst + (size_t)j * row_bytes);
+                            }
+                        }
+                        softmax_steps<D, U>(kr, vr, valid, qf, m, l, acc);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.empty[st]);
+                }
+                if (!ok) break;
+                merge_and_store<D>(m, l, acc, ((size_t)n + blockIdx.x) * H + h, part_ml, part_o);
+            }
         }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -493,7 +674,28 @@ cudaError_t launch_decode(const void* q, const void* kcache, const void* vcache,
     auto bk = static_cast<const __nv_bfloat16*>(kcache);
     auto bv = static_cast<const __nv_bfloat16*>(vcache);
     auto bo = static_cast<__nv_bfloat16*>(o);
-    if (decode_balanced(N, Tmax)) {
+    if (decode_balanced(N, Tmax) && H <= kBulkMaxHeads) {
+        // one CTA per SM (its stage ring takes most of the shared memory), H consumer warps + a producer warp
+        auto split = D == 128 ? decode_bulk_kernel<128> : decode_bulk_kernel<64>;
+        static std::atomic<bool> attr_done[2][kAttrDevices];
+        const int smem = static_cast<int>(sizeof(BulkSmem));
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(split), smem, attr_done[D == 128 ? 1 : 0]);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = multiprocessor_count(&sms);
+        if (e != cudaSuccess) return e;
+        const int grid = sms < kDecodeMaxGrid ? sms : kDecodeMaxGrid;
+        const int fit = kBulkHalfStage / (H * D * 2), batch = D == 128 ? 8 : 16;  // rows of one U-step batch
+        const int chunk_rows = fit >= batch ? fit / batch * batch : fit;
+        split<<<grid, 32 * (H + 1), smem, stream>>>(bq, bk, bv, lens, part_ml, part_o, meta, N, Tmax, H, window,
+                                                     scale_log2, chunk_rows, err);
+        if (D == 128)
+            launch_combine(decode_balanced_combine_kernel<128>, cblocks, stream, (const float*)part_ml,
+                           (const float*)part_o, (const int*)meta, lens, bo, lse, N, Tmax, H, err);
+        else
+            launch_combine(decode_balanced_combine_kernel<64>, cblocks, stream, (const float*)part_ml,
+                           (const float*)part_o, (const int*)meta, lens, bo, lse, N, Tmax, H, err);
+    } else if (decode_balanced(N, Tmax)) {
         // as many CTAs as fit on the GPU at once (looked up per call), at most kDecodeMaxGrid
         auto split = D == 128 ? decode_balanced_kernel<128> : decode_balanced_kernel<64>;
         int sms = 0, per_sm = 0;

@@ -287,6 +287,21 @@ def test_decode_many_sequences_fixed_chunks(nc, oracle_mod, window):
     assert abs_err(lse, lse_ref) <= LSE_TOL
 
 
+@pytest.mark.parametrize("window", [100, -1])
+def test_decode_more_heads_than_the_bulk_path_takes(nc, oracle_mod, window):
+    """More than 16 heads: the balanced split streams with plain loads (warps over heads) instead of the
+    bulk-copy stage ring."""
+    wl = workloads.DecodeWorkload("heads", 5, 700, 20, 64, 1, 700, (window,), 717)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda", poison_tail=True)
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
+                                           window, wl.scale)
+    assert ok
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
 def test_decode_equals_last_forward_row(nc):
     B, T, H, D, W = 2, 600, 2, 128, 256
     q, k, v, _ = workloads.make_qkvdo_shape(B, T, H, D, seed=31, device="cuda")
