@@ -114,11 +114,13 @@ struct FwdParams {
 enum FwdMode { kModePlain = 0, kModeCache = 1, kModeVarlen = 2 };
 
 // Key blocks [lo, hi] that intersect the window of some query of the tile whose first query sits at
-// position pos0; the last query of the sequence sits at position last.
-__device__ __forceinline__ void tile_blocks(int pos0, int last, int W, int& lo, int& hi) {
+// position pos0; the last query of the sequence sits at position last.  Key block kb holds the keys at
+// positions kb * kBN - kpad .. kb * kBN - kpad + kBN - 1 (kpad > 0 shifts the blocks so that their edges
+// line up with the query tiles' when the queries start at a position that is not a multiple of kBN).
+__device__ __forceinline__ void tile_blocks(int pos0, int last, int W, int kpad, int& lo, int& hi) {
     const int first_key = pos0 - W + 1;
-    lo = first_key <= 0 ? 0 : first_key / kBN;
-    hi = min(pos0 + kBM - 1, last) / kBN;
+    lo = ((first_key <= 0 ? 0 : first_key) + kpad) / kBN;
+    hi = (min(pos0 + kBM - 1, last) + kpad) / kBN;
 }
 
 __device__ __forceinline__ bool aborted(const FwdBarriers& bars) {
@@ -134,6 +136,9 @@ __device__ __forceinline__ void record_timeout(FwdBarriers& bars, int* err) {
 struct FwdItem {
     int b, h;
     int off;            // position of query row 0 among the keys (prefill); 0 otherwise
+    int kpad;           // key block kb starts at key position kb * kBN - kpad: (-off) mod kBN, so the key
+                        // blocks line up with the query tiles (prefill items whose window starts past
+                        // position 0); 0 otherwise
     int base;           // first packed row of the document (varlen); 0 otherwise
     int len;            // query rows of this sequence or document
     bool bad;           // the sequence's cache length (or the document's bounds) is out of range
@@ -177,10 +182,13 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
         it.empty = it.bad || it.r0[0] >= it.len;
         if (it.empty) it.len = 1;  // keeps the block arithmetic below in range; nothing is done
     }
+    // shifted blocks save the half-empty block at the window's far edge; an item whose window reaches back
+    // to position 0 keeps the unshifted blocks (a shift would only move the partial block to position 0)
+    it.kpad = (kMode == kModeCache && it.off + it.r0[0] - p.W + 1 > 0) ? (kBN - it.off % kBN) % kBN : 0;
     const int last = it.off + it.len - 1;
     it.active1 = it.r0[1] < it.len;
-    tile_blocks(it.off + it.r0[0], last, p.W, it.lo[0], it.hi[0]);
-    tile_blocks(it.off + it.r0[1], last, p.W, it.lo[1], it.hi[1]);
+    tile_blocks(it.off + it.r0[0], last, p.W, it.kpad, it.lo[0], it.hi[0]);
+    tile_blocks(it.off + it.r0[1], last, p.W, it.kpad, it.lo[1], it.hi[1]);
     if (!it.active1) {
         it.lo[1] = it.hi[0] + 1;
         it.hi[1] = it.hi[0];
@@ -338,7 +346,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint8_t* dst = smem + L::kKVOff + slot * L::kTileBytes;
                 mbar_arrive_expect_tx_w(&bars.kv_full[slot], L::kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, it.h, it.base + kb * kBN, it.b);
+                    // (a prefill block shifted by kpad may start before row 0: those rows read as zeros)
+                    tma_load_4d_w(dst + c * kBN * 128, tm, &bars.kv_full[slot], c * 64, it.h,
+                                  it.base + kb * kBN - it.kpad, it.b);
             }
         }
         if (!ok) record_timeout(bars, p.err);
@@ -430,7 +440,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     // the last block of a prefill item may hold cache rows at or past the sequence's
                     // length; their weights are 0, but 0 x NaN is NaN inside the product, so those
                     // value rows are zeroed in shared memory first (whatever the cache holds there)
-                    const int r0 = it.off + it.len - kb * kBN;  // first row past the last query position
+                    const int r0 = it.off + it.len - (kb * kBN - it.kpad);  // first row past the last query position
                     if (r0 < kBN) {
                         uint8_t* vt = smem + L::kKVOff + slot_v * L::kTileBytes;
                         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -515,6 +525,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int t_hi = t ? item.hi[1] : item.hi[0];
             const int pos = item.off + tr0 + row_in_tile;  // this row's position among the keys
             const int tpos0 = item.off + tr0;
+            const int key_lo = max(pos - p.W + 1, 0);  // this row's first visible key (none before position 0)
             const bool tile_on = (t == 0) || item.active1;
             float m_run = -INFINITY, l_run = 0.f;
             if (tile_on) {
@@ -523,8 +534,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!ok) break;
                     tc_fence_after();
                     // elementwise mask only on blocks that straddle the causal diagonal or the window edge
-                    const int k0 = kb * kBN;
-                    const bool masked = !((k0 + kBN - 1 <= tpos0) && (k0 >= tpos0 + kBM - p.W));
+                    const int k0 = kb * kBN - item.kpad;  // position of the block's first key
+                    // (a prefill block that starts before position 0 is masked too: those keys do not exist)
+                    const bool masked = !((k0 + kBN - 1 <= tpos0) && (k0 >= tpos0 + kBM - p.W) && k0 >= 0);
                     const bool first = kb == t_lo;
                     float sv[kBN];
                     {
@@ -542,7 +554,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < kBN; ++j) {
                             const int key = k0 + j;
-                            if (key > pos || pos - key >= p.W) sv[j] = -INFINITY;
+                            if (key > pos || key < key_lo) sv[j] = -INFINITY;
                         }
                     }
                     float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];

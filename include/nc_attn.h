@@ -199,11 +199,14 @@ nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
  *                that sequence's o and lse rows NaN
  *   o          : bf16 [N, Tq, H, D] device, written
  *   lse        : fp32 [N, H, Tq] device, written
- * The cache is read in 128-row blocks: rows from L up to the end of the
- * 128-row block that holds row L - 1 are loaded and masked out (their value
- * rows are zeroed on chip before use), so they may hold anything, NaN
- * included.  Rows beyond that block are never read.  Needs no workspace;
- * Tq <= Tmax.
+ * The cache is read in 128-row blocks; rows from L up to the end of the
+ * block that holds row L - 1 (fewer than 128) are loaded and masked out
+ * (their value rows are zeroed on chip before use), so they may hold
+ * anything, NaN included.  Rows beyond that block are never read.  Blocks
+ * start at multiples of 128 or, where the window does not reach back to row
+ * 0, at rows congruent to L - Tq modulo 128 (in line with the query tiles;
+ * none past L - 1 is then loaded when Tq is a multiple of 128).  Needs no
+ * workspace; Tq <= Tmax.
  */
 nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
                           void* o, float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale,
