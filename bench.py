@@ -45,9 +45,9 @@ METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor pe
 # (sha256 of the .cu file); otherwise the bench reports null.
 TRAFFIC = {
     "nc_attn_bwd": {"src": "causal_sliding_window_fwd_b300/csrc/bwd_sm103.cu",
-                    "sha256": "82ffd1d919772ba21bd100369fecee9b1ddf349a99f3dc7000b3ff4451a638a3",
-                    "bytes": {1024: 167795712 + 118093056 + 506067712 + 284666368 + 167781632 + 46675968,
-                              2048: 167796224 + 118525696 + 506013952 + 284948736 + 167776512 + 47624448}},
+                    "sha256": "c68e02afd975c8f64f805eebf7bb5a25b07870d5a58042fc85171a02dbc97551",
+                    "bytes": {1024: 167795968 + 118299648 + 506067712 + 284267520 + 167780608 + 47454464,
+                              2048: 167794944 + 118450432 + 506056448 + 285178624 + 167776000 + 47024384}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
                     "sha256": "5ee54cad6b1e648f194109827e3cfcf874b631b1a4998509fb1ba606b3ebb113",
                     "bytes": {1024: 609840640 + 61052160, 2048: 736825088 + 61344512}},

@@ -31,8 +31,10 @@ def test_scratch_limit_is_enforced_before_any_launch(nc):
     need = nc.nc_attn_decode_noalloc_scratch_bytes(1024, 256, 40, 128, -1)
     assert need > nc.NC_DECODE_NOALLOC_SCRATCH_BYTES
     fake = [ctypes.c_void_p(0x400000000 * (i + 1)) for i in range(6)]  # 16 GiB apart: no two ranges overlap
+    launches = nc.nc_launch_count()
     rc = nc.lib.nc_attn_decode_noalloc(*fake, 1024, 256, 40, 128, -1, ctypes.c_float(0.088), None)
     assert rc == nc.NC_ERR_WORKSPACE
+    assert nc.nc_launch_count() == launches  # refused before any launch
     # many sequences take fixed chunks: 2048 sequences, full window over 8192 rows needs far more
     assert nc.nc_attn_decode_noalloc_scratch_bytes(2048, 8192, 10, 128, -1) > nc.NC_DECODE_NOALLOC_SCRATCH_BYTES
     assert nc.nc_attn_decode_noalloc_scratch_bytes(64, 8192, 10, 128, 1024) <= nc.NC_DECODE_NOALLOC_SCRATCH_BYTES
