@@ -551,10 +551,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         }
                     }
                     if (masked) {
+                        // visible columns of this row: [lo, hi] within the block; one 32-bit mask per group
+                        const int lo = key_lo - k0, hi = pos - k0;
 #pragma unroll
-                        for (int j = 0; j < kBN; ++j) {
-                            const int key = k0 + j;
-                            if (key > pos || key < key_lo) sv[j] = -INFINITY;
+                        for (int g32 = 0; g32 < kBN / 32; ++g32) {
+                            const int a = min(max(lo - 32 * g32, 0), 32), e = min(max(hi - 32 * g32 + 1, 0), 32);
+                            const uint32_t upto = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+                            const uint32_t from = a >= 32 ? 0u : (0xffffffffu << a);
+                            const uint32_t vis = upto & from;
+#pragma unroll
+                            for (int x = 0; x < 32; ++x)
+                                if (!((vis >> x) & 1u)) sv[32 * g32 + x] = -INFINITY;
                         }
                     }
                     float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
