@@ -107,6 +107,11 @@ struct FwdParams {
     int* work;            // varlen: {next item, CTAs finished}, zero on entry and left zero on exit
     float scale_log2;
     int n_pairs;          // query-tile pairs per (b, h), or per (document, h): the longest document's
+    // Plain / prefill: items split0 .. n_items-1 are single query tiles, two per pair item split0 + (w -
+    // split0) / 2, so that a last round that would have kept fewer than half the CTAs busy runs half-length
+    // items on twice as many (split0 = n_items = pair items otherwise)
+    int split0;
+    int n_items;
     int* err;
 };
 
@@ -154,13 +159,18 @@ struct FwdItem {
 template <int kMode>
 __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     FwdItem it;
+    int tile_only = -1;  // a single-tile item: which tile of its pair
+    if (kMode != kModeVarlen && w >= p.split0) {
+        tile_only = (w - p.split0) & 1;
+        w = p.split0 + ((w - p.split0) >> 1);
+    }
     const int per_pair = kMode == kModeVarlen ? p.H * p.n_docs : p.B * p.H;
     const int bh = w % per_pair;
     const int pair = p.n_pairs - 1 - w / per_pair;
     it.h = bh % p.H;
     it.b = kMode == kModeVarlen ? 0 : bh / p.H;
-    it.r0[0] = pair * 2 * kBM;
-    it.r0[1] = pair * 2 * kBM + kBM;
+    it.r0[0] = pair * 2 * kBM + (tile_only > 0 ? kBM : 0);
+    it.r0[1] = it.r0[0] + kBM;
     it.off = 0;
     it.base = 0;
     it.len = p.Tq;
@@ -185,8 +195,9 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const FwdParams& p) {
     // shifted blocks save the half-empty block at the window's far edge; an item whose window reaches back
     // to position 0 keeps the unshifted blocks (a shift would only move the partial block to position 0)
     it.kpad = (kMode == kModeCache && it.off + it.r0[0] - p.W + 1 > 0) ? (kBN - it.off % kBN) % kBN : 0;
+    if (tile_only >= 0 && it.r0[0] >= it.len) it.empty = true;  // the pair's second tile lies past the end
     const int last = it.off + it.len - 1;
-    it.active1 = it.r0[1] < it.len;
+    it.active1 = tile_only < 0 && it.r0[1] < it.len;
     tile_blocks(it.off + it.r0[0], last, p.W, it.kpad, it.lo[0], it.hi[0]);
     tile_blocks(it.off + it.r0[1], last, p.W, it.kpad, it.lo[1], it.hi[1]);
     if (!it.active1) {
@@ -245,7 +256,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     float2* stats = reinterpret_cast<float2*>(smem + L::kStatsOff);
 
     const int warp = warp_id(), lane = lane_id();
-    const int n_items = p.n_pairs * p.H * (kMode == kModeVarlen ? p.n_docs : p.B);
+    const int n_items = kMode == kModeVarlen ? p.n_pairs * p.H * p.n_docs : p.n_items;
 
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
@@ -320,7 +331,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             const FwdItem it = fwd_item<kMode>(w, p);
             if (it.empty) {
-                if (it.bad && lane == 0) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
+                if (kMode == kModeVarlen && it.bad && lane == 0) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
                 continue;
             }
             // Q of this item once the previous item's S products have read theirs
@@ -770,7 +781,18 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, const int
     int n_sm = 0;
     e = multiprocessor_count(&n_sm);
     if (e != cudaSuccess) return e;
-    const long n_items = (long)p.n_pairs * H * (cu != nullptr ? n_docs : B);
+    const long n_pair_items = (long)p.n_pairs * H * (cu != nullptr ? n_docs : B);
+    long n_items = n_pair_items;
+    p.split0 = static_cast<int>(n_pair_items);
+    if (cu == nullptr) {
+        // a last round that would keep fewer than half the CTAs busy runs its pair items as single tiles
+        const long full = n_pair_items / n_sm, left = n_pair_items - full * n_sm;
+        if (full >= 1 && left > 0 && 2 * left <= n_sm) {
+            p.split0 = static_cast<int>(full * n_sm);
+            n_items = p.split0 + 2 * left;
+        }
+    }
+    p.n_items = static_cast<int>(n_items);
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     if (cu != nullptr) {
         static std::atomic<unsigned> work_seq{0};

@@ -302,6 +302,27 @@ def test_decode_more_heads_than_the_bulk_path_takes(nc, oracle_mod, window):
     assert abs_err(lse, lse_ref) <= LSE_TOL
 
 
+@pytest.mark.parametrize("N,H,D,window,Tmax", [(3, 16, 128, -1, 900), (5, 1, 64, 77, 640), (2, 7, 128, 300, 1000),
+                                                 (4, 16, 64, 129, 513)])
+def test_decode_bulk_chunk_shapes(nc, oracle_mod, N, H, D, window, Tmax):
+    """The bulk-copy split's chunk is as many whole cache rows (all heads) as fit a 24 KB stage, rounded to whole
+    batches of four steps: 6 rows at 16 heads of 128, 192 rows at one head of 64; lengths cover 1 and Tmax."""
+    wl = workloads.DecodeWorkload("bulk", N, Tmax, H, D, 1, Tmax, (window,), 818 + H + D)
+    q, kc, vc, lens = workloads.make_decode(wl, "cuda")
+    lens[0] = 1
+    lens[-1] = Tmax
+    dead = (torch.arange(wl.Tmax, device="cuda").view(1, -1) >= lens.view(-1, 1)).view(wl.N, wl.Tmax, 1, 1)
+    kc.masked_fill_(dead, float("nan"))
+    vc.masked_fill_(dead, float("nan"))
+    o, lse = nc.attn_decode(q, kc, vc, lens, window, wl.scale)
+    assert nc.nc_get_device_error() == 0
+    o_ref, lse_ref, ok = oracle_mod.decode(q.cpu(), kc.nan_to_num().cpu(), vc.nan_to_num().cpu(), lens.cpu(),
+                                           window, wl.scale)
+    assert ok
+    assert rel_err(o, o_ref) <= O_TOL
+    assert abs_err(lse, lse_ref) <= LSE_TOL
+
+
 def test_decode_equals_last_forward_row(nc):
     B, T, H, D, W = 2, 600, 2, 128, 256
     q, k, v, _ = workloads.make_qkvdo_shape(B, T, H, D, seed=31, device="cuda")
