@@ -49,8 +49,8 @@ TRAFFIC = {
                     "bytes": {1024: 167795968 + 118299648 + 506067712 + 284267520 + 167780608 + 47454464,
                               2048: 167794944 + 118450432 + 506056448 + 285178624 + 167776000 + 47024384}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
-                    "sha256": "264e22b2eb647ab4d81cb0471e0010ef79510029bdd88c0c09512535cd5da88c",
-                    "bytes": {1024: 600022528 + 61832448, 2048: 729701376 + 62256896}},
+                    "sha256": "5d02202722683e36718149b7695ba6fd568c94f7e4add2f51c143ce147b43bbf",
+                    "bytes": {1024: 602641664 + 62538240, 2048: 733189888 + 63022592}},
 }
 
 
