@@ -45,9 +45,9 @@ METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor pe
 # (sha256 of the .cu file); otherwise the bench reports null.
 TRAFFIC = {
     "nc_attn_bwd": {"src": "causal_sliding_window_fwd_b300/csrc/bwd_sm103.cu",
-                    "sha256": "c68e02afd975c8f64f805eebf7bb5a25b07870d5a58042fc85171a02dbc97551",
-                    "bytes": {1024: 167795968 + 118299648 + 506067712 + 284267520 + 167780608 + 47454464,
-                              2048: 167794944 + 118450432 + 506056448 + 285178624 + 167776000 + 47024384}},
+                    "sha256": "c86754a18d8e6b20625c8132cde82d2e3d2cae38ebc315c42f7f752d38b4bba3",
+                    "bytes": {1024: 167798528 + 118337792 + 506113792 + 284357888 + 167779584 + 45507584,
+                              2048: 167796992 + 118549248 + 506135808 + 285100288 + 167779328 + 46185472}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
                     "sha256": "5d02202722683e36718149b7695ba6fd568c94f7e4add2f51c143ce147b43bbf",
                     "bytes": {1024: 602641664 + 62538240, 2048: 733189888 + 63022592}},

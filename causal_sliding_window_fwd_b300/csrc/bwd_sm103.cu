@@ -17,8 +17,10 @@
 // bwd_dq_sm103.cu, instead of the accumulator.)
 //
 // bwd_main warp roles:
-//   warp 0      TMA producer: each item's V and K (V as soon as the previous item's last dP^T
-//               has read it, K after its last dQ), then Q and dO blocks (128-byte swizzle)
+//   warp 0      TMA producer: each item's K and V, then Q and dO blocks (128-byte swizzle).  The
+//               two K/V tiles swap roles from item to item, so an item's K loads as soon as the
+//               previous item's last dP^T has read that item's V, a block before its last dQ
+//               frees its K (the tile the V then goes to)
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns)
 //   warps 4-7   one thread per key row, query columns [0, 64): P^T and dS^T from S^T and
 //               dP^T; then the dK epilogue (staged in the dS tile)
@@ -80,10 +82,11 @@ struct BwdSmem {
 };
 
 struct BwdBarriers {
-    uint64_t k_full;
-    uint64_t k_empty;     // every product of the item that reads K (S^T, dQ) is done
-    uint64_t v_full;
-    uint64_t v_empty;     // the item's last dP^T (the only reader of V) is done
+    // K/V slots: tile s (s = 0 at kK, 1 at kV) holds K of the items of parity s and V of the others, so
+    // the next item's K goes into the tile whose V was freed by the item's last dP^T, a block before
+    // the item's K is freed by its last dQ.  Each slot is filled once per item.
+    uint64_t kv_full[2];
+    uint64_t kv_empty[2];  // the slot's K (last S^T and dQ) or V (last dP^T) reader is done
     uint64_t q_full[kQStages];
     uint64_t q_empty[kQStages];
     uint64_t do_full[2];
@@ -240,10 +243,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return;
     }
     if (threadIdx.x == 0) {
-        mbar_init(&bars->k_full, 1);
-        mbar_init(&bars->k_empty, 1);
-        mbar_init(&bars->v_full, 1);
-        mbar_init(&bars->v_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars->q_full[s], 1);
             mbar_init(&bars->q_empty[s], 1);
@@ -296,7 +299,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             __syncwarp();
             int gq = 0, gd = 0;  // Q and dO blocks loaded over all items (ring positions)
-            int kv_loads = 0, k_loads = 0;  // V and K loads issued
+            int fills[2] = {0, 0};  // loads issued into each K/V slot
             bool ok = true;
             for (int ii = 0; ok; ++ii) {
                 // varlen: pass over items past a document's end (and report bad document bounds)
@@ -309,26 +312,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (w < 0) break;
                 const BwdItem item = bwd_item<kVarlen>(w, p);
-                // V of this item once the previous item's last dP^T has read its V (a block before that
-                // item ends), then K once its last dQ has read its K
-                if (!mbar_wait_warp(&bars->v_empty, (ii & 1) ^ 1) || aborted(bars)) {
+                const int sk = ii & 1, sv = sk ^ 1;
+                // K into the slot whose V the previous item's last dP^T has read (a block before that item
+                // ends); V, after the first Q block, into the slot its last dQ frees
+                if (!mbar_wait_warp(&bars->kv_empty[sk], (ii & 1) ^ 1) || aborted(bars)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx_w(&bars->v_full, L::kTile);
+                mbar_arrive_expect_tx_w(&bars->kv_full[sk], L::kTile);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(smem + L::kV + c * kBK * 128, &tm_v, &bars->v_full, c * 64, item.h,
-                                  item.base + item.j0, item.b);
-                ++kv_loads;
-                if (!mbar_wait_warp(&bars->k_empty, (ii & 1) ^ 1) || aborted(bars)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx_w(&bars->k_full, L::kTile);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_w(smem + L::kK + c * kBK * 128, &tm_k, &bars->k_full, c * 64, item.h,
-                                  item.base + item.j0, item.b);
-                ++k_loads;
+                    tma_load_4d_w(smem + (sk ? L::kV : L::kK) + c * kBK * 128, &tm_k, &bars->kv_full[sk], c * 64,
+                                  item.h, item.base + item.j0, item.b);
+                ++fills[sk];
                 for (int it = 0; it < item.n_it; ++it) {
                     const int st = gq % kQStages, so = gd % L::kDOStages;
                     const int i0 = (item.m_lo + it) * kBQ;
@@ -341,6 +336,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tma_load_4d_w(smem + L::kQ + st * L::kTile + c * kBQ * 128, &tm_q, &bars->q_full[st], c * 64,
                                       item.h, item.base + i0, item.b);
                     ++gq;
+                    if (it == 0) {
+                        if (!mbar_wait_warp(&bars->kv_empty[sv], (ii & 1) ^ 1) || aborted(bars)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx_w(&bars->kv_full[sv], L::kTile);
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d_w(smem + (sv ? L::kV : L::kK) + c * kBK * 128, &tm_v, &bars->kv_full[sv],
+                                          c * 64, item.h, item.base + item.j0, item.b);
+                        ++fills[sv];
+                    }
                     // D = 128 with dQ: the previous item's dV epilogue stages its tile in the dO stage
                     if (L::kTmaReduce && !kNoDq && it == 0 && ii > 0 &&
                         (!mbar_wait_warp(&bars->do_epi_free, (ii - 1) & 1) || aborted(bars))) {
@@ -365,8 +371,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_wait_warp(&bars->q_full[x % kQStages], (x / kQStages) & 1);
             for (int x = gd - L::kDOStages < 0 ? 0 : gd - L::kDOStages; x < gd; ++x)
                 mbar_wait_warp(&bars->do_full[x % L::kDOStages], (x / L::kDOStages) & 1);
-            if (kv_loads > 0) mbar_wait_warp(&bars->v_full, (kv_loads - 1) & 1);
-            if (k_loads > 0) mbar_wait_warp(&bars->k_full, (k_loads - 1) & 1);
+            for (int s = 0; s < 2; ++s)
+                if (fills[s] > 0) mbar_wait_warp(&bars->kv_full[s], (fills[s] - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -377,14 +383,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             constexpr uint32_t id_kd = idesc_bf16(kBK, D, false, true);     // dV, dK (B MN-major)
             constexpr uint32_t id_qd = idesc_bf16(kBQ, D, true, true);      // dQ (A and B MN-major)
             constexpr uint32_t id_dqt = idesc_bf16(D, kBQ, true, true);     // dQ^T (A and B MN-major)
-            const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+            const uint32_t s_slot[2] = {smem_u32(smem + L::kK), smem_u32(smem + L::kV)};
             const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
             const uint32_t sDS = smem_u32(smem + L::kDS);
             // Descriptors are built once; each product adds a constant (bytes / 16) to the start field.
-            const uint64_t k_kmaj = sdesc(sK, 16, 1024), v_kmaj = sdesc(sV, 16, 1024);
+            uint64_t k_kmaj = sdesc(s_slot[0], 16, 1024), v_kmaj = sdesc(s_slot[1], 16, 1024);
             const uint64_t q_kmaj = sdesc(sQ, 16, 1024), do_kmaj = sdesc(sDO, 16, 1024);
             const uint64_t q_mn = sdesc(sQ, kBQ * 128, 1024), do_mn = sdesc(sDO, kBQ * 128, 1024);
-            const uint64_t ds_mn = sdesc(sDS, kBQ * 128, 1024), k_mn = sdesc(sK, kBK * 128, 1024);
+            const uint64_t ds_mn = sdesc(sDS, kBQ * 128, 1024);
+            uint64_t k_mn = sdesc(s_slot[0], kBK * 128, 1024);
             constexpr uint64_t kTileStep = L::kTile >> 4;
             constexpr uint64_t kChunk = (kBQ * 128) >> 4;
             auto issue_s = [&](int st) {  // S^T = K Q^T into ST
@@ -415,7 +422,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 if (w < 0) break;
                 const BwdItem item = bwd_item<kVarlen>(w, p);
-                ok = mbar_wait_warp(&bars->k_full, ii & 1) && !aborted(bars);
+                const int sk = ii & 1, sv = sk ^ 1;
+                k_kmaj = sdesc(s_slot[sk], 16, 1024);
+                v_kmaj = sdesc(s_slot[sv], 16, 1024);
+                k_mn = sdesc(s_slot[sk], kBK * 128, 1024);
+                ok = mbar_wait_warp(&bars->kv_full[sk], ii & 1) && !aborted(bars);
                 if (!ok) break;
                 {
                     // first block of the item: S^T, then dP^T once the previous block's dQ has left DPT
@@ -425,12 +436,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     issue_s(st);
                     ok = (kNoDq || gi == 0 || mbar_wait_warp(&bars->dq_empty, (gi - 1) & 1)) &&
-                         mbar_wait_warp(&bars->v_full, ii & 1) &&
+                         mbar_wait_warp(&bars->kv_full[sv], ii & 1) &&
                          mbar_wait_warp(&bars->do_full[so], (gi / L::kDOStages) & 1) && !aborted(bars);
                     if (!ok) break;
                     tc_fence_after();
                     issue_dp(so);
-                    if (item.n_it == 1) mma_commit_w(&bars->v_empty);  // the item's last dP^T is issued
+                    if (item.n_it == 1) mma_commit_w(&bars->kv_empty[sv]);  // the item's last dP^T is issued
                 }
                 for (int it = 0; it < item.n_it; ++it, ++gi) {
                     const int st = gi % kQStages, so = gi % L::kDOStages;
@@ -502,11 +513,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (!ok) break;
                         tc_fence_after();
                         issue_dp(so1);
-                        if (it + 2 == item.n_it) mma_commit_w(&bars->v_empty);  // the item's last dP^T is issued
+                        if (it + 2 == item.n_it) mma_commit_w(&bars->kv_empty[sv]);  // the item's last dP^T is issued
                     }
                 }
                 if (!ok) break;
-                mma_commit_w(&bars->k_empty);  // every product that reads this item's K is issued
+                mma_commit_w(&bars->kv_empty[sk]);  // every product that reads this item's K is issued
                 mma_commit_w(&bars->final_);    // DK and DV of this item are complete once these land
             }
             if (!ok) record_timeout(bars, p.err);
