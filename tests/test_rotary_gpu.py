@@ -1,10 +1,10 @@
-"""GPU parity of the rotary variants (rotary embedding of q and k fused into the attention kernels'
-load stage) against the fp64 oracle's rotary attention.
+"""GPU parity of the rotary entry points (q and k turned by one launch, then the attention; dq and dk
+turned back in the backward's conversion pass) and of the standalone turn, against the fp64 oracle.
 
 Tolerances as in test_parity_gpu: output <= 2e-2 max|ref|, lse <= 1e-3 absolute, gradients <= 3e-2
-max|ref| (per (b, h) slice at full size).  The kernels round the turned q and k to bf16 in shared memory
-before the products; the oracle turns the same bf16 inputs in fp64 and rounds the turned q and k to the
-nearest bf16 before its attention (the attention takes bf16 q and k in both).
+max|ref| (per (b, h) slice at full size).  The kernel turns q and k in float32 and rounds the turned rows to
+bf16; the oracle takes that quantisation the same way (float32 turn, then round to nearest even) and is fp64
+from there on, including its exact turn back of the gradients.
 """
 import math
 
@@ -147,3 +147,42 @@ def test_turned_rows_and_the_standalone_turn_agree(nc, oracle_mod):
     np.testing.assert_array_equal(qr.double().cpu().numpy(), oracle_mod.rotary_bf16(q.cpu(), c.cpu(), s.cpu()))
     o2, lse2 = nc.attn_fwd(qr, kr, v, W, 0.1)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_rotary_composes_with_packed_documents(nc, oracle_mod):
+    """Packed documents with each row turned by its position inside its document: the standalone turn with
+    per-row tables [total, D/2] (B = 1, T = total), the varlen forward and backward on the turned rows, and the
+    turn back of dq and dk.  The oracle composes its own turn, its per-document attention and its exact
+    transpose."""
+    lens = [130, 1, 257, 64, 300, 128]
+    H, D = 2, 128
+    total = sum(lens)
+    g = workloads.generator(4700, "cuda")
+    q, k, v, dO = (workloads.randn_bf16((total, H, D), g, "cuda") for _ in range(4))
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+    pos = torch.cat([torch.arange(n) for n in lens])
+    c_all, s_all = workloads.rope_tables(max(lens), D)
+    c, s = c_all[pos].contiguous().cuda(), s_all[pos].contiguous().cuda()
+    scale = 1.0 / math.sqrt(D)
+    for window in (-1, 100):
+        qr = nc.rotary(q.unsqueeze(0), c, s)[0]
+        kr = nc.rotary(k.unsqueeze(0), c, s)[0]
+        o, lse = nc.attn_fwd_varlen(qr, kr, v, cu, max(lens), window, scale)
+        dqr, dkr, dv = nc.attn_bwd_varlen(qr, kr, v, o, dO, lse, cu, max(lens), window, scale)
+        dq = nc.rotary(dqr.unsqueeze(0), c, s, inverse=True)[0]
+        dk = nc.rotary(dkr.unsqueeze(0), c, s, inverse=True)[0]
+        assert nc.nc_get_device_error() == 0
+        cc, ss = c.cpu(), s.cpu()
+        qr_o = oracle_mod.rotary_bf16(q.cpu().unsqueeze(0), cc, ss)
+        kr_o = oracle_mod.rotary_bf16(k.cpu().unsqueeze(0), cc, ss)
+        # the turned rows are a quantisation decided in float32: bit-exact
+        assert np.array_equal(qr.float().cpu().numpy(), qr_o[0]) and np.array_equal(kr.float().cpu().numpy(), kr_o[0])
+        vv, gg = v.cpu().unsqueeze(0), dO.cpu().unsqueeze(0)
+        o_r, lse_r = oracle_mod.fwd_varlen(qr_o, kr_o, vv, cu.cpu(), window, scale)
+        dqr_r, dkr_r, dv_r = oracle_mod.bwd_varlen(qr_o, kr_o, vv, gg, cu.cpu(), window, scale)
+        dq_r = oracle_mod.rotary(dqr_r, cc, ss, inverse=True)
+        dk_r = oracle_mod.rotary(dkr_r, cc, ss, inverse=True)
+        assert rel_err(o, o_r[0]) <= O_TOL
+        assert abs_err(lse, lse_r[0]) <= LSE_TOL
+        for got, ref in ((dq, dq_r[0]), (dk, dk_r[0]), (dv, dv_r[0])):
+            assert rel_err(got, ref) <= G_TOL
