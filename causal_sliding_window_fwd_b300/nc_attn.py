@@ -421,3 +421,80 @@ def attn_decode(q, kcache, vcache, cache_lens, window: int, scale: float | None 
     lse = torch.empty((N, H), dtype=torch.float32, device=q.device) if with_lse else None
     nc_attn_decode(q, kcache, vcache, cache_lens, o, lse, window, scale, workspace, stream)
     return o, lse
+
+
+# ---------------------------------------------------------------- autograd nodes (training)
+# Each node calls the library's forward, keeps what its backward call needs, and calls that backward:
+# no arithmetic here.  Non-contiguous inputs (views of a fused projection) are copied to contiguous ones,
+# since the kernels take dense [B, T, H, D] rows.
+
+
+class _SlidingWindowAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, window: int, scale: float, deterministic: bool):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o, lse = attn_fwd(q, k, v, window, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.window, ctx.scale, ctx.deterministic = window, scale, deterministic
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, dO.contiguous(), lse, ctx.window, ctx.scale,
+                              deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None
+
+
+class _VarlenAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, window, scale)
+        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
+        ctx.max_seqlen, ctx.window, ctx.scale = max_seqlen, window, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, o, lse, cu = ctx.saved_tensors
+        dq, dk, dv = attn_bwd_varlen(q, k, v, o, dO.contiguous(), lse, cu, ctx.max_seqlen, ctx.window, ctx.scale)
+        return dq, dk, dv, None, None, None, None
+
+
+class _RotaryAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, rope_cos, rope_sin, window: int, scale: float):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        o, lse, qr, kr = attn_fwd_rotary(q, k, v, rope_cos, rope_sin, window, scale)
+        ctx.save_for_backward(qr, kr, v, rope_cos, rope_sin, o, lse)
+        ctx.window, ctx.scale = window, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        qr, kr, v, c, s, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd_rotary(qr, kr, v, c, s, o, dO.contiguous(), lse, ctx.window, ctx.scale)
+        return dq, dk, dv, None, None, None, None
+
+
+def sliding_window_attention(q, k, v, window: int, scale: float | None = None, deterministic: bool = False):
+    """o for bf16 q, k, v [B, T, H, D] (D = 64 or 128), with a backward for autograd: causal attention in
+    which each query sees its own position and the window - 1 before it (window <= 0: full causal).
+    ``deterministic`` selects the bitwise-reproducible backward."""
+    scale = default_scale(q.shape[-1]) if scale is None else scale
+    return _SlidingWindowAttention.apply(q, k, v, int(window), float(scale), bool(deterministic))
+
+
+def varlen_attention(q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None):
+    """o for packed documents q, k, v [total, H, D] (document d is rows cu_seqlens[d] .. cu_seqlens[d+1]-1,
+    each attending only within itself), with a backward for autograd."""
+    scale = default_scale(q.shape[-1]) if scale is None else scale
+    return _VarlenAttention.apply(q, k, v, cu_seqlens, int(max_seqlen), int(window), float(scale))
+
+
+def rotary_attention(q, k, v, rope_cos, rope_sin, window: int, scale: float | None = None):
+    """o for q and k turned by the rotary tables (fp32 [T, D/2]) before the attention, with a backward for
+    autograd whose q and k gradients are with respect to the unturned q and k."""
+    scale = default_scale(q.shape[-1]) if scale is None else scale
+    return _RotaryAttention.apply(q, k, v, rope_cos, rope_sin, int(window), float(scale))
