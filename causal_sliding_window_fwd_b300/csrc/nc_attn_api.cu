@@ -207,6 +207,27 @@ nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache,
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
+nc_status nc_kv_append(const void* k_new, const void* v_new, void* kcache, void* vcache, const int* cache_lens,
+                       int N, int Tq, int Tmax, int H, int D, cudaStream_t stream) {
+    nc_status st = check_shape(N, Tmax, H, D, NC_WINDOW_FULL, 1.f);
+    if (st != NC_OK) return st;
+    if (Tq <= 0 || Tq > Tmax) return NC_ERR_INVALID;
+    if (!k_new || !v_new || !kcache || !vcache || !cache_lens) return NC_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kcache) || !aligned16(vcache)) return NC_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID;
+    const size_t nn = (size_t)N * Tq * H * D * 2, nc_ = (size_t)N * Tmax * H * D * 2;
+    // the caches are written: neither may overlap an input or the other cache
+    const void* ins[3] = {k_new, v_new, cache_lens};
+    const size_t in_n[3] = {nn, nn, (size_t)N * 4};
+    for (int i = 0; i < 3; ++i)
+        if (overlap(ins[i], in_n[i], kcache, nc_) || overlap(ins[i], in_n[i], vcache, nc_)) return NC_ERR_INVALID;
+    if (overlap(kcache, nc_, vcache, nc_)) return NC_ERR_INVALID;
+    int* err = error_word();
+    if (err == nullptr) return NC_ERR_CUDA;
+    const cudaError_t e = nc::launch_kv_append(k_new, v_new, kcache, vcache, cache_lens, N, Tq, Tmax, H, D, err, stream);
+    return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
 size_t nc_attn_bwd_workspace_bytes(int B, int T, int H, int D) {
     if (B <= 0 || T <= 0 || H <= 0 || D <= 0) return 0;
     return round_up((size_t)B * T * H * D * 4, 256) + round_up((size_t)B * H * T * 4, 256) + 256;

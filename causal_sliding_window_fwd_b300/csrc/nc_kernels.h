@@ -48,6 +48,11 @@ cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache
                            float* lse, int N, int Tq, int Tmax, int H, int D, int window, float scale, int* err,
                            cudaStream_t st);
 
+// KV-cache append: kcache/vcache [N,Tmax,H,D] rows L_n - Tq .. L_n - 1 from k_new/v_new [N,Tq,H,D] bf16,
+// lens device int32 [N] (each counting the new rows).
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* kcache, void* vcache, const int* lens, int N,
+                             int Tq, int Tmax, int H, int D, int* err, cudaStream_t st);
+
 // Backward: dq_acc fp32 [B,T,H,D], delta fp32 [B,H,T] and the work-item counter are workspace.
 cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                        void* dq, void* dk, void* dv, int B, int T, int H, int D, int window, float scale,

@@ -34,7 +34,8 @@ EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "n
             "nc_attn_bwd_varlen", "nc_attn_fwd_rotary", "nc_attn_bwd_rotary", "nc_rotary",
             "nc_get_device_error",
             "nc_launch_count",
-            "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest")
+            "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest",
+            "nc_kv_append")
 
 # Size of the library's fixed decode scratch array (NC_DECODE_NOALLOC_SCRATCH_BYTES).
 NC_DECODE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -68,6 +69,8 @@ def _load():
     lib.nc_attn_decode.restype = i
     lib.nc_attn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.nc_attn_prefill.restype = i
+    lib.nc_kv_append.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.nc_kv_append.restype = i
     lib.nc_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.nc_attn_fwd_varlen.restype = i
     lib.nc_attn_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
@@ -327,6 +330,20 @@ def nc_attn_prefill(q, kcache, vcache, cache_lens, o, lse, window: int, scale: f
     _check(lib.nc_attn_prefill(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(o), _ptr(lse),
                                N, Tq, Tmax, H, D, int(window), float(scale), _stream(q.device, stream)),
            "nc_attn_prefill")
+
+
+def nc_kv_append(k_new, v_new, kcache, vcache, cache_lens, stream=None) -> None:
+    """Writes the new rows k_new, v_new [N,Tq,H,D] bf16 into the caches [N,Tmax,H,D] at positions
+    cache_lens[n] - Tq .. cache_lens[n] - 1 (the lengths count the new tokens, as prefill and decode take them)."""
+    N, Tmax, H, D = kcache.shape
+    Tq = k_new.shape[1]
+    _need(k_new, "k_new", torch.bfloat16, (N, Tq, H, D))
+    _need(v_new, "v_new", torch.bfloat16, (N, Tq, H, D))
+    _need(kcache, "kcache", torch.bfloat16)
+    _need(vcache, "vcache", torch.bfloat16, (N, Tmax, H, D))
+    _need(cache_lens, "cache_lens", torch.int32, (N,))
+    _check(lib.nc_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(cache_lens),
+                            N, Tq, Tmax, H, D, _stream(kcache.device, stream)), "nc_kv_append")
 
 
 def nc_attn_decode_noalloc_scratch_bytes(N: int, Tmax: int, H: int, D: int, window: int) -> int:

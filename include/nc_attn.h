@@ -213,6 +213,28 @@ nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache,
                           cudaStream_t stream);
 
 /*
+ * Append of new tokens' keys and values to the KV cache ("nanochat"
+ * walkthrough, page 4: the Engine's KV cache, filled by prefill and extended
+ * by every decode step).  cache_lens[n] = L already counts the Tq new tokens,
+ * as nc_attn_prefill and nc_attn_decode take it, so new row t is written to
+ * cache position L - Tq + t:
+ *   kcache[n, L - Tq + t] = k_new[n, t],  vcache[n, L - Tq + t] = v_new[n, t].
+ * Run it before nc_attn_prefill (or nc_attn_decode, Tq = 1) with the same
+ * lengths.  Other cache rows are not touched.
+ *   k_new, v_new : const bf16 [N, Tq, H, D] device, 16-byte aligned
+ *   kcache       : bf16 [N, Tmax, H, D] device, written (rows L - Tq .. L - 1)
+ *   vcache       : bf16 [N, Tmax, H, D] device, written likewise
+ *   cache_lens   : const int32 [N] device, each in [Tq, Tmax]; a value
+ *                  outside that range sets NC_ERR_BAD_CACHE_LEN on the device
+ *                  and leaves that sequence's rows unwritten
+ * NC_ERR_INVALID for null or misaligned pointers, Tq outside [1, Tmax], or
+ * caches overlapping each other or an input; NC_ERR_UNSUPPORTED for D other
+ * than 64 or 128.  One launch, no workspace.
+ */
+nc_status nc_kv_append(const void* k_new, const void* v_new, void* kcache, void* vcache, const int* cache_lens,
+                       int N, int Tq, int Tmax, int H, int D, cudaStream_t stream);
+
+/*
  * Attention over rotary-embedded q and k ("nanochat" walkthrough, page 4,
  * comment thread: the model is Llama-like; the pages give no formula, and the
  * rotate-half pairing of Llama is the reading taken).  Each query and key row

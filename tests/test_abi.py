@@ -352,3 +352,31 @@ def test_rotary_entries_reject_bad_arguments(lib):
     assert _rot(lib, p) == lib.NC_ERR_INVALID
     p = list(A[:4]); p[3] = p[1]             # y over the cosine table
     assert _rot(lib, p) == lib.NC_ERR_INVALID
+
+
+def _append(lib, ptrs=None, N=2, Tq=4, Tmax=64, H=2, D=64):
+    p = list(A[:5]) if ptrs is None else ptrs
+    return lib.lib.nc_kv_append(*[ctypes.c_void_p(x) for x in p], N, Tq, Tmax, H, D, None)
+
+
+@host_only
+def test_kv_append_rejects_bad_arguments(lib):
+    # k_new v_new kcache vcache cache_lens
+    assert _append(lib, D=96) == lib.NC_ERR_UNSUPPORTED
+    assert _append(lib, N=0) == lib.NC_ERR_INVALID
+    assert _append(lib, Tq=0) == lib.NC_ERR_INVALID
+    assert _append(lib, Tq=65) == lib.NC_ERR_INVALID
+    for i in range(5):
+        p = list(A[:5]); p[i] = 0
+        assert _append(lib, p) == lib.NC_ERR_INVALID
+    for i in range(4):
+        p = list(A[:5]); p[i] += 8           # rows must be 16-byte aligned
+        assert _append(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[4] += 2               # lengths must be 4-byte aligned
+    assert _append(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[3] = p[2] + 256       # vcache overlapping kcache
+    assert _append(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[2] = p[0]             # kcache over k_new
+    assert _append(lib, p) == lib.NC_ERR_INVALID
+    p = list(A[:5]); p[3] = p[4] - 64        # vcache over the lengths
+    assert _append(lib, p) == lib.NC_ERR_INVALID
