@@ -729,6 +729,28 @@ def run_prefill(dev, stream, nc_attn, peaks, peak_kind):
                     "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                                  "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}
+    # the append that precedes a prefill: the new tokens' keys and values into the caches (an HBM copy of
+    # N*Tq rows of k and of v), timed last since it rewrites the cache rows the prefill calls above read
+    k_new, v_new = q, o
+    nbytes = 4 * k_new.numel() * k_new.element_size()  # read k_new, v_new; write as much into the caches
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            nc_attn.nc_kv_append(k_new, v_new, kc, vc, lens, stream)
+        evs = []
+        for _ in range(20):
+            flush.fill_(1)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            nc_attn.nc_kv_append(k_new, v_new, kc, vc, lens, stream)
+            e.record(stream)
+            evs.append((s, e))
+        torch.cuda.synchronize()
+    ms = statistics.median([s.elapsed_time(e) for s, e in evs])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["append"] = {"us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                  "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                  "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None}}
     assert nc_attn.nc_get_device_error(stream) == 0
     return res
 
