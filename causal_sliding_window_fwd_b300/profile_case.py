@@ -24,7 +24,7 @@ from causal_sliding_window_fwd_b300 import nc_attn, workloads
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["fwd", "bwd", "bwd_det", "decode", "prefill", "varlen_fwd", "varlen_bwd",
-                                     "rope_fwd", "rope_bwd"], default="fwd")
+                                     "rope_fwd", "rope_bwd", "append"], default="fwd")
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--H", type=int, default=10)
@@ -50,6 +50,13 @@ def main():
         lse = torch.empty((wl.N, wl.H, wl.Tq), dtype=torch.float32, device=dev)
         for _ in range(a.iters):
             nc_attn.nc_attn_prefill(q, kc, vc, lens, o, lse, a.window, wl.scale)
+    elif a.op == "append":
+        # the prefill workload's new tokens' keys and values into its caches
+        wl = workloads.PREFILL
+        q, kc, vc, lens = workloads.make_prefill(wl, dev)
+        v_new = torch.empty_like(q).copy_(q)
+        for _ in range(a.iters):
+            nc_attn.nc_kv_append(q, v_new, kc, vc, lens)
     elif a.op in ("varlen_fwd", "varlen_bwd"):
         wl = workloads.VARLEN
         q, k, v, dO, cu, max_len = workloads.make_varlen(wl, dev)
