@@ -112,6 +112,7 @@ nc_status nc_rotary(const void* x, const float* rope_cos, const float* rope_sin,
                     int D, int inverse, cudaStream_t stream) {
     if (B < 1 || T < 1 || H < 1) return NC_ERR_INVALID;
     if (D != 64 && D != 128) return NC_ERR_UNSUPPORTED;
+    if ((int64_t)B * T * H >= (int64_t(1) << 31)) return NC_ERR_UNSUPPORTED;
     if (!x || !rope_cos || !rope_sin || !y) return NC_ERR_INVALID;
     if (!aligned16(x) || !aligned16(rope_cos) || !aligned16(rope_sin) || !aligned16(y)) return NC_ERR_INVALID;
     const size_t nb = (size_t)B * T * H * D * 2, nt = (size_t)T * (D / 2) * 4;

@@ -50,9 +50,11 @@ __global__ void __launch_bounds__(256) rotary_kernel(const uint4* x0, uint4* y0,
     const uint4* x = blockIdx.y ? x1 : x0;
     uint4* y = blockIdx.y ? y1 : y0;
     for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < n_units; w += (size_t)gridDim.x * blockDim.x) {
-        const size_t row = w / kUnits;
+        const size_t row = w / kUnits;  // a shift
         const int u = static_cast<int>(w - row * kUnits);
-        const int pos = static_cast<int>((row / H) % T);
+        // B * T * H < 2^31 (checked by every entry point), so the position comes from 32-bit divisions
+        const uint32_t row32 = static_cast<uint32_t>(row);
+        const int pos = static_cast<int>((row32 / static_cast<uint32_t>(H)) % static_cast<uint32_t>(T));
         const size_t i1 = row * kRowVec + u, i2 = i1 + kUnits;  // dimensions 8u .. 8u+7 and their partners
         float a[8], b[8], c[8], s[8];
         unpack_bf16x8(x[i1], a);

@@ -282,8 +282,9 @@ nc_status nc_attn_bwd_rotary(const void* qr, const void* kr, const void* v, cons
  *   y                  : bf16 [B, T, H, D] device, written; either x itself
  *                        (in place) or a range that does not overlap x
  * D is 64 or 128.  Errors: NC_ERR_INVALID for a null or unaligned pointer, a
- * partial overlap, or B, T, H < 1; NC_ERR_UNSUPPORTED for another D;
- * NC_ERR_CUDA if the launch fails.  One kernel launch, asynchronous.
+ * partial overlap, or B, T, H < 1; NC_ERR_UNSUPPORTED for another D or for
+ * B * T * H >= 2^31; NC_ERR_CUDA if the launch fails.  One kernel launch,
+ * asynchronous.
  */
 nc_status nc_rotary(const void* x, const float* rope_cos, const float* rope_sin, void* y, int B, int T,
                     int H, int D, int inverse, cudaStream_t stream);

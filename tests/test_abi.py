@@ -343,6 +343,7 @@ def test_rotary_entries_reject_bad_arguments(lib):
     # the standalone turn: x cos sin y
     assert _rot(lib, D=96) == lib.NC_ERR_UNSUPPORTED
     assert _rot(lib, B=0) == lib.NC_ERR_INVALID
+    assert _rot(lib, B=1 << 16, T=1 << 15, H=1) == lib.NC_ERR_UNSUPPORTED   # B * T * H = 2^31 rows
     for i in range(4):
         p = list(A[:4]); p[i] = 0
         assert _rot(lib, p) == lib.NC_ERR_INVALID
