@@ -186,3 +186,25 @@ def test_rotary_composes_with_packed_documents(nc, oracle_mod):
         assert abs_err(lse, lse_r[0]) <= LSE_TOL
         for got, ref in ((dq, dq_r[0]), (dk, dk_r[0]), (dv, dv_r[0])):
             assert rel_err(got, ref) <= G_TOL
+
+
+def test_rotary_composes_with_the_deterministic_backward(nc):
+    """Rotary q and k with a bitwise-reproducible backward: the deterministic backward on the turned rows, then
+    the turn back of dq and dk.  Two runs are bitwise equal, and the result agrees with the fused rotary
+    backward (which adds dQ with fp32 atomics) to its atomic-order noise."""
+    B, T, H, D, W = 2, 520, 2, 128, 200
+    q, k, v, dO = workloads.make_qkvdo_shape(B, T, H, D, seed=4800, device="cuda")
+    c, s = workloads.rope_tables(T, D, device="cuda")
+    o, lse, qr, kr = nc.attn_fwd_rotary(q, k, v, c, s, W)
+    runs = []
+    for _ in range(2):
+        dqr, dkr, dv = nc.attn_bwd(qr, kr, v, o, dO, lse, W, deterministic=True)
+        runs.append((nc.rotary(dqr, c, s, inverse=True), nc.rotary(dkr, c, s, inverse=True), dv))
+    assert all(torch.equal(a, b) for a, b in zip(*runs))
+    dq_f, dk_f, dv_f = nc.attn_bwd_rotary(qr, kr, v, c, s, o, dO, lse, W)
+    dq, dk, dv = runs[0]
+    assert torch.equal(dv, dv_f)
+    for got, ref in ((dq, dq_f), (dk, dk_f)):
+        err = (got.float() - ref.float()).abs().max().item()
+        assert err <= 1e-2 * ref.float().abs().max().item()
+    assert nc.nc_get_device_error() == 0
