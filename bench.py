@@ -580,6 +580,8 @@ def run_varlen(dev, stream, nc_attn, peaks, peak_kind):
         fwd_ms = timed(lambda: nc_attn.nc_attn_fwd_varlen(q, k, v, cu, o, lse, max_len, window, wl.scale, stream))
         bwd_ms = timed(lambda: nc_attn.nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu, dq, dk, dv, max_len, window,
                                                           wl.scale, ws, stream))
+        det_ms = timed(lambda: nc_attn.nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu, dq, dk, dv, max_len, window,
+                                                          wl.scale, ws, stream, deterministic=True))
         pairs = wl.H * sum(workloads.pairs_in_window(L, window) for L in lens)
         fwd_tf = 4.0 * wl.D * pairs / (fwd_ms * 1e-3) / 1e12
         bwd_tf = 10.0 * wl.D * pairs / (bwd_ms * 1e-3) / 1e12
@@ -588,6 +590,8 @@ def run_varlen(dev, stream, nc_attn, peaks, peak_kind):
         res[key] = {"window": window, "fwd_us": round(fwd_ms * 1e3, 2), "bwd_us": round(bwd_ms * 1e3, 2),
                     "fwd_TFLOP_s": round(fwd_tf, 1), "bwd_TFLOP_s": round(bwd_tf, 1),
                     "TFLOP_s": round(step_tf, 1),
+                    "deterministic_bwd_us": round(det_ms * 1e3, 2),
+                    "deterministic_bwd_useful_TFLOP_s": round(10.0 * wl.D * pairs / (det_ms * 1e-3) / 1e12, 1),
                     "roofline": {"bound": "tensor", "achieved": round(step_tf, 1), "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": round(step_tf / peaks["bf16_tflops"], 4),
                                  "peak_kind": f"{peak_kind} bf16 dense (burst)", "traffic": None}}

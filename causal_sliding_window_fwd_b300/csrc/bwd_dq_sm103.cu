@@ -10,7 +10,8 @@
 //
 // Persistent CTAs (one per SM, 384 threads).  A work item is one query block m of one
 // (batch, head); the producer warp takes item indices from a global counter and publishes them
-// in a shared-memory ring.  Indices run over groups of about one wave of items; inside a group
+// in a shared-memory ring.  Packed documents (kVarlen): the pairs are (document, head), positions
+// count from the document's first row, and the producer passes over items past a document's end.  Indices run over groups of about one wave of items; inside a group
 // m runs outermost from the last block down (the longest causal walks first), so the CTAs that
 // run at the same time read the K and V of a few heads and share them in L2.  Warp roles:
 //   warp 0      TMA producer: Q and dO of the item once, then K blocks through a 3-slot ring and V
@@ -88,23 +89,45 @@ struct DqParams {
     bool dq32;           // dq is 32-byte aligned: the epilogue writes whole 32-byte sectors
     int* work;           // work-item counter, zero on entry
     int* err;
+    // packed documents (B = 1, T = total): document d is rows cu[d] .. cu[d+1]-1; n_qb counts the query
+    // blocks of the longest document.  nullptr otherwise.
+    const int* cu;
+    int n_docs;
 };
 
-// One item: query block m of one (batch, head) and the key blocks n_lo .. m that its window reaches.
+// One item: query block m of one (batch, head) -- or (document, head) -- and the key blocks n_lo .. m
+// that its window reaches.
 struct DqItem {
     int m, h, b, n_lo;
+    int base;    // first packed row of the document, else 0
+    int len;     // rows of the sequence or document
+    bool bad;    // the document's bounds are out of range
+    bool empty;  // the block lies past the document's end (or the document is bad)
 };
 
+template <bool kVarlen>
 __device__ __forceinline__ DqItem dq_item(int w, const DqParams& p) {
     DqItem it;
-    const int n_pairs = p.B * p.H;
+    const int n_pairs = (kVarlen ? p.n_docs : p.B) * p.H;
     const int per_group = p.n_qb * p.group;
     const int grp = w / per_group, r = w - grp * per_group;
     const int in_grp = min(p.group, n_pairs - grp * p.group);  // the last group may be short
     const int bh = grp * p.group + r % in_grp;
     it.m = p.n_qb - 1 - r / in_grp;
     it.h = bh % p.H;
-    it.b = bh / p.H;
+    it.b = kVarlen ? 0 : bh / p.H;
+    it.base = 0;
+    it.len = p.T;
+    it.bad = false;
+    it.empty = false;
+    if (kVarlen) {
+        const int d = bh / p.H;
+        const int a = p.cu[d], e = p.cu[d + 1];
+        it.bad = a < 0 || e < a || e > p.T || e - a > p.n_qb * kBQ;
+        it.base = it.bad ? 0 : a;
+        it.len = it.bad ? 0 : e - a;
+        it.empty = it.bad || it.m * kBQ >= it.len;
+    }
     // the earliest key any row of the block sees is m*128 - W + 1; key block n holds one of
     // those keys iff n*128 + 127 >= m*128 - W + 1
     const int x = it.m * kBQ - p.W - (kBK - 2);
@@ -121,7 +144,33 @@ __device__ __forceinline__ void record_timeout(DqBarriers& bars, int* err) {
     atomicExch(&bars.abort, 1);
 }
 
-template <int D>
+// Producer (converged warp): the next item index into ring slot k; with packed documents, indices of empty
+// items are passed over (and bad document bounds reported) so the other roles only see items with work.
+// -1 once every item is taken, -2 if the wait for the slot ran out.
+template <bool kVarlen>
+__device__ __forceinline__ int publish_dq_item(DqBarriers& bars, int k, int n_items, const DqParams& p) {
+    if (!kVarlen) return ring_publish_item(bars.item_full, bars.item_empty, bars.item, k, n_items, p.work);
+    const int slot = k % kItemSlots;
+    if (!mbar_wait_warp(&bars.item_empty[slot], ((k / kItemSlots) & 1) ^ 1)) return -2;
+    int w = 0;
+    if (lane_id() == 0) {
+        for (;;) {
+            w = atomicAdd(p.work, 1);
+            if (w >= n_items) {
+                w = -1;
+                break;
+            }
+            const DqItem it = dq_item<kVarlen>(w, p);
+            if (it.bad) set_device_error(p.err, NC_ERR_BAD_SEQLENS);
+            if (!it.empty) break;
+        }
+        bars.item[slot] = w;
+        mbar_arrive(&bars.item_full[slot]);
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+}
+
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const DqParams p) {
@@ -129,7 +178,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ DqBarriers bars;
     const int warp = warp_id(), lane = lane_id();
-    const int n_items = p.n_qb * p.H * p.B;
+    const int n_items = p.n_qb * p.H * (kVarlen ? p.n_docs : p.B);
 
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (threadIdx.x == 0) set_device_error(p.err, NC_ERR_CUDA);
@@ -188,13 +237,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int seq = 0, q_loads = 0, k_loads = 0, v_loads = 0;
         bool ok = true;
         for (int ii = 0; ok; ++ii) {
-            const int w = ring_publish_item(bars.item_full, bars.item_empty, bars.item, ii, n_items, p.work);
+            const int w = publish_dq_item<kVarlen>(bars, ii, n_items, p);
             if (w == -2 || aborted(bars)) {
                 ok = false;
                 break;
             }
             if (w < 0) break;
-            const DqItem it = dq_item(w, p);
+            const DqItem it = dq_item<kVarlen>(w, p);
             // Q and dO of this item once the previous item's S and dP products have read theirs
             if (!mbar_wait_warp(&bars.q_empty, (ii & 1) ^ 1) || aborted(bars)) {
                 ok = false;
@@ -202,8 +251,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             mbar_arrive_expect_tx_w(&bars.q_full, 2 * L::kTile);
             for (int c = 0; c < D / 64; ++c) {
-                tma_load_4d_w(smem + L::kQ + c * kBQ * 128, &tm_q, &bars.q_full, c * 64, it.h, it.m * kBQ, it.b);
-                tma_load_4d_w(smem + L::kDO + c * kBQ * 128, &tm_do, &bars.q_full, c * 64, it.h, it.m * kBQ, it.b);
+                tma_load_4d_w(smem + L::kQ + c * kBQ * 128, &tm_q, &bars.q_full, c * 64, it.h,
+                              it.base + it.m * kBQ, it.b);
+                tma_load_4d_w(smem + L::kDO + c * kBQ * 128, &tm_do, &bars.q_full, c * 64, it.h,
+                              it.base + it.m * kBQ, it.b);
             }
             ++q_loads;
             for (int n = it.n_lo; n <= it.m; ++n, ++seq) {
@@ -215,7 +266,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mbar_arrive_expect_tx_w(&bars.k_full[ks], L::kTile);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_4d_w(smem + L::kK + ks * L::kTile + c * kBK * 128, &tm_k, &bars.k_full[ks], c * 64, it.h,
-                                  n * kBK, it.b);
+                                  it.base + n * kBK, it.b);
                 ++k_loads;
                 if (!mbar_wait_warp(&bars.v_empty[vs], ((seq / kVStages) & 1) ^ 1) || aborted(bars)) {
                     ok = false;
@@ -224,7 +275,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mbar_arrive_expect_tx_w(&bars.v_full[vs], L::kTile);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_4d_w(smem + L::kV + vs * L::kTile + c * kBK * 128, &tm_v, &bars.v_full[vs], c * 64, it.h,
-                                  n * kBK, it.b);
+                                  it.base + n * kBK, it.b);
                 ++v_loads;
             }
         }
@@ -284,7 +335,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 break;
             }
             if (w < 0) break;
-            const DqItem it = dq_item(w, p);
+            const DqItem it = dq_item<kVarlen>(w, p);
             ok = mbar_wait_warp(&bars.q_full, ii & 1) && issue_s_dp(seq, gj);
             if (!ok) break;
             if (it.n_lo == it.m) mma_commit_w(&bars.q_empty);  // every S and dP of this item is issued
@@ -341,12 +392,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // row.  It runs after the next item's first dS, so the MMA warp has that block's S and dP products to
         // run meanwhile; dq_free then lets the next item's first dQ product overwrite DQ.
         auto epilogue = [&](const DqItem& item, int ie) -> bool {
-            const int i = item.m * kBQ + tid;
-            const bool row_ok = i < p.T;
+            const int i = item.m * kBQ + tid;  // row within the sequence or document
+            const bool row_ok = i < item.len;  // (a document's last block: the next document's rows are left alone)
             if (!(mbar_wait_warp(&bars.dq_final, ie & 1) && !aborted(bars))) return false;
             tc_fence_after();
             __nv_bfloat16* drow =
-                p.dq + ((static_cast<size_t>(item.b) * p.T + (row_ok ? i : 0)) * p.H + item.h) * D + g * (D / 2);
+                p.dq + ((static_cast<size_t>(item.b) * p.T + item.base + (row_ok ? i : 0)) * p.H + item.h) * D +
+                g * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
@@ -383,10 +435,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 break;
             }
             if (w < 0) break;
-            const DqItem item = dq_item(w, p);
-            const int i = item.m * kBQ + tid;  // this thread's query row
-            const bool row_ok = i < p.T;
-            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T;
+            const DqItem item = dq_item<kVarlen>(w, p);
+            const int i = item.m * kBQ + tid;  // this thread's query row (within the sequence or document)
+            const bool row_ok = i < item.len;
+            const size_t rowvec = (static_cast<size_t>(item.b) * p.H + item.h) * p.T + item.base;
             // past the last row: lse = inf, so P = 0 and dS = 0
             const float lse_l2 = row_ok ? p.lse[rowvec + i] * kLog2e : INFINITY;
             const float dlt = row_ok ? p.delta[rowvec + i] : 0.f;
@@ -466,10 +518,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D>
+template <int D, bool kVarlen>
 cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                          const float* delta, void* dq, int B, int T, int H, int window, float scale, int* work,
-                         int* err, cudaStream_t st) {
+                         const int* cu, int n_docs, int max_len, int* err, cudaStream_t st) {
     CUtensorMap tq, tk, tv, tdo;
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ))
@@ -484,26 +536,28 @@ cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void
     p.W = (window <= 0 || window >= T) ? T : window;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
-    p.n_qb = (T + kBQ - 1) / kBQ;
+    p.n_qb = ((kVarlen ? max_len : T) + kBQ - 1) / kBQ;
     p.work = work;
     p.err = err;
+    p.cu = cu;
+    p.n_docs = n_docs;
     p.dq32 = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     const int smem = DqSmem<D>::kBytes;
     // the shared-memory limit is raised once per device (atomic flags), the SM count is looked up
     // on every call
     static std::atomic<bool> attr_done[kAttrDevices];
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel<D>), smem, attr_done);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel<D, kVarlen>), smem, attr_done);
     if (e != cudaSuccess) return e;
     int n_sm = 0;
     e = multiprocessor_count(&n_sm);
     if (e != cudaSuccess) return e;
-    const int n_pairs = B * H;
+    const int n_pairs = (kVarlen ? n_docs : B) * H;
     const long n_items = (long)p.n_qb * n_pairs;
     const int grid = (int)(n_items < n_sm ? n_items : n_sm);
     // a scheduling group holds about one wave of items
     p.group = (n_sm + p.n_qb - 1) / p.n_qb;
     if (p.group > n_pairs) p.group = n_pairs;
-    bwd_dq_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, p);
+    bwd_dq_kernel<D, kVarlen><<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, p);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -512,9 +566,16 @@ cudaError_t launch_dq_tc(const void* q, const void* k, const void* v, const void
 
 cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                           const float* delta, void* dq, int B, int T, int H, int D, int window, float scale, int* work,
-                          int* err, cudaStream_t st) {
-    return D == 128 ? launch_dq_tc<128>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, err, st)
-                    : launch_dq_tc<64>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, err, st);
+                          int* err, cudaStream_t st, const int* cu, int n_docs, int max_len) {
+    if (cu != nullptr)
+        return D == 128 ? launch_dq_tc<128, true>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, cu,
+                                                  n_docs, max_len, err, st)
+                        : launch_dq_tc<64, true>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, cu,
+                                                 n_docs, max_len, err, st);
+    return D == 128 ? launch_dq_tc<128, false>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, nullptr, 0,
+                                               0, err, st)
+                    : launch_dq_tc<64, false>(q, k, v, dO, lse, delta, dq, B, T, H, window, scale, work, nullptr, 0,
+                                              0, err, st);
 }
 
 }  // namespace nc

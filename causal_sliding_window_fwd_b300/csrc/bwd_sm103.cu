@@ -872,13 +872,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // Delta = rowsum(dO * O) per (b, h, i), a zeroed dQ accumulator (unless dq_acc is null) and zeroed
-// work-item counters (work[0] for the main kernel, work[1] for the deterministic dQ pass).
+// work-item counters (work[0] for the main kernel, work[1] for the deterministic dQ pass).  Packed documents
+// with the deterministic dQ pass (cu != nullptr): dq rows outside [cu[0], cu[n_docs]) are zeroed here, since
+// that pass writes only the documents' rows.
 // D / 8 lanes per row, each with one 16-byte load of O and of dO.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                      int* __restrict__ work, int B, int T, int H) {
+                                                      int* __restrict__ work, int B, int T, int H,
+                                                      __nv_bfloat16* __restrict__ dq, const int* __restrict__ cu,
+                                                      int n_docs) {
     constexpr int G = D / 8;          // lanes per row
     constexpr int RPW = 32 / G;       // rows per warp
     const long tid_g = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -905,6 +909,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    }
+    if (cu != nullptr && row < rows) {
+        const long i = row / H;  // B = 1
+        if (i < __ldg(cu) || i >= __ldg(cu + n_docs))
+            reinterpret_cast<uint4*>(dq + (size_t)row * D)[c] = make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -1007,7 +1016,8 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     const long pre_threads = ((rows * (D / 8) + 31) / 32) * 32;
     bwd_pre_kernel<D><<<(unsigned)((pre_threads + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), delta,
-        deterministic ? nullptr : dq_acc, work, B, T, H);
+        deterministic ? nullptr : dq_acc, work, B, T, H, static_cast<__nv_bfloat16*>(dq),
+        deterministic ? cu : nullptr, n_docs);
     BwdParams p;
     p.lse = lse;
     p.delta = delta;
@@ -1029,10 +1039,11 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     const int smem = BwdSmem<D>::kBytes;
     // the shared-memory limit is raised once per device and variant (atomic flags), the SM count
     // is looked up on every call
-    static std::atomic<bool> attr_done[3][kAttrDevices];
-    const int variant = deterministic ? 2 : (cu != nullptr ? 1 : 0);
-    auto kern = variant == 2 ? bwd_main_kernel<D, false, true>
-                             : (variant == 1 ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
+    static std::atomic<bool> attr_done[4][kAttrDevices];
+    const int variant = deterministic ? (cu != nullptr ? 3 : 2) : (cu != nullptr ? 1 : 0);
+    auto kern = variant == 3   ? bwd_main_kernel<D, true, true>
+                : variant == 2 ? bwd_main_kernel<D, false, true>
+                               : (variant == 1 ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>);
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, attr_done[variant]);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (its shared memory and TMEM allow one), looping over the items
@@ -1050,7 +1061,8 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
         count_launches(2);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        return launch_bwd_dq(q, k, v, dO, lse, delta, dq, B, T, H, D, window, scale, work + 1, err, st);
+        return launch_bwd_dq(q, k, v, dO, lse, delta, dq, B, T, H, D, window, scale, work + 1, err, st, cu, n_docs,
+                             max_len);
     }
     if (rcos != nullptr) {
         const size_t nu = (size_t)rows * (D / 16);
@@ -1080,11 +1092,11 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
 cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, const int* cu, int n_docs, int max_len, void* dq, void* dk, void* dv,
                               int total, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
-                              int* err, cudaStream_t st) {
+                              int* err, cudaStream_t st, bool deterministic) {
     return D == 128 ? launch_bwd_tc<128>(q, k, v, o, dO, lse, dq, dk, dv, 1, total, H, window, scale, dq_acc, delta,
-                                         work, cu, n_docs, max_len, err, st)
+                                         work, cu, n_docs, max_len, err, st, deterministic)
                     : launch_bwd_tc<64>(q, k, v, o, dO, lse, dq, dk, dv, 1, total, H, window, scale, dq_acc, delta,
-                                        work, cu, n_docs, max_len, err, st);
+                                        work, cu, n_docs, max_len, err, st, deterministic);
 }
 
 cudaError_t launch_bwd_rotary(const void* qr, const void* kr, const void* v, const float* rcos, const float* rsin,

@@ -145,10 +145,10 @@ nc_status nc_attn_fwd_varlen(const void* q, const void* k, const void* v, const 
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
-nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                             const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv, int n_docs,
-                             int total, int max_seqlen, int H, int D, int window, float scale, void* workspace,
-                             size_t workspace_bytes, cudaStream_t stream) {
+static nc_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                 const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv, int n_docs,
+                                 int total, int max_seqlen, int H, int D, int window, float scale, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream, bool deterministic) {
     nc_status st = check_shape(1, total, H, D, window, scale);
     if (st != NC_OK) return st;
     if (n_docs <= 0 || max_seqlen <= 0 || max_seqlen > total) return NC_ERR_INVALID;
@@ -181,8 +181,26 @@ nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
     ws += round_up((size_t)H * total * 4, 256);
     int* work = reinterpret_cast<int*>(ws);
     const cudaError_t e = nc::launch_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, n_docs, max_seqlen, dq, dk, dv,
-                                                total, H, D, window, scale, dq_acc, delta, work, err, stream);
+                                                total, H, D, window, scale, dq_acc, delta, work, err, stream,
+                                                deterministic);
     return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv, int n_docs,
+                             int total, int max_seqlen, int H, int D, int window, float scale, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    return attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, n_docs, total, max_seqlen, H, D, window, scale,
+                           workspace, workspace_bytes, stream, false);
+}
+
+nc_status nc_attn_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                           const float* lse, const int* cu_seqlens, void* dq, void* dk, void* dv,
+                                           int n_docs, int total, int max_seqlen, int H, int D, int window,
+                                           float scale, void* workspace, size_t workspace_bytes,
+                                           cudaStream_t stream) {
+    return attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, n_docs, total, max_seqlen, H, D, window, scale,
+                           workspace, workspace_bytes, stream, true);
 }
 
 nc_status nc_attn_prefill(const void* q, const void* kcache, const void* vcache, const int* cache_lens, void* o,

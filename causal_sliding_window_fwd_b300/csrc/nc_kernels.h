@@ -38,10 +38,11 @@ cudaError_t launch_fwd_varlen(const void* q, const void* k, const void* v, const
                               cudaStream_t st);
 
 // Document-masked backward over packed rows; workspace as for launch_bwd with B = 1, T = total.
+// deterministic: dK and dV from the main kernel without its dQ product, dq from the query-stationary pass.
 cudaError_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, const int* cu, int n_docs, int max_len, void* dq, void* dk, void* dv,
                               int total, int H, int D, int window, float scale, float* dq_acc, float* delta, int* work,
-                              int* err, cudaStream_t st);
+                              int* err, cudaStream_t st, bool deterministic = false);
 
 // Prefill over a KV cache: q/o [N,Tq,H,D] bf16, lse [N,H,Tq] fp32, caches [N,Tmax,H,D], lens device int32 [N].
 cudaError_t launch_prefill(const void* q, const void* kcache, const void* vcache, const int* lens, void* o,
@@ -73,9 +74,10 @@ cudaError_t launch_bwd_deterministic(const void* q, const void* k, const void* v
                                      cudaStream_t st);
 
 // Query-stationary dQ pass: dq [B,T,H,D] bf16 from q, k, v, dO, lse and delta [B,H,T] fp32.
-// `work` is a work-item counter that must be zero when the kernel starts.
+// `work` is a work-item counter that must be zero when the kernel starts.  cu != nullptr: packed documents
+// (B = 1, T = total, cu device int32 [n_docs+1], max_len the longest document).
 cudaError_t launch_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                           const float* delta, void* dq, int B, int T, int H, int D, int window, float scale, int* work,
-                          int* err, cudaStream_t st);
+                          int* err, cudaStream_t st, const int* cu = nullptr, int n_docs = 0, int max_len = 0);
 
 }  // namespace nc

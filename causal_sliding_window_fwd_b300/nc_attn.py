@@ -35,7 +35,7 @@ EXPORTED = ("nc_status_string", "nc_attn_fwd", "nc_attn_bwd_workspace_bytes", "n
             "nc_get_device_error",
             "nc_launch_count",
             "nc_attn_decode_noalloc_scratch_bytes", "nc_attn_decode_noalloc", "nc_debug_watchdog_selftest",
-            "nc_kv_append")
+            "nc_kv_append", "nc_attn_bwd_varlen_deterministic")
 
 # Size of the library's fixed decode scratch array (NC_DECODE_NOALLOC_SCRATCH_BYTES).
 NC_DECODE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -75,6 +75,8 @@ def _load():
     lib.nc_attn_fwd_varlen.restype = i
     lib.nc_attn_bwd_varlen.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
     lib.nc_attn_bwd_varlen.restype = i
+    lib.nc_attn_bwd_varlen_deterministic.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp, sz, vp]
+    lib.nc_attn_bwd_varlen_deterministic.restype = i
     lib.nc_attn_fwd_rotary.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp]
     lib.nc_attn_fwd_rotary.restype = i
     lib.nc_attn_bwd_rotary.argtypes = [vp] * 11 + [i, i, i, i, i, f, vp, sz, vp]
@@ -280,8 +282,9 @@ def nc_attn_fwd_varlen(q, k, v, cu_seqlens, o, lse, max_seqlen: int, window: int
 
 
 def nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen: int, window: int, scale: float,
-                       workspace, stream=None) -> None:
-    """Backward of the document-masked forward into caller-owned dq, dk, dv [total,H,D]."""
+                       workspace, stream=None, deterministic: bool = False) -> None:
+    """Backward of the document-masked forward into caller-owned dq, dk, dv [total,H,D]; ``deterministic``
+    calls nc_attn_bwd_varlen_deterministic (bitwise-reproducible)."""
     total, H, D = q.shape
     n_docs = cu_seqlens.shape[0] - 1
     for name, x in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dq", dq), ("dk", dk), ("dv", dv)):
@@ -289,21 +292,30 @@ def nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen: 
     _need(lse, "lse", torch.float32, (H, total))
     _need(cu_seqlens, "cu_seqlens", torch.int32, (n_docs + 1,))
     _need(workspace, "workspace", torch.uint8)
-    _check(lib.nc_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(cu_seqlens),
-                                  _ptr(dq), _ptr(dk), _ptr(dv), n_docs, total, int(max_seqlen), H, D, int(window),
-                                  float(scale), _ptr(workspace), workspace.numel(), _stream(q.device, stream)),
-           "nc_attn_bwd_varlen")
+    fn, name = ((lib.nc_attn_bwd_varlen_deterministic, "nc_attn_bwd_varlen_deterministic") if deterministic
+                else (lib.nc_attn_bwd_varlen, "nc_attn_bwd_varlen"))
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(cu_seqlens), _ptr(dq), _ptr(dk), _ptr(dv),
+              n_docs, total, int(max_seqlen), H, D, int(window), float(scale), _ptr(workspace), workspace.numel(),
+              _stream(q.device, stream)), name)
+
+
+def nc_attn_bwd_varlen_deterministic(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen: int, window: int,
+                                     scale: float, workspace, stream=None) -> None:
+    """The bitwise-reproducible backward of the document-masked forward."""
+    nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen, window, scale, workspace, stream,
+                       deterministic=True)
 
 
 def attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None,
-                    workspace=None, stream=None):
-    """Returns (dq, dk, dv), each [total,H,D] bf16."""
+                    workspace=None, stream=None, deterministic: bool = False):
+    """Returns (dq, dk, dv), each [total,H,D] bf16; ``deterministic`` selects the bitwise-reproducible backward."""
     total, H, D = q.shape
     scale = default_scale(D) if scale is None else scale
     if workspace is None:
         workspace = torch.empty(nc_attn_bwd_workspace_bytes(1, total, H, D), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen, window, scale, workspace, stream)
+    nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, dq, dk, dv, max_seqlen, window, scale, workspace, stream,
+                       deterministic)
     return dq, dk, dv
 
 
@@ -465,18 +477,19 @@ class _SlidingWindowAttention(torch.autograd.Function):
 
 class _VarlenAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float):
+    def forward(ctx, q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float, deterministic: bool):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, window, scale)
         ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
-        ctx.max_seqlen, ctx.window, ctx.scale = max_seqlen, window, scale
+        ctx.max_seqlen, ctx.window, ctx.scale, ctx.deterministic = max_seqlen, window, scale, deterministic
         return o
 
     @staticmethod
     def backward(ctx, dO):
         q, k, v, o, lse, cu = ctx.saved_tensors
-        dq, dk, dv = attn_bwd_varlen(q, k, v, o, dO.contiguous(), lse, cu, ctx.max_seqlen, ctx.window, ctx.scale)
-        return dq, dk, dv, None, None, None, None
+        dq, dk, dv = attn_bwd_varlen(q, k, v, o, dO.contiguous(), lse, cu, ctx.max_seqlen, ctx.window, ctx.scale,
+                                     deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None, None, None
 
 
 class _RotaryAttention(torch.autograd.Function):
@@ -503,11 +516,12 @@ def sliding_window_attention(q, k, v, window: int, scale: float | None = None, d
     return _SlidingWindowAttention.apply(q, k, v, int(window), float(scale), bool(deterministic))
 
 
-def varlen_attention(q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None):
+def varlen_attention(q, k, v, cu_seqlens, max_seqlen: int, window: int, scale: float | None = None,
+                     deterministic: bool = False):
     """o for packed documents q, k, v [total, H, D] (document d is rows cu_seqlens[d] .. cu_seqlens[d+1]-1,
-    each attending only within itself), with a backward for autograd."""
+    each attending only within itself), with a backward for autograd (``deterministic``: bitwise-reproducible)."""
     scale = default_scale(q.shape[-1]) if scale is None else scale
-    return _VarlenAttention.apply(q, k, v, cu_seqlens, int(max_seqlen), int(window), float(scale))
+    return _VarlenAttention.apply(q, k, v, cu_seqlens, int(max_seqlen), int(window), float(scale), bool(deterministic))
 
 
 def rotary_attention(q, k, v, rope_cos, rope_sin, window: int, scale: float | None = None):

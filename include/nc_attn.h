@@ -185,6 +185,20 @@ nc_status nc_attn_bwd_varlen(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Deterministic form of nc_attn_bwd_varlen: the same gradients, arguments,
+ * layouts, workspace and errors, but dq, dk and dv are bitwise identical from
+ * run to run (as nc_attn_bwd_deterministic for packed rows: dK and dV from the
+ * main kernel, dq from a pass in which one CTA owns each 128-row query block
+ * of a document and sums its key blocks in a fixed order).  Rows that belong
+ * to no document get dq = 0.
+ */
+nc_status nc_attn_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                           const void* dO, const float* lse, const int* cu_seqlens, void* dq,
+                                           void* dk, void* dv, int n_docs, int total, int max_seqlen, int H,
+                                           int D, int window, float scale, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Prefill (append) over a KV cache: Tq new tokens per sequence attend over the
  * cache ("nanochat" walkthrough, page 4: the Engine's prefill/decode split
  * over a KV cache).  The keys and values of the new tokens are already in the

@@ -211,16 +211,17 @@ def test_fwd_varlen_rejects_bad_arguments(lib):
 
 
 @host_only
-def test_bwd_varlen_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("entry", ["nc_attn_bwd_varlen", "nc_attn_bwd_varlen_deterministic"])
+def test_bwd_varlen_rejects_bad_arguments(lib, entry):
     def call(ptrs=None, ws_bytes=None, **kw):
         a = dict(n_docs=3, total=512, max_seqlen=300, H=2, D=128, window=64, scale=0.1)
         a.update(kw)
         p = list(A[:10]) if ptrs is None else ptrs
         need = lib.nc_attn_bwd_workspace_bytes(1, a["total"], a["H"], a["D"])
-        return lib.lib.nc_attn_bwd_varlen(*[ctypes.c_void_p(x) if x is not None else None for x in p],
-                                          a["n_docs"], a["total"], a["max_seqlen"], a["H"], a["D"], a["window"],
-                                          ctypes.c_float(a["scale"]), ctypes.c_void_p(A[11]),
-                                          need if ws_bytes is None else ws_bytes, None)
+        return getattr(lib.lib, entry)(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                                       a["n_docs"], a["total"], a["max_seqlen"], a["H"], a["D"], a["window"],
+                                       ctypes.c_float(a["scale"]), ctypes.c_void_p(A[11]),
+                                       need if ws_bytes is None else ws_bytes, None)
     assert call(n_docs=0) == lib.NC_ERR_INVALID
     assert call(max_seqlen=600) == lib.NC_ERR_INVALID
     assert call(D=80) == lib.NC_ERR_UNSUPPORTED

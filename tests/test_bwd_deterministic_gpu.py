@@ -128,3 +128,68 @@ def test_deterministic_full_size(nc, oracle_mod, wl_name, call_idx):
         g = sel(g).float().cpu()
         for i, (b, h) in enumerate(picks):
             assert rel_err(g[i], r[i]) <= G_TOL, (name, b, h)
+
+
+# ---------------------------------------------------------------- packed documents
+
+
+def varlen_inputs(lens, H, D, seed, total=None):
+    total = sum(lens) if total is None else total
+    g = workloads.generator(seed, "cuda")
+    q, k, v, dO = (workloads.randn_bf16((total, H, D), g, "cuda") for _ in range(4))
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+    return q, k, v, dO, cu
+
+
+def varlen_backward(nc, q, k, v, o, dO, lse, cu, max_len, window, scale, deterministic, fill=0xFF):
+    total, H, D = q.shape
+    ws = torch.full((nc.nc_attn_bwd_workspace_bytes(1, total, H, D),), fill, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    nc.nc_attn_bwd_varlen(q, k, v, o, dO, lse, cu, dq, dk, dv, max_len, window, scale, ws,
+                          deterministic=deterministic)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("lens,H,D,window", [
+    ([130, 1, 257, 64, 300], 2, 128, -1), ([130, 1, 257, 64, 300], 2, 128, 100), ([1000, 24, 512], 3, 64, 200),
+    ([5, 3], 1, 128, 1), ([640], 2, 128, 256),
+])
+def test_varlen_deterministic_matches_oracle_and_repeats(nc, oracle_mod, lens, H, D, window):
+    q, k, v, dO, cu = varlen_inputs(lens, H, D, 7600 + sum(lens) + D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = nc.attn_fwd_varlen(q, k, v, cu, max(lens), window, scale)
+    runs = [varlen_backward(nc, q, k, v, o, dO, lse, cu, max(lens), window, scale, True, fill) for fill in (0xFF, 0x00)]
+    assert nc.nc_get_device_error() == 0
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
+    dq, dk, dv = runs[0]
+    pq, pk, pv = varlen_backward(nc, q, k, v, o, dO, lse, cu, max(lens), window, scale, False)
+    assert torch.equal(dk, pk) and torch.equal(dv, pv)
+    refs = oracle_mod.bwd_varlen(q.unsqueeze(0).cpu(), k.unsqueeze(0).cpu(), v.unsqueeze(0).cpu(),
+                                 dO.unsqueeze(0).cpu(), cu.cpu(), window, scale)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        assert rel_err(got, ref[0]) <= G_TOL, name
+
+
+def test_varlen_deterministic_rows_outside_documents(nc):
+    """Rows past the last document: dq is zero (as from nc_attn_bwd_varlen), dk and dv are not written."""
+    lens, total, H, D = [100, 200], 400, 2, 128
+    q, k, v, dO, cu = varlen_inputs(lens, H, D, 7700, total=total)
+    o, lse = nc.attn_fwd_varlen(q, k, v, cu, 200, 64)
+    dq, dk, dv = varlen_backward(nc, q, k, v, o, dO, lse, cu, 200, 64, 1.0 / math.sqrt(D), True)
+    assert nc.nc_get_device_error() == 0
+    assert (dq[300:].float() == 0).all()
+    assert torch.isnan(dk[300:].float()).all() and torch.isnan(dv[300:].float()).all()
+    pq, pk, pv = varlen_backward(nc, q, k, v, o, dO, lse, cu, 200, 64, 1.0 / math.sqrt(D), False)
+    assert torch.equal(dk[:300], pk[:300]) and torch.equal(dv[:300], pv[:300])
+    assert (pq[300:].float() == 0).all()
+
+
+def test_varlen_deterministic_bad_document_reports(nc):
+    lens = [100, 400, 50]  # the middle document is longer than max_seqlen below
+    q, k, v, dO, cu = varlen_inputs(lens, 2, 128, 7800)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((2, sum(lens)), dtype=torch.float32, device="cuda")
+    varlen_backward(nc, q, k, v, o, dO, lse, cu, 256, -1, 0.1, True)
+    assert nc.nc_get_device_error() == nc.NC_ERR_BAD_SEQLENS
+    assert nc.nc_get_device_error() == 0
