@@ -45,9 +45,9 @@ METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor pe
 # (sha256 of the .cu file); otherwise the bench reports null.
 TRAFFIC = {
     "nc_attn_bwd": {"src": "causal_sliding_window_fwd_b300/csrc/bwd_sm103.cu",
-                    "sha256": "c86754a18d8e6b20625c8132cde82d2e3d2cae38ebc315c42f7f752d38b4bba3",
-                    "bytes": {1024: 167798528 + 118337792 + 506113792 + 284357888 + 167779584 + 45507584,
-                              2048: 167796992 + 118549248 + 506135808 + 285100288 + 167779328 + 46185472}},
+                    "sha256": "13fff9ad1c6c8ec634ed1086a8e3a0ac4a4f185bcfbb9582eceba0b9dc782805",
+                    "bytes": {1024: 167795712 + 118148096 + 506127104 + 284383232 + 167780608 + 45846016,
+                              2048: 167798016 + 118627072 + 506454528 + 285092864 + 167780608 + 46832384}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
                     "sha256": "5d02202722683e36718149b7695ba6fd568c94f7e4add2f51c143ce147b43bbf",
                     "bytes": {1024: 602641664 + 62538240, 2048: 733189888 + 63022592}},
