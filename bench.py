@@ -45,9 +45,9 @@ METRIC = "sliding-window causal attn fwd+bwd TFLOP/s (bf16), % of B300 tensor pe
 # (sha256 of the .cu file); otherwise the bench reports null.
 TRAFFIC = {
     "nc_attn_bwd": {"src": "causal_sliding_window_fwd_b300/csrc/bwd_sm103.cu",
-                    "sha256": "13fff9ad1c6c8ec634ed1086a8e3a0ac4a4f185bcfbb9582eceba0b9dc782805",
-                    "bytes": {1024: 167795712 + 118148096 + 506127104 + 284383232 + 167780608 + 45846016,
-                              2048: 167798016 + 118627072 + 506454528 + 285092864 + 167780608 + 46832384}},
+                    "sha256": "5e188d4cfd69a5c717de18074d4d80a120d5a2f885d5afe2584086106fc3e13b",
+                    "bytes": {1024: 167795968 + 118603776 + 506095872 + 284486656 + 167778560 + 47483904,
+                              2048: 167795200 + 118697728 + 506144512 + 285011456 + 167781632 + 46414336}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
                     "sha256": "5d02202722683e36718149b7695ba6fd568c94f7e4add2f51c143ce147b43bbf",
                     "bytes": {1024: 602641664 + 62538240, 2048: 733189888 + 63022592}},

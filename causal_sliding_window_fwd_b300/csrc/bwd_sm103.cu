@@ -26,9 +26,10 @@
 //               dP^T; then the dK epilogue (staged in the dS tile)
 //   warps 8-11  the same for query columns [64, 128); then the dV epilogue (staged in the
 //               dO stage for D = 128, in the second half of the dS tile for D = 64)
-//   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator: for D = 128
-//               the product is dQ^T (one thread per dQ column), staged in shared memory and
-//               added by TMA reduce-adds; for D = 64 one thread per row, vector atomics
+//   warps 12-15 the block's dQ partial from TMEM into the fp32 accumulator by TMA reduce-adds
+//               from a shared-memory staging tile: for D = 128 the product is dQ^T (one thread
+//               per dQ column, staged a 64-row half at a time); for D = 64 it is dQ (one thread
+//               per query row, the whole block in the 128-byte swizzle of two 32-column boxes)
 // TMEM: ST [0,128) holds S^T, then P^T (bf16, two per column) in columns
 //       [0,32) for queries 0-63 and [64,96) for queries 64-127, so each
 //       warpgroup overwrites only columns it has already read.  DPT [128,256)
@@ -60,12 +61,16 @@ constexpr int kItemReaders = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // D = 128: dQ partials leave through a TMA reduce-add from a 64-row fp32 staging tile,
-// which takes the place of the second dO stage.  D = 64: vector atomics, two dO stages.
+// which takes the place of the second dO stage.  D = 64: two dO stages and a 128-row staging
+// tile (two swizzled 32-column boxes).
 template <int D>
 struct BwdSmem {
     static constexpr bool kTmaReduce = (D == 128);
+    // D = 64: the block's dQ (thread = query row) leaves through a 128-row fp32 staging tile in the 128-byte
+    // swizzle of two 32-column TMA boxes, added by TMA reduce-adds
+    static constexpr bool kStagedRows = (D == 64);
     static constexpr int kDOStages = kTmaReduce ? 1 : 2;
-    static constexpr int kStageRows = 64;                 // dQ rows per reduce-add
+    static constexpr int kStageRows = 64;                 // dQ rows per reduce-add (D = 128)
     static constexpr int kTile = kBQ * D * 2;            // 128 rows x D bf16
     static constexpr int kK = 0;
     static constexpr int kV = kK + kTile;
@@ -74,7 +79,7 @@ struct BwdSmem {
     static constexpr int kDS = kDO + kDOStages * kTile;   // dS [key][query], 128 x 128 bf16
     static constexpr int kDSBytes = kBK * kBQ * 2;
     static constexpr int kStage = kDS + kDSBytes;         // fp32 [kStageRows][D] (D = 128 only)
-    static constexpr int kStageBytes = kTmaReduce ? kStageRows * D * 4 : 0;
+    static constexpr int kStageBytes = kTmaReduce ? kStageRows * D * 4 : (kStagedRows ? kBQ * D * 4 : 0);
     static constexpr int kLse = kStage + kStageBytes;     // [2][128] fp32 (log2 units)
     static constexpr int kDelta = kLse + 2 * kBQ * 4;     // [2][128] fp32
     static constexpr int kBars = kDelta + 2 * kBQ * 4;
@@ -215,11 +220,6 @@ __device__ __forceinline__ int read_item(BwdBarriers* bars, int k) {
 __device__ __forceinline__ void record_timeout(BwdBarriers* bars, int* err) {
     set_device_error(err, NC_ERR_DEVICE_TIMEOUT);
     atomicExch(&bars->abort, 1);
-}
-
-__device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
 }
 
 // kNoDq: dK and dV only (the deterministic backward computes dQ in a separate pass).
@@ -782,7 +782,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int tid = threadIdx.x - 384;
         const int lane_base = 32 * (warp % 4);
         const uint32_t st_addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + kColDPT;  // dQ lives in DPT
-        const size_t row_stride = static_cast<size_t>(p.H) * D;
         bool ok = true;
         int gi = 0;  // query blocks processed over all items
         for (int ii = 0; ok; ++ii) {
@@ -833,9 +832,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 } else {
                     // thread = query row, TMEM columns = the D dQ columns
-                    const int i = i0 + tid;
-                    float* dst =
-                        p.dq_acc + (static_cast<size_t>(b) * p.T + base + i) * row_stride + static_cast<size_t>(h) * D;
                     uint32_t r[64];
                     {
                         uint32_t a[32], c2[32];
@@ -848,16 +844,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                     tc_fence_before();
                     mbar_arrive(&bars->dq_empty);
-                    if (i < item.len) {
+                    // the block's 128 rows into the staging tile (box c: columns 32c .. 32c+31, 128 bytes a row, its
+                    // 16-byte units in the 128-byte swizzle), then one reduce-add per box.  Rows past a varlen
+                    // document's end carry exact zeros (P = 0 there); rows past the tensor are clipped by the copy.
+                    uint8_t* stage = smem + L::kStage;
+                    if (tid == 0) bulk_wait_read();  // the previous reduce-adds have read the staging tile
+                    named_bar_sync(3, 128);
 #pragma unroll
-                        for (int v4 = 0; v4 < 16; ++v4)
-                            red_add_f32x4(dst + 4 * v4, __uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                                          __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<uint4*>(stage + c * (kBQ * 128) + tid * 128 + ((u ^ (tid & 7)) << 4)) =
+                                make_uint4(r[32 * c + 4 * u], r[32 * c + 4 * u + 1], r[32 * c + 4 * u + 2],
+                                           r[32 * c + 4 * u + 3]);
+                    fence_async_smem();
+                    named_bar_sync(3, 128);
+                    if (tid == 0) {
+                        for (int c = 0; c < 2; ++c) tma_reduce_add_4d(&tm_dq, stage + c * (kBQ * 128), 32 * c, h, base + i0, b);
+                        bulk_commit();
                     }
                 }
             }
         }
-        if constexpr (L::kTmaReduce) {
+        if constexpr (L::kTmaReduce || L::kStagedRows) {
             if (tid == 0) bulk_wait_all();  // every reduce-add has landed before the CTA exits
         }
         }
@@ -1010,7 +1019,8 @@ cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const voi
     if (!make_tmap_bthd(&tq, q, B, T, H, D, 64, kBQ) || !make_tmap_bthd(&tk, k, B, T, H, D, 64, kBK) ||
         !make_tmap_bthd(&tv, v, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdo, dO, B, T, H, D, 64, kBQ) ||
         !make_tmap_bthd(&tdk, dk, B, T, H, D, 64, kBK) || !make_tmap_bthd(&tdv, dv, B, T, H, D, 64, kBK) ||
-        !make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, D, BwdSmem<D>::kStageRows))
+        !(D == 128 ? make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, D, BwdSmem<D>::kStageRows)
+                   : make_tmap_bthd_f32(&tdq, dq_acc, B, T, H, D, 32, kBQ, true)))
         return cudaErrorInvalidValue;
     const long rows = (long)B * T * H;
     const long pre_threads = ((rows * (D / 8) + 31) / 32) * 32;

@@ -39,8 +39,9 @@ inline bool make_tmap_bthd(CUtensorMap* map, const void* base, int B, int T, int
 }
 
 // View a contiguous fp32 [B, T, H, D] tensor as {D, H, T, B} with a {box_d, 1, box_t, 1}
-// box and no swizzle (used as the target of TMA reduce-adds).
-inline bool make_tmap_bthd_f32(CUtensorMap* map, const void* base, int B, int T, int H, int D, int box_d, int box_t) {
+// box (used as the target of TMA reduce-adds): no swizzle, or the 128-byte swizzle for a 32-float box.
+inline bool make_tmap_bthd_f32(CUtensorMap* map, const void* base, int B, int T, int H, int D, int box_d, int box_t,
+                               bool swizzle128 = false) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -48,8 +49,8 @@ inline bool make_tmap_bthd_f32(CUtensorMap* map, const void* base, int B, int T,
     const cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_t, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
