@@ -49,8 +49,8 @@ TRAFFIC = {
                     "bytes": {1024: 167795968 + 118603776 + 506095872 + 284486656 + 167778560 + 47483904,
                               2048: 167795200 + 118697728 + 506144512 + 285011456 + 167781632 + 46414336}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
-                    "sha256": "5d02202722683e36718149b7695ba6fd568c94f7e4add2f51c143ce147b43bbf",
-                    "bytes": {1024: 602641664 + 62538240, 2048: 733189888 + 63022592}},
+                    "sha256": "00a72f7e8f3d42c9032636f162a95c37070066ec11f43d0a5373610137dbc4be",
+                    "bytes": {1024: 607711232 + 60981504, 2048: 730025984 + 61417984}},
 }
 
 

@@ -586,9 +586,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     mx0 = max3f(mx0, sv[kBN - 4], sv[kBN - 3]);
                     mx1 = max3f(mx1, sv[kBN - 2], sv[kBN - 1]);
                     const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-                    if (first) {
-                        m_run = m_cand;
-                    } else if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleThreshold)) {
+                    // a row that has seen no visible key yet (its window starts past the first block) still
+                    // has l = 0 and an exactly zero O row: it takes this block's maximum as is, like a
+                    // first block, rather than asking for a rescale of O
+                    const bool fresh = first || m_run == -INFINITY;
+                    const bool grow = !fresh && m_cand > m_run + kRescaleThreshold;
+                    if (fresh) m_run = m_cand;
+                    if (__any_sync(0xffffffffu, grow)) {
                         const float m_new = fmaxf(m_run, m_cand);
                         const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
                         m_run = m_new;
