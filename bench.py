@@ -159,7 +159,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu_index), "-lms", "200"],
+                                          "-i", str(self.gpu_index), "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -172,7 +172,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
@@ -183,12 +183,22 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                power.append(float("nan"))
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        # samples under load: power draw at least half the highest seen (the sampler also runs through a short
+        # idle lead-in before the timed region)
+        finite = [w for w in power if w == w]
+        top = max(finite) if finite else 0.0
+        loaded = [f for f, w in zip(sm, power) if w == w and top > 0 and w >= 0.5 * top]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "samples_under_load": len(loaded),
+                "power_w_max": top if finite else None, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
