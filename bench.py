@@ -49,7 +49,7 @@ TRAFFIC = {
                     "bytes": {1024: 167795968 + 118603776 + 506095872 + 284486656 + 167778560 + 47483904,
                               2048: 167795200 + 118697728 + 506144512 + 285011456 + 167781632 + 46414336}},
     "nc_attn_fwd": {"src": "causal_sliding_window_fwd_b300/csrc/fwd_sm103.cu",
-                    "sha256": "00a72f7e8f3d42c9032636f162a95c37070066ec11f43d0a5373610137dbc4be",
+                    "sha256": "05ed65579b2a10eb4dba455921189e3b1021e474c8778623f500e159072476af",
                     "bytes": {1024: 607711232 + 60981504, 2048: 730025984 + 61417984}},
 }
 

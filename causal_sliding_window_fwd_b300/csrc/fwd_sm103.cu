@@ -24,7 +24,8 @@
 //   S0(j+1) after PV0(j), S1(j+1) after PV1(j)
 // lets one tile's softmax overlap the other tile's products.  The running
 // maximum is only raised (and O rescaled in TMEM) when it grows by more
-// than 2^8, which keeps every exponent bounded and the sum exact.
+// than 2^8, which keeps every exponent bounded and the sum exact; a row that
+// has seen no visible key yet simply takes the next block's maximum.
 #include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
